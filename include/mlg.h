@@ -1,0 +1,280 @@
+/*
+ * mlg.h -- C ABI of libmlg, the GB300 (sm_103a) MoE expert LoRA fold.
+ *
+ * The fold, for every row it covers:
+ *
+ *     base_out[row] += scale_e * (x[x_row] @ A_e^T) @ B_e^T
+ *
+ * with A_e [max_rank, k_in] and B_e [n_out, max_rank] the LoRA pair of expert
+ * e.  Source: the "metrale" documentation pages -- the module index of
+ * metrale_model_layers::layers::ops::moe_lora_grouped (items
+ * moe_lora_gather_bgmv, moe_lora_grouped_down, MoeExpertRoute,
+ * pack_expert_tables, grouped_down_windows, grouped_down_wc,
+ * gather_row_token, MLG_M_TILE and the module invariant on zero table cells)
+ * and the source page moe_row_adapter.rs (resolve_moe_lora_route,
+ * ensure_decode_route_servable, build_moe_row_adapter_host,
+ * build_moe_row_adapter_decode).
+ *
+ * Conventions shared by every call:
+ *  - Every call that can fail returns an mlg_status; the library never
+ *    aborts, asserts or prints.  The pages' `None` becomes MLG_ERR_EMPTY or
+ *    MLG_ERR_INVALID_ARG, their panic MLG_ERR_CAP_ZERO, their `Err`
+ *    MLG_ERR_REFUSE.
+ *  - The caller owns every buffer, host and device.  The fold entry points
+ *    allocate no memory, never synchronise the device or the host, and
+ *    enqueue only on the stream they are given, so each can be captured in a
+ *    CUDA graph.  `stream` is a cudaStream_t passed as void* (0 = the legacy
+ *    default stream).
+ *  - All arguments are validated on the host before anything is enqueued or
+ *    written; on any error nothing is launched and no output is written.
+ *  - Device arrays are row-major.  bf16 values are raw IEEE bfloat16 bit
+ *    patterns (uint16).  Device pointers must come from the CUDA allocator
+ *    of the current device (or be offsets into such allocations).
+ *  - Table cells are data: an expert folds nothing when its id is negative,
+ *    at or above n_experts, or either of its table cells is 0.  A non-zero
+ *    cell that is not 16-byte aligned is also treated as 0 (the kernels never
+ *    fault on table contents they can check).  A non-zero, aligned cell must
+ *    hold the device address of an array of the stated shape.
+ *  - Rows that do not fold keep their input bits exactly (including -0.0).
+ *  - Arithmetic: bf16 inputs, fp32 products and sums, the rank-r
+ *    intermediate h kept in fp32 (never rounded to bf16), and one
+ *    round-to-nearest-even to bf16 of base + scale * delta per element.
+ */
+#ifndef MLG_H_
+#define MLG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t mlg_status;
+
+#if defined(__GNUC__)
+#define MLG_API __attribute__((visibility("default")))
+#else
+#define MLG_API
+#endif
+
+#define MLG_OK 0
+#define MLG_ERR_INVALID_ARG (-1)      /* bad pointer, size or relation; the pages' None */
+#define MLG_ERR_EMPTY (-2)            /* empty input where the pages return None */
+#define MLG_ERR_CAP_ZERO (-3)         /* window cap of 0: the pages' panic */
+#define MLG_ERR_REFUSE (-4)           /* a decode batch the single-active fold cannot serve */
+#define MLG_ERR_UNSUPPORTED (-5)      /* alignment or size limit of this implementation */
+#define MLG_ERR_BUFFER_TOO_SMALL (-6) /* output buffer shorter than the result */
+#define MLG_ERR_CUDA (-7)             /* a CUDA runtime call failed; see mlg_last_cuda_error() */
+
+/* Route values of resolve_moe_lora_route (moe_row_adapter.rs). */
+#define MLG_ROUTE_FOLD 0
+#define MLG_ROUTE_SKIP 1
+#define MLG_ROUTE_REFUSE 2
+
+/* Largest max_rank the fold kernels accept.  max_rank must also be a
+ * multiple of 8 so that every row of B_e starts on a 16-byte boundary; a
+ * smaller true rank is stored zero-padded to max_rank. */
+#define MLG_MAX_RANK 64
+
+typedef uint16_t mlg_bf16;
+
+/* One (expert_id, a_addr, b_addr, scale) entry of pack_expert_tables. */
+typedef struct mlg_expert_entry {
+  uint32_t expert_id;
+  uint32_t reserved0; /* ignored */
+  uint64_t a_addr;    /* device address of A_e [max_rank, k_in] bf16, or 0 */
+  uint64_t b_addr;    /* device address of B_e [n_out, max_rank] bf16, or 0 */
+  float scale;        /* scale_e */
+  uint32_t reserved1; /* ignored */
+} mlg_expert_entry;
+
+/* One [start, end) window of grouped_down_windows. */
+typedef struct mlg_window {
+  uint32_t start;
+  uint32_t end;
+} mlg_window;
+
+/* ------------------------------------------------------------------------
+ * Fold entry points (device work; enqueue on `stream`, return immediately).
+ * ------------------------------------------------------------------------ */
+
+/* moe_lora_gather_bgmv (moe_lora_grouped module index): the decode-side fold
+ * over flat (token, slot) rows, row = token * top_k + slot.  For every row in
+ * [0, n_slots): e = indices[row], t = row / top_k (gather_row_token); the row
+ * folds x[t] through expert e unless row_adapter[t] < 0 (the decode row map of
+ * build_moe_row_adapter_decode) or expert e folds nothing (see above).
+ *
+ *   x            device, [ceil(n_slots / top_k), k_in] bf16, 16-byte aligned
+ *   indices      device, [n_slots] int32 expert ids (any value: invalid ids fold nothing)
+ *   row_adapter  device, [ceil(n_slots / top_k)] int32, required (non-NULL)
+ *   a_table      device, [n_experts] uint64 addresses of A_e (0 = unadapted)
+ *   b_table      device, [n_experts] uint64 addresses of B_e (0 = unadapted)
+ *   scale_table  device, [n_experts] float scale_e
+ *   base_out     device, [n_slots, n_out] bf16, updated in place, 16-byte aligned
+ *   k_in         >= 8, multiple of 8;  n_out >= 8, multiple of 8
+ *   max_rank     1..MLG_MAX_RANK, multiple of 8
+ *   top_k        >= 1;  n_experts >= 0 (0: nothing folds, nothing is launched)
+ * n_slots == 0 is a no-op.  Errors: INVALID_ARG (NULL pointer, negative size,
+ * top_k < 1), UNSUPPORTED (alignment, k_in / n_out / max_rank limits),
+ * CUDA (the launch failed). */
+MLG_API mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices, const int32_t *row_adapter,
+                           const uint64_t *a_table, const uint64_t *b_table,
+                           const float *scale_table, mlg_bf16 *base_out, int32_t n_slots,
+                           int32_t k_in, int32_t max_rank, int32_t n_out, int32_t top_k,
+                           int32_t n_experts, void *stream);
+
+/* moe_lora_grouped_down (moe_lora_grouped module index): the prefill-side fold
+ * over expert-sorted rows r in the window [row_offset, row_end).  e is the
+ * expert whose span expert_offsets[e] <= r < expert_offsets[e + 1] holds r
+ * (e < n_experts); the row's input is x[src[r] / top_k].  base_out is indexed
+ * by sorted row.  Rows outside the window, rows in no span below n_experts
+ * (at or past expert_offsets[n_experts]) and rows whose token has a negative
+ * row_adapter entry keep their input.
+ *
+ *   x              device, [n_tokens, k_in] bf16, 16-byte aligned
+ *   expert_offsets device, >= n_experts + 1 int32, non-decreasing; read on the
+ *                  device only (no host copy), so the call is graph-capturable
+ *   src            device, int32 sorted row -> flat (token, slot) row; every
+ *                  src[r] in the window must be < n_tokens * top_k (a negative
+ *                  entry folds nothing)
+ *   row_adapter    device, [n_tokens] int32 prefill row map, or NULL (every row folds)
+ *   tables         as for mlg_gather_bgmv
+ *   base_out       device, [>= row_end, n_out] bf16, in place, 16-byte aligned
+ *   0 <= row_offset <= row_end; an empty window is a no-op
+ * Errors as for mlg_gather_bgmv, plus INVALID_ARG for row_end < row_offset. */
+MLG_API mlg_status mlg_grouped_down(const mlg_bf16 *x, const int32_t *expert_offsets, const int32_t *src,
+                            const int32_t *row_adapter, const uint64_t *a_table,
+                            const uint64_t *b_table, const float *scale_table,
+                            mlg_bf16 *base_out, int32_t k_in, int32_t max_rank, int32_t n_out,
+                            int32_t top_k, int32_t n_experts, int32_t row_offset,
+                            int32_t row_end, void *stream);
+
+/* The router fold (MoeExpertRoute, moe_lora_grouped module index): a one-entry
+ * route whose expert 0 is the router pair, so every token t folds
+ * base_out[t] += scale_0 * (x[t] @ A_0^T) @ B_0^T.  The tables have one entry;
+ * a zero cell makes the call a no-op on the device.
+ *
+ *   x            device, [n_tokens, k_in] bf16;  base_out device, [n_tokens, n_out] bf16
+ *   row_adapter  device, [n_tokens] int32 or NULL (negative entries skip the token)
+ * Limits and errors as for mlg_grouped_down. */
+MLG_API mlg_status mlg_router_fold(const mlg_bf16 *x, const int32_t *row_adapter, const uint64_t *a_table,
+                           const uint64_t *b_table, const float *scale_table, mlg_bf16 *base_out,
+                           int32_t n_tokens, int32_t k_in, int32_t max_rank, int32_t n_out,
+                           void *stream);
+
+/* ------------------------------------------------------------------------
+ * Host helpers (pure CPU unless stated; no device work).
+ * ------------------------------------------------------------------------ */
+
+/* resolve_moe_lora_route (moe_row_adapter.rs): the fold decision for one
+ * request.  Returns MLG_ROUTE_FOLD when has_moe_lora is 0; else SKIP for a
+ * negative slot; else FOLD when slot == active; else REFUSE. */
+MLG_API int32_t mlg_resolve_moe_lora_route(int32_t adapter_slot, int32_t active, int32_t has_moe_lora);
+
+/* ensure_decode_route_servable (moe_row_adapter.rs): MLG_ERR_REFUSE when
+ * route is MLG_ROUTE_REFUSE (a decode batch cannot serve a non-active adapter
+ * under the single-active fold), MLG_OK for FOLD / SKIP, INVALID_ARG for any
+ * other value. */
+MLG_API mlg_status mlg_ensure_decode_route_servable(int32_t route);
+
+/* build_moe_row_adapter_decode (moe_row_adapter.rs): writes the [padded_n]
+ * decode row map to out: entry i is `active` when i < n_slots and slot i
+ * routes to FOLD, else -1 (Skip, Refuse and padding).  out must hold padded_n
+ * entries.  Errors: INVALID_ARG for out == NULL with padded_n > 0, or
+ * adapter_slots == NULL with n_slots > 0. */
+MLG_API mlg_status mlg_build_moe_row_adapter_decode(const int32_t *adapter_slots, size_t n_slots,
+                                            size_t padded_n, int32_t active,
+                                            int32_t has_moe_lora, int32_t *out);
+
+/* build_moe_row_adapter_host (moe_row_adapter.rs): the [total_tokens] prefill
+ * row map.  cu_seqlens holds n_cu = batch + 1 prefix sums; stream b's slot is
+ * written over rows cu[b]..cu[b+1].  INVALID_ARG (nothing written) when
+ * n_cu < 2, n_slots != n_cu - 1, cu[0] != 0, or a boundary is negative or
+ * decreasing -- the pages' None.  *total_out receives cu[n_cu-1] whenever the
+ * boundaries are valid; BUFFER_TOO_SMALL (nothing written) when cap is below
+ * it, so a caller may size the buffer with a first call of cap 0. */
+MLG_API mlg_status mlg_build_moe_row_adapter_host(const int32_t *cu_seqlens, size_t n_cu,
+                                          const int32_t *adapter_slots, size_t n_slots,
+                                          int32_t *out, size_t cap, size_t *total_out);
+
+/* pack_expert_tables (moe_lora_grouped module index): dense tables indexed by
+ * expert id with n_experts = max id + 1, 0 / 0 / 0.0f at every id without an
+ * entry, and the last entry winning for a duplicated id.  EMPTY for n == 0.
+ * *n_experts_out is set whenever n > 0; BUFFER_TOO_SMALL (nothing written)
+ * when cap < n_experts.  UNSUPPORTED (nothing written) when a non-zero
+ * address is not 16-byte aligned.  The tables are host arrays; upload them
+ * with mlg_upload_expert_tables. */
+MLG_API mlg_status mlg_pack_expert_tables(const mlg_expert_entry *entries, size_t n, uint64_t *a_out,
+                                  uint64_t *b_out, float *scale_out, size_t cap,
+                                  uint32_t *n_experts_out);
+
+/* Table upload: three cudaMemcpyAsync host-to-device copies of n_experts
+ * entries on `stream`.  Staging in pinned memory is the caller's choice; with
+ * pageable memory the copies are synchronous with respect to the host.
+ * Errors: INVALID_ARG (NULL), CUDA. */
+MLG_API mlg_status mlg_upload_expert_tables(const uint64_t *a_host, const uint64_t *b_host,
+                                    const float *scale_host, uint32_t n_experts,
+                                    uint64_t *a_dev, uint64_t *b_dev, float *scale_dev,
+                                    void *stream);
+
+/* Row-map upload (the engine's upload_moe_row_adapter): one cudaMemcpyAsync
+ * of n int32 entries, host to device, on `stream`. */
+MLG_API mlg_status mlg_upload_row_adapter(const int32_t *map_host, size_t n, int32_t *map_dev,
+                                  void *stream);
+
+/* grouped_down_windows (moe_lora_grouped module index): contiguous windows
+ * [i*cap, min((i+1)*cap, total_rows)) covering 0..total_rows.  CAP_ZERO for
+ * cap == 0.  *n_windows receives the window count; BUFFER_TOO_SMALL (nothing
+ * written) when out_cap is below it. */
+MLG_API mlg_status mlg_grouped_down_windows(uint32_t total_rows, uint32_t cap, mlg_window *out,
+                                    size_t out_cap, size_t *n_windows);
+
+/* grouped_down_wc (moe_lora_grouped module index): the tile count of a
+ * window, max(1, ceil((row_end - row_offset) / MLG_M_TILE)); 1 when
+ * row_end <= row_offset. */
+MLG_API uint32_t mlg_grouped_down_wc(uint32_t row_offset, uint32_t row_end);
+
+/* gather_row_token (moe_lora_grouped module index): row / top_k; 0 when
+ * top_k == 0. */
+MLG_API uint32_t mlg_gather_row_token(uint32_t row, uint32_t top_k);
+
+/* MLG_M_TILE: sorted rows per grouped-fold tile (the tensor-core M of the
+ * grouped kernel).  mlg_grouped_down_wc uses the same value. */
+MLG_API uint32_t mlg_m_tile(void);
+
+/* A static, NUL-terminated description of a status code. */
+MLG_API const char *mlg_status_string(mlg_status status);
+
+/* The cudaError_t of the last failing CUDA call made by this library on the
+ * calling thread (0 when none). */
+MLG_API int32_t mlg_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+MLG_API int32_t mlg_version(void);
+
+/* Device error bits the fold kernels recorded on the current device instead
+ * of trapping: MLG_DEVERR_WAIT_TIMEOUT (a wait for a copy or an MMA ran past
+ * its one-second limit; the kernel stopped issuing work and the affected rows
+ * may be unfolded), MLG_DEVERR_TMEM_ALLOC (tensor memory could not be
+ * allocated; the affected tiles were not folded).  Reads the OR of all bits
+ * since the last clear into *flags_out and clears them when `clear` is
+ * non-zero.  Synchronous (a device-to-host copy); not for the hot path. */
+#define MLG_DEVERR_WAIT_TIMEOUT 1u
+#define MLG_DEVERR_TMEM_ALLOC 2u
+MLG_API mlg_status mlg_read_device_errors(uint32_t *flags_out, int32_t clear);
+
+/* Launch-shape knobs for benchmarking sweeps; 0 restores the automatic
+ * choice.  Process-wide; set them only while no other thread launches folds.
+ *   MLG_TUNE_GATHER_CLUSTER   CTAs per expert cluster of mlg_gather_bgmv (1, 2, 4, 8)
+ *   MLG_TUNE_GROUPED_CTAS     persistent CTAs of mlg_grouped_down / mlg_router_fold
+ * Errors: INVALID_ARG for an unknown knob or a value out of range. */
+#define MLG_TUNE_GATHER_CLUSTER 1
+#define MLG_TUNE_GROUPED_CTAS 2
+MLG_API mlg_status mlg_set_tuning(int32_t knob, int32_t value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLG_H_ */

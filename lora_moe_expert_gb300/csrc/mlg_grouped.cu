@@ -1,0 +1,728 @@
+// mlg_grouped.cu -- prefill-side grouped fold (moe_lora_grouped_down of the
+// moe_lora_grouped module index) and the router fold (MoeExpertRoute: a
+// one-entry route whose expert 0 is the router pair).
+//
+// For every expert-sorted row r of the window [row_offset, row_end) held by
+// expert e's span expert_offsets[e] .. expert_offsets[e+1]:
+//     base_out[r] += scale_e * (x[src[r] / top_k] @ A_e^T) @ B_e^T.
+//
+// GB300 design (not the pages' MLG_M_TILE grid):
+//  * tiles are expert-aligned runs of <= 128 sorted rows (one tcgen05 M), so
+//    a tile never mixes experts and every output row has one owner; the tile
+//    list is built on the device from expert_offsets and the tables (no host
+//    copy), and persistent CTAs (one per SM) walk it round-robin;
+//  * warp 0 issues the tensor-core work: shrink H = X A_e^T (M=128, N=rank,
+//    K=k_in in 64-wide chunks) into tensor memory, then expand
+//    ACC = [H_hi | H_lo] [B_e | B_e]^T (M=128, N=64/128 columns per chunk) into
+//    a double-buffered TMEM accumulator -- h is split into two bf16 halves so
+//    it enters the expand at ~2^-17 relative precision (kept fp32 in effect);
+//  * warp 1 gathers the X rows (via src) and A_e chunks, warp 2 the B_e
+//    chunks, with 16-byte cp.async into 128-byte-swizzled K-major tiles;
+//  * warps 4-7 (one TMEM lane quarter each) scale and split h, then stream
+//    base_out: each warp owns 32 rows of the tile and runs its own ring of
+//    32x64 TMA boxes (prefetch depth D-1), adds the accumulator, rounds once
+//    to bf16 (RNE) and TMA-stores boxes it owns whole; rows of a box it owns
+//    only in part are stored row by row, so no row of another tile is written.
+//  Every wait is bounded; a timeout sets an error bit and the CTA drains and
+//  exits instead of hanging.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "mlg_internal.h"
+#include "mlg_ptx.cuh"
+
+namespace mlg {
+namespace {
+
+constexpr int kGThreads = 256;
+constexpr int kTileM = MLG_M_TILE;   // 128 rows per tile
+constexpr int kBoxRows = 32;         // rows per TMA box (one epilogue warp)
+constexpr int kBoxCols = 64;         // bf16 columns per TMA box (128 bytes)
+constexpr int kMaxDepth = 8;         // base-ring stages per epilogue warp
+constexpr int kMaxStages = 4;        // operand ring stages
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemH = 0, kTmemAcc0 = 128, kTmemAcc1 = 256;
+
+static __device__ uint32_t g_grouped_errors;
+
+struct GroupedParams {
+  const uint8_t *x;              // bf16 [n_tokens, k_in]
+  const int32_t *offsets;        // [n_experts + 1] or null (router: one span)
+  const int32_t *src;            // sorted row -> flat row, or null (identity)
+  const int32_t *row_adapter;    // [n_tokens] or null
+  const uint64_t *a_table;
+  const uint64_t *b_table;
+  const float *scale_table;
+  uint8_t *base_out;             // bf16 [>= row_end, n_out]
+  int32_t k_in, rank, n_out, top_k, n_experts, row_offset, row_end;
+  int32_t r_pad;                 // rank rounded up to 16 (shrink N)
+  int32_t k_exp;                 // expand K: [hi | lo] padded to a multiple of 64
+  int32_t n_ch;                  // expand N per accumulator chunk (64 or 128)
+  int32_t kc_count, nc_count, nbx;  // k chunks, n chunks, 64-column boxes per row
+  int32_t nxa, nbs, depth;       // ring stages
+  uint32_t xa_stage, b_stage;    // bytes per stage
+  uint32_t off_xa, off_b, off_h, off_base, off_tab, smem_bytes;
+};
+
+// Byte offset of 16-byte chunk `c` (of 8 per 128-byte row) of row `row` in a
+// K-major 128-byte-swizzled tile whose 8-row atoms are 1024 bytes apart.
+__device__ __forceinline__ uint32_t sw128(int row, int c) {
+  return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4));
+}
+
+struct Ctl {
+  uint64_t xa_full[kMaxStages], xa_empty[kMaxStages];
+  uint64_t b_full[kMaxStages], b_empty[kMaxStages];
+  uint64_t h_full, hs_full, hs_empty, drain;
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t base_full[4][kMaxDepth];
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_bar(Ctl &ctl, uint64_t &bar, uint32_t parity) {
+  const uint32_t a = smem_addr(&bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (ctl.abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(&g_grouped_errors, kErrWaitTimeout);
+      ctl.abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+struct TileInfo {
+  int e, r0, r1;
+};
+
+__device__ __forceinline__ int span_lo(const GroupedParams &p, int e) {
+  const int lo = p.offsets ? __ldg(p.offsets + e) : 0;
+  return max(lo, p.row_offset);
+}
+__device__ __forceinline__ int span_hi(const GroupedParams &p, int e) {
+  const int hi = p.offsets ? __ldg(p.offsets + e + 1) : p.row_end;
+  return min(hi, p.row_end);
+}
+
+// Tile t of the window: the expert owning it (tile_start is an exclusive
+// prefix over experts) and its rows [r0, r1).
+__device__ TileInfo tile_info(const GroupedParams &p, const int *tile_start, int n_e, int t) {
+  int lo = 0, hi = n_e - 1;  // largest e with tile_start[e] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  TileInfo ti;
+  ti.e = lo;
+  ti.r0 = span_lo(p, lo) + (t - tile_start[lo]) * kTileM;
+  ti.r1 = min(ti.r0 + kTileM, span_hi(p, lo));
+  return ti;
+}
+
+__device__ __forceinline__ bool cells_fold(uint64_t a, uint64_t b) {
+  return a != 0 && b != 0 && ((a | b) & 15u) == 0;
+}
+
+__device__ __forceinline__ uint32_t pack8_add(const uint4 b, const float *v, uint4 &out) {
+  const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = pack_bf16x2(bf16lo_to_f32(w[i]) + v[2 * i], bf16hi_to_f32(w[i]) + v[2 * i + 1]);
+  out = make_uint4(o[0], o[1], o[2], o[3]);
+  return 0;
+}
+
+template <int RP>  // rank rounded up to a multiple of 16
+__global__ void __launch_bounds__(kGThreads, 1)
+    grouped_fold_kernel(const __grid_constant__ CUtensorMap tmap_base, const GroupedParams p) {
+  constexpr int KEXP = (2 * RP + 63) / 64 * 64;  // expand K: [hi | lo | zero pad]
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ Ctl ctl;
+  // 1024-byte alignment for the swizzled tiles.
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_e = p.offsets ? p.n_experts : 1;
+  int *tile_start = reinterpret_cast<int *>(smem + p.off_tab);  // [n_e + 1]
+
+  // ---- prologue: barriers, zeroed operand padding, tile table, TMEM ------
+  if (tid == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(smem_addr(&ctl.xa_full[s]), 32);
+      mbar_init(smem_addr(&ctl.xa_empty[s]), 1);
+      mbar_init(smem_addr(&ctl.b_full[s]), 32);
+      mbar_init(smem_addr(&ctl.b_empty[s]), 1);
+    }
+    mbar_init(smem_addr(&ctl.h_full), 1);
+    mbar_init(smem_addr(&ctl.hs_full), 4);
+    mbar_init(smem_addr(&ctl.hs_empty), 1);
+    mbar_init(smem_addr(&ctl.drain), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&ctl.acc_full[s]), 1);
+      mbar_init(smem_addr(&ctl.acc_empty[s]), 4);
+    }
+    for (int w = 0; w < 4; ++w)
+      for (int s = 0; s < kMaxDepth; ++s) mbar_init(smem_addr(&ctl.base_full[w][s]), 1);
+    ctl.abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_base);
+  }
+  // Operand padding read by the MMAs but never written by a copy: A_e rows
+  // [rank, r_pad) of every X/A stage and the B positions outside the two
+  // copies of B_e's rank columns.
+  for (uint32_t i = tid * 16; i < p.off_h; i += kGThreads * 16)
+    *reinterpret_cast<uint4 *>(smem + i) = make_uint4(0, 0, 0, 0);
+  // Tile table: tiles of expert e = ceil(rows of e in the window / 128), 0 if
+  // the expert folds nothing; exclusive prefix over experts.
+  {
+    constexpr int kPer = 16;  // experts per thread per pass
+    int carry = 0;
+    for (int base = 0; base < n_e; base += kGThreads * kPer) {
+      int cnt[kPer];
+      int sum = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = base + tid * kPer + i;
+        int n = 0;
+        if (e < n_e) {
+          const int lo = span_lo(p, e), hi = span_hi(p, e);
+          if (hi > lo && cells_fold(__ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + e),
+                                    __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + e)))
+            n = (hi - lo + kTileM - 1) / kTileM;
+        }
+        cnt[i] = n;
+        sum += n;
+      }
+      // block exclusive scan of the per-thread sums
+      int incl = sum;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      __shared__ int warp_tot[kGThreads / 32];
+      if (lane == 31) warp_tot[warp] = incl;
+      __syncthreads();
+      int before = carry, total = 0;
+      for (int w = 0; w < kGThreads / 32; ++w) {
+        before += (w < warp) ? warp_tot[w] : 0;
+        total += warp_tot[w];
+      }
+      int run = before + incl - sum;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = base + tid * kPer + i;
+        if (e < n_e) tile_start[e] = run;
+        run += cnt[i];
+      }
+      carry += total;
+      __syncthreads();
+    }
+    if (tid == 0) tile_start[n_e] = carry;
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const int n_tiles = tile_start[n_e];
+  const uint32_t idesc_shrink = umma_idesc_bf16(kTileM, RP);
+  const uint32_t idesc_expand = umma_idesc_bf16(kTileM, p.n_ch);
+  const uint32_t xa_base = smem_addr(smem + p.off_xa);
+  const uint32_t b_base = smem_addr(smem + p.off_b);
+  const uint32_t h_base = smem_addr(smem + p.off_h);
+
+  if (warp == 0) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      uint32_t xa_it = 0, b_it = 0, acc_it = 0, tile_it = 0;
+      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_it) {
+        for (int kc = 0; kc < p.kc_count; ++kc, ++xa_it) {
+          const int st = xa_it % p.nxa;
+          if (!wait_bar(ctl, ctl.xa_full[st], (xa_it / p.nxa) & 1)) goto mma_done;
+          tc_fence_after();
+          const uint32_t xs = xa_base + st * p.xa_stage;
+          const uint32_t as = xs + kTileM * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(tmem + kTmemH, umma_desc_sw128(xs + k * 32), umma_desc_sw128(as + k * 32),
+                      idesc_shrink, (kc | k) != 0);
+          umma_commit(smem_addr(&ctl.xa_empty[st]));
+        }
+        umma_commit(smem_addr(&ctl.h_full));
+        if (!wait_bar(ctl, ctl.hs_full, tile_it & 1)) goto mma_done;
+        tc_fence_after();
+        for (int nc = 0; nc < p.nc_count; ++nc, ++b_it, ++acc_it) {
+          const int st = b_it % p.nbs;
+          const int ab = acc_it & 1;
+          if (!wait_bar(ctl, ctl.b_full[st], (b_it / p.nbs) & 1)) goto mma_done;
+          if (!wait_bar(ctl, ctl.acc_empty[ab], ((acc_it >> 1) & 1) ^ 1)) goto mma_done;
+          tc_fence_after();
+          const uint32_t bs = b_base + st * p.b_stage;
+          const uint32_t d = tmem + (ab ? kTmemAcc1 : kTmemAcc0);
+#pragma unroll
+          for (int k = 0; k < KEXP / 16; ++k) {
+            const uint32_t koff = (k & 3) * 32;
+            const uint32_t a_atom = h_base + (k >> 2) * (kTileM * 128);
+            const uint32_t b_atom = bs + (k >> 2) * (p.n_ch * 128);
+            umma_bf16(d, umma_desc_sw128(a_atom + koff), umma_desc_sw128(b_atom + koff),
+                      idesc_expand, k != 0);
+          }
+          umma_commit(smem_addr(&ctl.b_empty[st]));
+          umma_commit(smem_addr(&ctl.acc_full[ab]));
+        }
+        umma_commit(smem_addr(&ctl.hs_empty));
+      }
+    mma_done:
+      umma_commit(smem_addr(&ctl.drain));
+      mbar_wait_bounded(smem_addr(&ctl.drain), 0);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ X / A_e producer
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      const TileInfo ti = tile_info(p, tile_start, n_e, t);
+      const uint8_t *A = reinterpret_cast<const uint8_t *>(
+          __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + ti.e));
+      const uint8_t *xrow[4];
+      bool xv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = ti.r0 + lane + 32 * q;
+        int s = -1;
+        if (r < ti.r1) s = p.src ? __ldg(p.src + r) : r;
+        xv[q] = s >= 0;
+        xrow[q] = p.x + static_cast<size_t>(s >= 0 ? s / p.top_k : 0) * p.k_in * 2;
+      }
+      for (int kc = 0; kc < p.kc_count; ++kc, ++it) {
+        const int st = it % p.nxa;
+        if (!wait_bar(ctl, ctl.xa_empty[st], ((it / p.nxa) & 1) ^ 1)) goto prod_a_done;
+        const uint32_t xs = xa_base + st * p.xa_stage;
+        const uint32_t as = xs + kTileM * 128;
+        const int k0 = kc * 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (!xv[q]) continue;
+          const int row = lane + 32 * q;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int kk = k0 + 8 * c;
+            const bool in = kk < p.k_in;
+            cp_async_16(xs + sw128(row, c), xrow[q] + (in ? kk * 2 : 0), in ? 16u : 0u);
+          }
+        }
+        for (int j = lane; j < p.rank; j += 32) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int kk = k0 + 8 * c;
+            const bool in = kk < p.k_in;
+            cp_async_16(as + sw128(j, c), A + (static_cast<size_t>(j) * p.k_in + (in ? kk : 0)) * 2,
+                        in ? 16u : 0u);
+          }
+        }
+        cp_async_commit();
+        cp_async_wait_group<0>();
+        fence_proxy_async_smem();
+        mbar_arrive(smem_addr(&ctl.xa_full[st]));
+      }
+    }
+  prod_a_done:
+    cp_async_wait_group<0>();
+  } else if (warp == 2) {
+    // ================================================================ B_e producer
+    uint32_t it = 0;
+    const int rc = p.rank / 8;           // 16-byte chunks per B_e row
+    constexpr int hi_chunks = RP / 8;    // position of the lo copy
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      const TileInfo ti = tile_info(p, tile_start, n_e, t);
+      const uint8_t *B = reinterpret_cast<const uint8_t *>(
+          __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ti.e));
+      for (int nc = 0; nc < p.nc_count; ++nc, ++it) {
+        const int st = it % p.nbs;
+        if (!wait_bar(ctl, ctl.b_empty[st], ((it / p.nbs) & 1) ^ 1)) goto prod_b_done;
+        const uint32_t bs = b_base + st * p.b_stage;
+        const int n0 = nc * p.n_ch;
+        for (int i = lane; i < p.n_ch; i += 32) {
+          const int n = n0 + i;
+          const bool in = n < p.n_out;
+          const uint8_t *brow = B + static_cast<size_t>(in ? n : 0) * p.rank * 2;
+          for (int c = 0; c < rc; ++c) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int kc16 = half * hi_chunks + c;  // 16-byte chunk index along K
+              const uint32_t dst = bs + (kc16 >> 3) * (p.n_ch * 128) + sw128(i, kc16 & 7);
+              cp_async_16(dst, brow + c * 16, in ? 16u : 0u);
+            }
+          }
+        }
+        cp_async_commit();
+        cp_async_wait_group<0>();
+        fence_proxy_async_smem();
+        mbar_arrive(smem_addr(&ctl.b_full[st]));
+      }
+    }
+  prod_b_done:
+    cp_async_wait_group<0>();
+  } else if (warp >= 4) {
+    // ================================================================ epilogue
+    const int ew = warp - 4;  // TMEM lanes [32 ew, 32 ew + 32)
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(ew * 32) << 16);
+    uint8_t *ring = smem + p.off_base + ew * p.depth * 4096;
+    const uint32_t ring_addr = smem_addr(ring);
+    uint32_t tile_it = 0, acc_it = 0;
+    // box sequence of this warp: (tile, box column) for tiles with rows here
+    int ld_t = blockIdx.x, ld_b = 0, ld_y = 0;
+    uint32_t ld_count = 0, box_it = 0;
+    auto ld_advance = [&](bool first) {
+      if (!first) {
+        if (++ld_b < p.nbx) return;
+        ld_b = 0;
+        ld_t += gridDim.x;
+      }
+      for (; ld_t < n_tiles; ld_t += gridDim.x) {
+        const TileInfo ti = tile_info(p, tile_start, n_e, ld_t);
+        if (ti.r1 > ti.r0 + ew * kBoxRows) {
+          ld_y = ti.r0 + ew * kBoxRows;
+          return;
+        }
+      }
+    };
+    auto ld_issue = [&]() {  // lane 0 only
+      if (ld_t >= n_tiles) return;
+      const int st = ld_count % p.depth;
+      const uint32_t bar = smem_addr(&ctl.base_full[ew][st]);
+      mbar_arrive_expect_tx(bar, kBoxRows * kBoxCols * 2);
+      tma_load_2d(ring_addr + st * 4096, &tmap_base, ld_b * kBoxCols, ld_y, bar);
+      ++ld_count;
+      ld_advance(false);
+    };
+    ld_advance(true);
+    if (lane == 0)
+      for (int i = 0; i < p.depth - 1; ++i) ld_issue();
+
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_it) {
+      const TileInfo ti = tile_info(p, tile_start, n_e, t);
+      const int row = ew * kBoxRows + lane;
+      const int rg = ti.r0 + row;
+      bool folds = false;
+      if (rg < ti.r1) {
+        const int s = p.src ? __ldg(p.src + rg) : rg;
+        folds = s >= 0 && (p.row_adapter == nullptr || __ldg(p.row_adapter + s / p.top_k) >= 0);
+      }
+      const float scale = __ldg(p.scale_table + ti.e);
+      const int owned = min(max(ti.r1 - (ti.r0 + ew * kBoxRows), 0), kBoxRows);
+
+      // ---- h: tensor memory -> scaled, split into bf16 hi / lo -> shared memory
+      if (!wait_bar(ctl, ctl.h_full, tile_it & 1)) goto epi_done;
+      tc_fence_after();
+      float h[RP];
+#pragma unroll
+      for (int q = 0; q < RP / 16; ++q) {
+        float v[16];
+        tmem_ld16(lane_addr + kTmemH + q * 16, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) h[q * 16 + i] = v[i];
+      }
+      tmem_wait_ld();
+      if (!wait_bar(ctl, ctl.hs_empty, (tile_it & 1) ^ 1)) goto epi_done;
+      {
+        float hi[RP], lo[RP];
+#pragma unroll
+        for (int j = 0; j < RP; ++j) {
+          split_hi_lo(folds ? h[j] * scale : 0.f, hi[j], lo[j]);
+        }
+        uint8_t *hrow = smem + p.off_h;
+#pragma unroll
+        for (int kk = 0; kk < KEXP; kk += 8) {
+          uint32_t w[4] = {0u, 0u, 0u, 0u};
+          if (kk < 2 * RP) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int j = (kk < RP ? kk : kk - RP) + 2 * i;
+              w[i] = kk < RP ? pack_bf16x2(hi[j], hi[j + 1]) : pack_bf16x2(lo[j], lo[j + 1]);
+            }
+          }
+          const uint32_t off = (kk >> 6) * (kTileM * 128) + sw128(row, (kk & 63) >> 3);
+          *reinterpret_cast<uint4 *>(hrow + off) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&ctl.hs_full));
+
+      // ---- expand epilogue: base_out boxes of this warp's rows -------------
+      for (int nc = 0; nc < p.nc_count; ++nc, ++acc_it) {
+        const int ab = acc_it & 1;
+        if (!wait_bar(ctl, ctl.acc_full[ab], (acc_it >> 1) & 1)) goto epi_done;
+        tc_fence_after();
+        for (int j = 0; j < p.n_ch / kBoxCols; ++j) {
+          const int bcol = nc * (p.n_ch / kBoxCols) + j;
+          if (owned == 0 || bcol >= p.nbx) continue;
+          const int st = box_it % p.depth;
+          if (!wait_bar(ctl, ctl.base_full[ew][st], (box_it / p.depth) & 1)) goto epi_done;
+          float v[64];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float u[16];
+            tmem_ld16(lane_addr + (ab ? kTmemAcc1 : kTmemAcc0) + j * kBoxCols + q * 16, u);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[q * 16 + i] = u[i];
+          }
+          tmem_wait_ld();
+          uint8_t *boxp = ring + st * 4096 + lane * 128;
+          const bool whole = owned == kBoxRows;
+          if (folds) {
+            const int col0 = bcol * kBoxCols;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint4 *cp = reinterpret_cast<uint4 *>(boxp + ((c ^ (lane & 7)) << 4));
+              uint4 o;
+              pack8_add(*cp, v + 8 * c, o);
+              if (whole) {
+                *cp = o;
+              } else if (col0 + 8 * c < p.n_out) {
+                *reinterpret_cast<uint4 *>(p.base_out +
+                                           (static_cast<size_t>(rg) * p.n_out + col0 + 8 * c) * 2) = o;
+              }
+            }
+          }
+          if (whole) fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (whole) tma_store_2d(&tmap_base, bcol * kBoxCols, ti.r0 + ew * kBoxRows,
+                                    ring_addr + st * 4096);
+            bulk_commit();
+            bulk_wait_read_1();  // the previous box's store has left its stage
+            ld_issue();
+          }
+          __syncwarp();
+          ++box_it;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ctl.acc_empty[ab]));
+      }
+    }
+  epi_done:
+    if (lane == 0) {
+      bulk_wait_all();
+      // loads issued but not consumed (only after an abort): let them land
+      for (uint32_t k = box_it; k < ld_count; ++k)
+        mbar_wait_bounded(smem_addr(&ctl.base_full[ew][k % p.depth]), (k / p.depth) & 1);
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+int g_grouped_ctas = 0;
+// Dynamic shared memory cap: 227 KB per block minus room for the static part.
+constexpr uint32_t kGSmemLimit = 227 * 1024 - 2048;
+
+uint32_t rup(uint32_t v, uint32_t m) { return (v + m - 1) / m * m; }
+
+// Shared-memory plan; returns total dynamic bytes (including 1 KB alignment slack).
+uint32_t plan(GroupedParams &p, int n_ch, int nxa, int nbs, int depth, int n_e) {
+  p.n_ch = n_ch;
+  p.nxa = nxa;
+  p.nbs = nbs;
+  p.depth = depth;
+  p.nc_count = (p.n_out + n_ch - 1) / n_ch;
+  p.xa_stage = rup(kTileM * 128 + p.r_pad * 128, 1024);
+  p.b_stage = rup(static_cast<uint32_t>(n_ch * p.k_exp * 2), 1024);
+  uint32_t off = 0;
+  p.off_xa = off;
+  off += nxa * p.xa_stage;
+  p.off_b = off;
+  off += nbs * p.b_stage;
+  p.off_h = off;
+  off += kTileM * p.k_exp * 2;
+  p.off_base = off;
+  off += 4 * depth * 4096;
+  p.off_tab = off;
+  off += rup((n_e + 1) * 4, 16);
+  p.smem_bytes = off;
+  return off + 1024;
+}
+
+mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return MLG_ERR_CUDA;
+  const int n_e = p.offsets ? p.n_experts : 1;
+  p.r_pad = static_cast<int>(rup(p.rank, 16));
+  p.k_exp = static_cast<int>(rup(2 * p.r_pad, 64));
+  p.kc_count = (p.k_in + 63) / 64;
+  p.nbx = (p.n_out + kBoxCols - 1) / kBoxCols;
+  // Largest rings that fit: accumulator chunk, operand stages, base depth.
+  bool ok = false;
+  uint32_t total = 0;
+  const int n_chs[2] = {128, 64};
+  for (int a = 0; a < 2 && !ok; ++a)
+    for (int depth = 6; depth >= 3 && !ok; --depth)
+      for (int nxa = 3; nxa >= 2 && !ok; --nxa) {
+        total = plan(p, n_chs[a], nxa, 2, depth, n_e);
+        ok = total <= kGSmemLimit;
+      }
+  if (!ok) return MLG_ERR_UNSUPPORTED;
+
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.n_out), static_cast<cuuint64_t>(p.row_end)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.n_out) * 2};
+  const cuuint32_t box[2] = {kBoxCols, kBoxRows};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.base_out, dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MLG_ERR_CUDA;
+
+  static std::once_flag once[64];
+  static cudaError_t attr_err[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(once[dev & 63], [d = dev & 63] {
+    cudaError_t e = cudaSuccess;
+    const int lim = static_cast<int>(kGSmemLimit);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_fold_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_fold_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_fold_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_fold_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    attr_err[d] = e;
+  });
+  if (attr_err[dev & 63] != cudaSuccess) return cuda_status(attr_err[dev & 63]);
+  // Persistent: one CTA per SM, or fewer when the window has fewer tiles.
+  const uint32_t window_rows = static_cast<uint32_t>(p.row_end - p.row_offset);
+  const uint32_t max_tiles = (window_rows + kTileM - 1) / kTileM + static_cast<uint32_t>(n_e);
+  int grid = sm_count();
+  if (g_grouped_ctas > 0) grid = g_grouped_ctas;
+  if (static_cast<uint32_t>(grid) > max_tiles) grid = static_cast<int>(max_tiles);
+  switch (p.r_pad) {
+    case 16: grouped_fold_kernel<16><<<grid, kGThreads, total, stream>>>(tmap, p); break;
+    case 32: grouped_fold_kernel<32><<<grid, kGThreads, total, stream>>>(tmap, p); break;
+    case 48: grouped_fold_kernel<48><<<grid, kGThreads, total, stream>>>(tmap, p); break;
+    default: grouped_fold_kernel<64><<<grid, kGThreads, total, stream>>>(tmap, p); break;
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+mlg_status fill_common(GroupedParams &p, const mlg_bf16 *x, const int32_t *row_adapter,
+                       const uint64_t *a_table, const uint64_t *b_table, const float *scale_table,
+                       mlg_bf16 *base_out, int32_t k_in, int32_t max_rank, int32_t n_out) {
+  const mlg_status shape = check_shapes(k_in, max_rank, n_out);
+  if (shape != MLG_OK) return shape;
+  if (!x || !a_table || !b_table || !scale_table || !base_out) return MLG_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(base_out)) return MLG_ERR_UNSUPPORTED;
+  p.x = reinterpret_cast<const uint8_t *>(x);
+  p.row_adapter = row_adapter;
+  p.a_table = a_table;
+  p.b_table = b_table;
+  p.scale_table = scale_table;
+  p.base_out = reinterpret_cast<uint8_t *>(base_out);
+  p.k_in = k_in;
+  p.rank = max_rank;
+  p.n_out = n_out;
+  return MLG_OK;
+}
+
+}  // namespace
+
+uint32_t grouped_read_errors(bool clear) {
+  uint32_t v = 0;
+  cudaMemcpyFromSymbol(&v, g_grouped_errors, sizeof v);
+  if (clear) {
+    const uint32_t z = 0;
+    cudaMemcpyToSymbol(g_grouped_errors, &z, sizeof z);
+  }
+  return v;
+}
+
+void grouped_set_ctas(int ctas) { g_grouped_ctas = ctas; }
+
+}  // namespace mlg
+
+extern "C" mlg_status mlg_grouped_down(const mlg_bf16 *x, const int32_t *expert_offsets,
+                                       const int32_t *src, const int32_t *row_adapter,
+                                       const uint64_t *a_table, const uint64_t *b_table,
+                                       const float *scale_table, mlg_bf16 *base_out,
+                                       int32_t k_in, int32_t max_rank, int32_t n_out,
+                                       int32_t top_k, int32_t n_experts, int32_t row_offset,
+                                       int32_t row_end, void *stream) {
+  using namespace mlg;
+  if (top_k < 1 || n_experts < 0 || row_offset < 0 || row_end < row_offset)
+    return MLG_ERR_INVALID_ARG;
+  GroupedParams p = {};
+  const mlg_status st = fill_common(p, x, row_adapter, a_table, b_table, scale_table, base_out,
+                                    k_in, max_rank, n_out);
+  if (st != MLG_OK) return st;
+  if (!expert_offsets || !src) return MLG_ERR_INVALID_ARG;
+  if (row_end == row_offset || n_experts == 0) return MLG_OK;
+  p.offsets = expert_offsets;
+  p.src = src;
+  p.top_k = top_k;
+  p.n_experts = n_experts;
+  p.row_offset = row_offset;
+  p.row_end = row_end;
+  return launch_grouped(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mlg_status mlg_router_fold(const mlg_bf16 *x, const int32_t *row_adapter,
+                                      const uint64_t *a_table, const uint64_t *b_table,
+                                      const float *scale_table, mlg_bf16 *base_out,
+                                      int32_t n_tokens, int32_t k_in, int32_t max_rank,
+                                      int32_t n_out, void *stream) {
+  using namespace mlg;
+  if (n_tokens < 0) return MLG_ERR_INVALID_ARG;
+  GroupedParams p = {};
+  const mlg_status st = fill_common(p, x, row_adapter, a_table, b_table, scale_table, base_out,
+                                    k_in, max_rank, n_out);
+  if (st != MLG_OK) return st;
+  if (n_tokens == 0) return MLG_OK;
+  p.offsets = nullptr;  // one span [0, n_tokens): expert 0 of a one-entry table
+  p.src = nullptr;      // identity rows, x_row = t
+  p.top_k = 1;
+  p.n_experts = 1;
+  p.row_offset = 0;
+  p.row_end = n_tokens;
+  return launch_grouped(p, static_cast<cudaStream_t>(stream));
+}

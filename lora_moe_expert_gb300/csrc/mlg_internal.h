@@ -1,0 +1,37 @@
+// mlg_internal.h -- declarations shared by the translation units of libmlg.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mlg.h"
+
+// Sorted rows per grouped-fold tile: the M of one tcgen05 MMA (cta_group::1).
+#define MLG_M_TILE 128u
+
+namespace mlg {
+
+extern thread_local int32_t g_last_cuda_error;
+mlg_status cuda_status(cudaError_t err);
+
+// Device-side error word: kernels OR bits into it instead of trapping.  Read
+// and cleared on the host by mlg_read_device_errors().
+enum DeviceError : uint32_t {
+  kErrWaitTimeout = 1u,   // an mbarrier wait ran past its time limit
+  kErrTmemAlloc = 2u,     // tensor-memory allocation did not succeed
+};
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side validation shared by the fold entry points.
+inline mlg_status check_shapes(int32_t k_in, int32_t max_rank, int32_t n_out) {
+  if (k_in <= 0 || max_rank <= 0 || n_out <= 0) return MLG_ERR_INVALID_ARG;
+  if (k_in % 8 != 0 || n_out % 8 != 0) return MLG_ERR_UNSUPPORTED;
+  if (max_rank % 8 != 0 || max_rank > MLG_MAX_RANK) return MLG_ERR_UNSUPPORTED;
+  return MLG_OK;
+}
+
+int sm_count();  // multiprocessors of the current device (cached per device)
+
+}  // namespace mlg

@@ -116,6 +116,8 @@ def _experts(rng, ids, k_in, max_rank, n_out, rank: Optional[int] = None) -> Lis
 def top_k_routing(rng, n_tokens: int, n_experts: int, top_k: int,
                   bias_variance: float = 0.0) -> np.ndarray:
     """[n_tokens, top_k] expert ids: the top_k of N(0,1) logits (+ per-expert bias)."""
+    if top_k > n_experts:
+        raise ValueError(f"top_k={top_k} exceeds n_experts={n_experts}")
     logits = rng.standard_normal((n_tokens, n_experts), dtype=np.float32)
     if bias_variance > 0:
         bias = rng.standard_normal(n_experts, dtype=np.float32) * np.float32(np.sqrt(bias_variance))

@@ -1,0 +1,66 @@
+"""Oracle side of the parity tests and the comparison rules.
+
+Comparison rules (the fold's contract):
+  * a folded bf16 element passes when |out - ref| <= 4e-3 * max(1, |ref|),
+    ref being the unrounded fp64 oracle value;
+  * an element that must not fold keeps its input bits exactly (-0.0 too);
+  * guard rows around base_out keep their sentinel bits.
+The 4e-3 bound: the output is one round-to-nearest-even to bf16 (half an ulp,
+2^-9 relative = 1.95e-3 of |ref| at most, 3.9e-3 absolute just below 2), so
+the fp32 arithmetic before the rounding may add up to ~9e-5 at |ref| ~ 1.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from lora_moe_expert_gb300 import synth
+
+TOL = 4e-3
+
+
+def oracle_reference(w, o=None, row_offset=None, row_end=None):
+    """(ref fp64, folded bool, keepalive) for the whole workload."""
+    o = o or oracle.get()
+    he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
+    at, bt, st = he.tables(o)
+    if w.kind == "gather":
+        ra = o.build_moe_row_adapter_decode(w.adapter_slots, w.padded_n, w.active,
+                                            w.has_moe_lora)
+        ref, folded = o.gather_fold(w.x, w.indices, ra, at, bt, st, w.base, w.k_in, w.max_rank,
+                                    w.n_out, w.top_k)
+    elif w.kind == "grouped":
+        ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+        lo = 0 if row_offset is None else row_offset
+        hi = w.rows if row_end is None else row_end
+        ref, folded = o.grouped_fold(w.x, w.expert_offsets, w.src, ra, at, bt, st, w.base,
+                                     w.k_in, w.max_rank, w.n_out, w.top_k, lo, hi)
+    else:
+        ref, folded = o.router_fold(w.x, None, at, bt, st, w.base, w.k_in, w.max_rank, w.n_out)
+    return ref, folded, (he, at.size)
+
+
+def check_fold(out_bits: np.ndarray, base_bits: np.ndarray, ref: np.ndarray,
+               folded: np.ndarray, tol: float = TOL) -> dict:
+    """Assert the comparison rules; returns error statistics."""
+    out_bits = np.asarray(out_bits, np.uint16)
+    base_bits = np.asarray(base_bits, np.uint16)
+    assert out_bits.shape == ref.shape == base_bits.shape
+    keep = ~folded
+    if keep.any():
+        diff = out_bits[keep] != base_bits[keep]
+        assert not diff.any(), f"{int(diff.sum())} elements of unfolded rows changed"
+    stats = {"rows": int(folded.size), "folded_rows": int(folded.sum()), "max_err": 0.0,
+             "max_rel": 0.0}
+    if folded.any():
+        out = synth.bf16_to_f32(out_bits[folded]).astype(np.float64)
+        r = ref[folded]
+        err = np.abs(out - r)
+        bound = tol * np.maximum(1.0, np.abs(r))
+        worst = np.argmax(err - bound)
+        assert np.all(err <= bound), (
+            f"{int((err > bound).sum())} folded elements out of tolerance; worst "
+            f"out={out.flat[worst]!r} ref={r.flat[worst]!r}")
+        stats["max_err"] = float(err.max())
+        stats["max_rel"] = float((err / bound).max())
+    return stats

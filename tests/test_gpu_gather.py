@@ -1,0 +1,161 @@
+"""GPU parity of mlg_gather_bgmv (decode fold) against the fp64 oracle.
+
+Every element of every row is compared: folded elements within
+4e-3 * max(1, |ref|), all other elements bit-identical, guard rows untouched.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import fold_harness as fh  # noqa: E402
+import lora_moe_expert_gb300 as mlg  # noqa: E402
+from lora_moe_expert_gb300 import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mlg.lib()
+    mlg.mlg_read_device_errors(clear=True)
+    yield
+    torch.cuda.synchronize()
+    assert mlg.mlg_read_device_errors(clear=True) == 0
+
+
+def _run_and_check(w, guard_rows=3, tol=fh.TOL):
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    prob = FoldProblem(w, guard_rows=guard_rows)
+    ref, folded, keep = fh.oracle_reference(w)
+    assert keep[1] == prob.n_experts  # both sides packed the same table length
+    prob.run()
+    torch.cuda.synchronize()
+    stats = fh.check_fold(prob.base_bits(), w.base, ref, folded, tol)
+    assert np.all(prob.guard_bits() == 0x7FC1), "guard rows changed"
+    return prob, stats, folded
+
+
+def test_tiny_decode():
+    w = synth.tiny_decode()
+    _, stats, folded = _run_and_check(w)
+    # rows of token 0 slot 1 and token 2 slot 0 fold; id 9, ids 1/3 and the
+    # Skip / Refuse tokens keep their input
+    assert stats["folded_rows"] == int(folded.sum()) > 0
+
+
+def test_decode_down_full():
+    _, stats, folded = _run_and_check(synth.decode_down())
+    assert folded.all()
+
+
+def test_decode_gate_up_full():
+    w = synth.decode_gate_up()
+    _, stats, folded = _run_and_check(w)
+    assert 0 < folded.sum() < folded.size
+
+
+SHAPES = [
+    # (tokens, top_k, experts, k_in, n_out, max_rank, adapted, base, pad, bad_ids)
+    (7, 3, 5, 8, 8, 8, 1.0, 0.0, 0, 0),
+    (13, 2, 6, 24, 40, 24, 0.7, 0.3, 2, 3),
+    (33, 4, 4, 776, 136, 16, 1.0, 0.2, 0, 0),  # > 32 rows per expert, k tail
+    (64, 2, 2, 200, 1000, 40, 1.0, 0.0, 0, 0),  # many row groups per expert
+    (5, 8, 700, 264, 72, 56, 0.5, 0.0, 0, 2),  # table longer than the cluster cap
+    (20, 6, 40, 4104, 48, 64, 0.6, 0.1, 3, 2),
+    (9, 1, 4, 2048, 8200, 32, 1.0, 0.0, 0, 0),
+    (1, 1, 1, 64, 64, 8, 1.0, 0.0, 0, 0),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s[:6])))
+def test_gather_shapes(shape):
+    T, K, E, k_in, n_out, r, adapted, base, pad, bad = shape
+    w = synth.custom_gather(100 + T, T, K, E, k_in, n_out, r, adapted_frac=adapted,
+                            base_frac=base, pad=pad, bad_ids=bad)
+    _run_and_check(w)
+
+
+def test_smaller_true_rank_zero_padded():
+    w = synth.custom_gather(5, 16, 4, 8, 512, 256, 64, rank=20)
+    _run_and_check(w)
+
+
+@pytest.mark.parametrize("cs", [1, 2, 4, 8])
+def test_cluster_sizes(cs):
+    """Every cluster size meets the tolerance, and repeats of one size are bit-exact
+    (fixed-order reductions; only the k split, hence the fp32 summation order,
+    differs between sizes)."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_gather(77, 24, 8, 32, 1024, 512, 32, adapted_frac=0.8, base_frac=0.2)
+    ref, folded, _ = fh.oracle_reference(w)
+    try:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_CLUSTER, cs)
+        prob = FoldProblem(w)
+        outs = []
+        for _ in range(2):
+            prob.reset()
+            prob.run()
+            torch.cuda.synchronize()
+            outs.append(prob.base_bits())
+        fh.check_fold(outs[0], w.base, ref, folded)
+        assert np.array_equal(outs[0], outs[1])
+    finally:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_CLUSTER, 0)
+
+
+def test_repeat_is_deterministic_and_negative_zero_kept():
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_gather(9, 16, 4, 16, 256, 128, 16, adapted_frac=0.5, base_frac=0.4)
+    w.base[::3] = 0x8000  # -0.0 in a third of the rows
+    ref, folded, _ = fh.oracle_reference(w)
+    prob = FoldProblem(w)
+    prob.run()
+    torch.cuda.synchronize()
+    first = prob.base_bits()
+    fh.check_fold(first, w.base, ref, folded)
+    prob.reset()
+    prob.run()
+    torch.cuda.synchronize()
+    assert np.array_equal(prob.base_bits(), first)
+    assert np.all(first[~folded][::3] == w.base[~folded][::3])
+
+
+def test_cuda_graph_replay_matches_eager():
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.decode_down()
+    prob = FoldProblem(w)
+    prob.run()
+    torch.cuda.synchronize()
+    eager = prob.base_bits()
+    prob.reset()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            prob.run(stream=s)
+    prob.reset()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(prob.base_bits(), eager)
+
+
+def test_device_side_errors_are_status_codes():
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.tiny_decode()
+    prob = FoldProblem(w)
+    with pytest.raises(mlg.MlgError) as ei:
+        mlg.mlg_gather_bgmv(prob.x.data_ptr() + 2, prob.indices, prob.row_adapter, prob.a_table,
+                            prob.b_table, prob.scale_table, prob.base, w.rows, w.k_in,
+                            w.max_rank, w.n_out, w.top_k, prob.n_experts)
+    assert ei.value.status == mlg.MLG_ERR_UNSUPPORTED
+    assert np.array_equal(prob.base_bits(), w.base)

@@ -1,0 +1,224 @@
+"""GPU parity of mlg_grouped_down (prefill fold) and mlg_router_fold against the
+fp64 oracle: every element of every row (sampled rows at the largest size),
+folded elements within 4e-3 * max(1, |ref|), everything else bit-identical."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import fold_harness as fh  # noqa: E402
+import oracle  # noqa: E402
+import lora_moe_expert_gb300 as mlg  # noqa: E402
+from lora_moe_expert_gb300 import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mlg.lib()
+    mlg.mlg_read_device_errors(clear=True)
+    yield
+    torch.cuda.synchronize()
+    assert mlg.mlg_read_device_errors(clear=True) == 0
+
+
+def _run_and_check(w, guard_rows=3):
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    prob = FoldProblem(w, guard_rows=guard_rows)
+    ref, folded, keep = fh.oracle_reference(w)
+    assert keep[1] == prob.n_experts
+    prob.run()
+    torch.cuda.synchronize()
+    stats = fh.check_fold(prob.base_bits(), w.base, ref, folded)
+    assert np.all(prob.guard_bits() == 0x7FC1), "guard rows changed"
+    return prob, stats, folded
+
+
+def test_small_grouped_multiple_windows():
+    w = synth.custom_grouped(5, [70, 130, 60], 4, 16, 256, 512, 32, cap=300, adapted_frac=0.8)
+    _, stats, folded = _run_and_check(w)
+    assert 0 < folded.sum() < folded.size
+
+
+def test_prefill_down_full():
+    _, stats, folded = _run_and_check(synth.prefill_down())
+    assert folded.all()
+
+
+GROUPED_SHAPES = [
+    # (lengths, top_k, experts, k_in, n_out, max_rank, cap, adapted, stream_base)
+    ([5, 9], 2, 4, 64, 64, 8, 1000, 1.0, None),
+    ([33, 17, 80], 3, 7, 72, 72, 24, 50, 0.6, [0, 1, 0]),
+    ([200], 4, 5, 200, 1000, 40, 128, 1.0, None),
+    ([64, 64], 2, 3, 1000, 8, 48, 97, 1.0, None),
+    ([150, 40], 6, 30, 520, 328, 64, 256, 0.5, [1, 0]),
+    ([300], 8, 64, 128, 136, 16, 1 << 20, 0.9, None),
+    ([1], 1, 1, 64, 64, 8, 1, 1.0, None),
+]
+
+
+@pytest.mark.parametrize("shape", GROUPED_SHAPES, ids=lambda s: f"{sum(s[0])}x{s[1]}_{s[3]}_{s[4]}_r{s[5]}")
+def test_grouped_shapes(shape):
+    lengths, K, E, k_in, n_out, r, cap, adapted, sb = shape
+    w = synth.custom_grouped(200 + k_in, lengths, K, E, k_in, n_out, r, cap=cap,
+                             adapted_frac=adapted, stream_base=sb)
+    _run_and_check(w)
+
+
+def test_smaller_true_rank_zero_padded():
+    w = synth.custom_grouped(31, [100, 50], 4, 8, 256, 256, 64, cap=90, rank=20)
+    _run_and_check(w)
+
+
+def test_window_split_is_bit_exact():
+    """Any window split gives the bits of one window (each row's arithmetic is
+    independent of which tile it lands in)."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_grouped(8, [120, 260, 90], 4, 12, 192, 384, 32, cap=1 << 20,
+                             adapted_frac=0.75, stream_base=[0, 1, 0])
+    outs = []
+    for cap in (1 << 20, 128, 77, 5):
+        w.cap = cap
+        prob = FoldProblem(w)
+        prob.run()
+        torch.cuda.synchronize()
+        outs.append(prob.base_bits())
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    ref, folded, _ = fh.oracle_reference(w)
+    fh.check_fold(outs[0], w.base, ref, folded)
+
+
+def test_negative_zero_and_repeat():
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_grouped(12, [90, 70], 4, 10, 128, 256, 16, cap=100, adapted_frac=0.6,
+                             stream_base=[1, 0])
+    w.base[::2] = 0x8000
+    ref, folded, _ = fh.oracle_reference(w)
+    prob = FoldProblem(w)
+    prob.run()
+    torch.cuda.synchronize()
+    first = prob.base_bits()
+    fh.check_fold(first, w.base, ref, folded)
+    prob.reset()
+    prob.run()
+    torch.cuda.synchronize()
+    assert np.array_equal(prob.base_bits(), first)
+
+
+def test_router_small_and_row_map():
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_router(6, 200, 512, 256, 32)
+    _run_and_check(w)
+    # with a row map: negative tokens keep their input
+    prob = FoldProblem(w)
+    ra_host = np.where(np.arange(200) % 3 == 0, -1, 0).astype(np.int32)
+    ra = torch.from_numpy(ra_host).cuda()
+    mlg.mlg_router_fold(prob.x, ra, prob.a_table, prob.b_table, prob.scale_table, prob.base,
+                        w.rows, w.k_in, w.max_rank, w.n_out)
+    torch.cuda.synchronize()
+    o = oracle.get()
+    he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
+    at, bt, st = he.tables(o)
+    ref, folded = o.router_fold(w.x, ra_host, at, bt, st, w.base, w.k_in, w.max_rank, w.n_out)
+    fh.check_fold(prob.base_bits(), w.base, ref, folded)
+
+
+def test_router_zero_cell_is_noop():
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_router(7, 64, 128, 64, 16)
+    prob = FoldProblem(w)
+    zero = torch.zeros(1, dtype=torch.int64, device="cuda")
+    mlg.mlg_router_fold(prob.x, None, zero, prob.b_table, prob.scale_table, prob.base, w.rows,
+                        w.k_in, w.max_rank, w.n_out)
+    torch.cuda.synchronize()
+    assert np.array_equal(prob.base_bits(), w.base)
+
+
+def test_router_full():
+    _, stats, folded = _run_and_check(synth.router())
+    assert folded.all()
+
+
+def test_prefill_large_sampled():
+    """The 163840-row prefill at full size, in the window split and launch
+    configuration the benchmark uses; 256 sampled rows checked against the
+    oracle one by one (every row folds here)."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.prefill_large()
+    prob = FoldProblem(w)
+    prob.run()
+    torch.cuda.synchronize()
+    out = prob.base.view(torch.int16)
+    rng = np.random.default_rng(99)
+    rows = np.unique(np.concatenate([rng.integers(0, w.rows, 250),
+                                     [0, 1, w.rows - 1] + [int(v) for v in w.expert_offsets[1:6]]]))
+    rows = rows[rows < w.rows].astype(np.int32)
+    got = out[torch.from_numpy(rows).long().cuda()].cpu().numpy().view(np.uint16)
+    o = oracle.get()
+    he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
+    at, bt, st = he.tables(o)
+    ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+    ref, folded = o.grouped_fold_rows(w.x, w.expert_offsets, w.src, ra, at, bt, st,
+                                      w.base[rows], rows, w.k_in, w.max_rank, w.n_out, w.top_k,
+                                      0, w.rows)
+    assert folded.all()
+    fh.check_fold(got, w.base[rows], ref, folded)
+
+
+def test_cuda_graph_replay_matches_eager():
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_grouped(3, [300, 200, 100], 8, 32, 256, 512, 32, cap=1000)
+    prob = FoldProblem(w)
+    prob.run()
+    torch.cuda.synchronize()
+    eager = prob.base_bits()
+    prob.reset()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            prob.run(stream=s)
+    prob.reset()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(prob.base_bits(), eager)
+
+
+def test_grouped_matches_gather_form():
+    """Cross-form: the same decode batch folded through the grouped kernel on
+    expert-sorted rows equals the gather kernel's result un-permuted, within
+    the tolerance (the two kernels sum in different orders)."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    g = synth.custom_gather(41, 96, 4, 16, 256, 384, 32, adapted_frac=0.7, base_frac=0.2)
+    gp = FoldProblem(g)
+    gp.run()
+    torch.cuda.synchronize()
+    gather_out = gp.base_bits()
+    offsets, src = synth.sort_rows_by_expert(g.indices, g.n_experts_model)
+    row_map = gp.row_map_host
+    sp = FoldProblem(g)  # reuse allocations for x / tables; sorted base below
+    sorted_base = torch.from_numpy(g.base[src].view(np.int16)).cuda().view(torch.bfloat16)
+    mlg.mlg_grouped_down(sp.x, torch.from_numpy(offsets).cuda(), torch.from_numpy(src).cuda(),
+                         torch.from_numpy(row_map).cuda(), sp.a_table, sp.b_table,
+                         sp.scale_table, sorted_base, g.k_in, g.max_rank, g.n_out, g.top_k,
+                         sp.n_experts, 0, src.size)
+    torch.cuda.synchronize()
+    grouped_out = np.empty_like(gather_out)
+    grouped_out[src] = sorted_base.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref, folded, _ = fh.oracle_reference(g)
+    fh.check_fold(grouped_out, g.base, ref, folded)
+    fh.check_fold(gather_out, g.base, ref, folded)

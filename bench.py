@@ -1,0 +1,515 @@
+"""Benchmark of the MoE expert LoRA fold on GB300 (prints ONE JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the hot path over one batch of synthetic input: one
+fold launch for the decode workloads, one launch per row window for the
+prefill workloads, one router-fold launch for the router.  The default
+workload is the decode gather BGMV at the down-projection shape (64 tokens,
+top-8, 128 experts at rank 16, k_in 768, n_out 2048).
+
+value      rows folded-or-skipped per second over the timed steps (all ranks),
+           device-timed with CUDA events around a CUDA-graph replay of the K
+           steps; the steps rotate over input sets whose total size exceeds L2
+           (each step's inputs are cold in L2), inputs resident in HBM.
+e2e        the same metric through the C ABI with host buffers: per step the
+           host route + row map and table packing, pinned host->device copies
+           of x, routing, row map, tables and base_out, the fold, and the
+           device->host copy of base_out, wall-clock timed with a device sync.
+roofline   algorithmic bytes of one launch / its mean duration vs the measured
+           HBM copy bandwidth of this GPU model (MEASURED_PEAKS.json).
+cpu_baseline / --impl reference
+           the fp64 CPU oracle as it stands, single-threaded, on a bounded
+           sample of the same workload.
+Multi-GPU (torchrun): replicas -- every rank folds its own copy of the
+workload, no collective on the data path; barrier + max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE LoRA fold rows/s and achieved HBM GB/s (% of GB300 roofline), 1 GPU"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+# workload name -> (generator, description)
+WORKLOADS = {
+    "decode_down": "decode gather BGMV, down-proj: 64 tokens x top-8 (512 rows), 128 experts "
+                   "all adapted, rank 16, k_in 768, n_out 2048, bf16",
+    "decode_gate_up": "decode gather BGMV, gate/up: 256 tokens x top-8 (2048 rows), 64 of 128 "
+                      "experts adapted, rank 64, k_in 2048, n_out 768; 154 active / 64 base / 38 pad",
+    "prefill_down": "prefill grouped fold, down-proj: 8 streams U[256,768] tokens x top-8, 128 "
+                    "experts, rank 16, k_in 768, n_out 2048, skewed routing, windows of 8192 rows",
+    "prefill_large": "large prefill grouped fold: 16384 tokens x top-10 (163840 rows), 512 experts, "
+                     "rank 32, k_in 512, n_out 2048, skewed routing, windows of 32768 rows",
+    "router": "router fold (one-entry route): 16384 tokens, k_in 2048, n_out 512, rank 32",
+    "tiny_decode": "tiny decode gather fold: 4 tokens x top-2, 8 experts (2 unadapted), rank 8",
+}
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_src, workload):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    is unchanged since it was captured; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+        ent = rec[workload]
+        if ent["source_sha"] != source_hash(os.path.join(ROOT, kernel_src)):
+            return None
+        return ent["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def algorithmic(w, row_map, tables):
+    """(rows, folded_rows, bytes, flops) of one step: the bytes the method must
+    move -- x rows of tokens with a folding row, A_e + B_e of each expert hit,
+    the base_out read + write of each folding row, and the index arrays."""
+    a, b, _ = tables
+    E = a.size
+    if w.kind == "gather":
+        rows = w.indices.size
+        tok = np.arange(rows) // w.top_k
+        e = w.indices.astype(np.int64)
+    elif w.kind == "grouped":
+        rows = w.rows
+        e = np.repeat(np.arange(w.n_experts_model), np.diff(w.expert_offsets))
+        e = np.concatenate([e, np.full(rows - e.size, -1)])
+        tok = w.src // w.top_k
+    else:
+        rows = w.rows
+        e = np.zeros(rows, np.int64)
+        tok = np.arange(rows)
+    ok = (e >= 0) & (e < E)
+    ec = np.clip(e, 0, max(E - 1, 0))
+    ok &= (a[ec] != 0) & (b[ec] != 0)
+    if row_map is not None:
+        ok &= row_map[tok] >= 0
+    folded = int(ok.sum())
+    experts = np.unique(e[ok]).size
+    tokens = np.unique(tok[ok]).size
+    r, k, n = w.max_rank, w.k_in, w.n_out
+    idx_bytes = rows * 4 + (row_map.size * 4 if row_map is not None else 0) + E * 20
+    if w.kind == "grouped":
+        idx_bytes += (w.n_experts_model + 1) * 4
+    nbytes = tokens * k * 2 + experts * r * (k + n) * 2 + folded * n * 4 + idx_bytes
+    flops = 2 * folded * r * (k + n)
+    return rows, folded, int(nbytes), int(flops)
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[4:8]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle timing
+def time_oracle(w, budget_s=10.0):
+    """The fp64 oracle as it stands on host cores, on a bounded sample of the
+    workload: whole-workload passes for small workloads, else a row sample
+    (sampled rows / elapsed).  Returns (rows_per_s, sample description)."""
+    import oracle
+
+    o = oracle.get()
+    he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
+    at, bt, st = he.tables(o)
+    flops_row = 2 * w.max_rank * (w.k_in + w.n_out)
+    full_cost = w.rows * flops_row
+    rng = np.random.default_rng(0)
+    t0 = time.perf_counter()
+    done = 0
+    passes = 0
+    if full_cost <= 2e9:
+        while time.perf_counter() - t0 < budget_s or passes == 0:
+            if w.kind == "gather":
+                ra = o.build_moe_row_adapter_decode(w.adapter_slots, w.padded_n, w.active,
+                                                    w.has_moe_lora)
+                o.gather_fold(w.x, w.indices, ra, at, bt, st, w.base, w.k_in, w.max_rank,
+                              w.n_out, w.top_k)
+            elif w.kind == "grouped":
+                ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+                for s, e in o.grouped_down_windows(w.rows, w.cap):
+                    o.grouped_fold(w.x, w.expert_offsets, w.src, ra, at, bt, st, w.base, w.k_in,
+                                   w.max_rank, w.n_out, w.top_k, s, e)
+            else:
+                o.router_fold(w.x, None, at, bt, st, w.base, w.k_in, w.max_rank, w.n_out)
+            done += w.rows
+            passes += 1
+        dt = time.perf_counter() - t0
+        return done / dt, f"{passes} whole-workload pass(es) of {w.rows} rows in {dt:.1f} s"
+    chunk = 64
+    while time.perf_counter() - t0 < budget_s:
+        rows = np.sort(rng.choice(w.rows, size=chunk, replace=False)).astype(np.int32)
+        if w.kind == "grouped":
+            ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+            o.grouped_fold_rows(w.x, w.expert_offsets, w.src, ra, at, bt, st, w.base[rows], rows,
+                                w.k_in, w.max_rank, w.n_out, w.top_k, 0, w.rows)
+        elif w.kind == "gather":
+            ra = o.build_moe_row_adapter_decode(w.adapter_slots, w.padded_n, w.active,
+                                                w.has_moe_lora)
+            o.gather_fold_rows(w.x, w.indices, ra, at, bt, st, w.base[rows], rows, w.k_in,
+                               w.max_rank, w.n_out, w.top_k)
+        else:
+            o.gather_fold_rows(w.x, np.zeros(w.rows, np.int32), None, at, bt, st, w.base[rows],
+                               rows, w.k_in, w.max_rank, w.n_out, 1)
+        done += chunk
+    dt = time.perf_counter() - t0
+    return done / dt, f"{done} sampled rows of {w.rows} in {dt:.1f} s (row-by-row oracle)"
+
+
+# ------------------------------------------------------------------ GPU arm
+def n_sets_for(w_bytes):
+    return max(1, min(32, int(np.ceil(2.0 * L2_BYTES / max(w_bytes, 1)))))
+
+
+def kernel_source(kind):
+    return "lora_moe_expert_gb300/csrc/" + ("mlg_gather.cu" if kind == "gather"
+                                            else "mlg_grouped.cu")
+
+
+def gpu_measure(name, steps, warmup, device, seed_base=1000, e2e=True):
+    import torch
+
+    import lora_moe_expert_gb300 as mlg
+    from lora_moe_expert_gb300 import synth
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    gen = synth.NAMED[name]
+    w0 = gen()
+    p0 = FoldProblem(w0, device=device)
+    rows, folded, nbytes, flops = algorithmic(w0, p0.row_map_host, p0.tables_host)
+    ws_bytes = w0.x.nbytes + w0.base.nbytes + sum(e.A.nbytes + e.B.nbytes for e in w0.experts)
+    nsets = n_sets_for(ws_bytes)
+    probs = [p0] + [FoldProblem(gen(seed=seed_base + i), device=device) for i in range(1, nsets)]
+    launches_per_step = len(p0.windows) if w0.kind == "grouped" else 1
+
+    stream = torch.cuda.Stream(device=device)
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):  # eager warm-up steps
+            probs[i % nsets].run(stream=stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(steps):
+                probs[i % nsets].run(stream=stream)
+        for _ in range(max(warmup, 3)):  # warm-up replays of the timed graph
+            graph.replay()
+        stream.synchronize()
+    errors_before = mlg.mlg_read_device_errors(clear=True)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize(device)
+    ms_total = e0.elapsed_time(e1)
+    if mlg.mlg_read_device_errors(clear=True) or errors_before:
+        raise RuntimeError("device error bits were set during the benchmark")
+    out = {"rows": rows, "folded_rows": folded, "alg_bytes": nbytes, "alg_flops": flops,
+           "ms_total": ms_total, "launches_per_step": launches_per_step, "sets": nsets,
+           "set_bytes": ws_bytes, "clocks": clocks.summary(), "kind": w0.kind}
+    if e2e:
+        out["e2e"] = e2e_measure(probs[0], max(3, min(steps, 50)), device)
+    del graph
+    return out
+
+
+def e2e_measure(prob, steps, device):
+    """Through the public API with host buffers: route + map and table packing on
+    the host, pinned H2D copies of the step's inputs, the fold, D2H of base_out."""
+    import torch
+
+    import lora_moe_expert_gb300 as mlg
+
+    w = prob.w
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_x = pin(w.x.view(np.int16))
+    h_base = pin(w.base.view(np.int16))
+    h_out = torch.empty_like(h_base).pin_memory()
+    h_idx = pin(w.indices) if w.kind == "gather" else None
+    h_off = pin(w.expert_offsets) if w.kind == "grouped" else None
+    h_src = pin(w.src) if w.kind == "grouped" else None
+    s = torch.cuda.Stream(device=device)
+    h2d = d2h = 0
+
+    def step():
+        nonlocal h2d, d2h
+        h2d = d2h = 0
+        with torch.cuda.stream(s):
+            if w.kind == "gather":
+                m = mlg.mlg_build_moe_row_adapter_decode(w.adapter_slots, w.padded_n, w.active,
+                                                         w.has_moe_lora)
+            elif w.kind == "grouped":
+                m = mlg.mlg_build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+            else:
+                m = None
+            a, b, sc = mlg.mlg_pack_expert_tables(prob.pool.ids, prob.pool.a_addr,
+                                                  prob.pool.b_addr, prob.pool.scale)
+            mlg.mlg_upload_expert_tables(a, b, sc, prob.a_table, prob.b_table, prob.scale_table,
+                                         stream=s)
+            h2d += a.nbytes + b.nbytes + sc.nbytes
+            if m is not None:
+                mlg.mlg_upload_row_adapter(m, prob.row_adapter, stream=s)
+                h2d += m.nbytes
+            prob.x.view(torch.int16).copy_(h_x, non_blocking=True)
+            prob.base.view(torch.int16).copy_(h_base, non_blocking=True)
+            h2d += h_x.numel() * 2 + h_base.numel() * 2
+            if h_idx is not None:
+                prob.indices.copy_(h_idx, non_blocking=True)
+                h2d += h_idx.numel() * 4
+            if h_off is not None:
+                prob.expert_offsets.copy_(h_off, non_blocking=True)
+                prob.src.copy_(h_src, non_blocking=True)
+                h2d += h_off.numel() * 4 + h_src.numel() * 4
+            prob.run(stream=s)
+            h_out.copy_(prob.base.view(torch.int16), non_blocking=True)
+            d2h += h_out.numel() * 2
+        s.synchronize()
+
+    for _ in range(3):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t0) / steps
+    return {"s_per_step": dt, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps}
+
+
+# ------------------------------------------------------------------ main
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from lora_moe_expert_gb300 import synth
+
+    w = synth.NAMED[args.workload]()
+    steps_rows = []
+    for _ in range(args.warmup):
+        time_oracle(w, budget_s=0.0)
+    t0 = time.perf_counter()
+    samples = []
+    for _ in range(args.steps):
+        rps, desc = time_oracle(w, budget_s=args.ref_budget)
+        steps_rows.append(rps)
+        samples.append(desc)
+    total = time.perf_counter() - t0
+    value = statistics.mean(steps_rows)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "description": WORKLOADS[args.workload],
+                       "parallelism": "none (host oracle)"},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": samples[0]},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_down", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--extra", default="decode_gate_up,prefill_down,prefill_large,router",
+                    help="other workloads measured in the same run (comma list, or 'none')")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+    main_res = gpu_measure(args.workload, args.steps, args.warmup, device,
+                           seed_base=1000 + 97 * rank)
+    ms_step = main_res["ms_total"] / args.steps
+    if ws > 1:
+        t = torch.tensor([ms_step], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)  # timing only
+        ms_step = float(t.item())
+        e2e_s = torch.tensor([main_res["e2e"]["s_per_step"]], device=device)
+        torch.distributed.all_reduce(e2e_s, op=torch.distributed.ReduceOp.MAX)
+        main_res["e2e"]["s_per_step"] = float(e2e_s.item())
+    peak, peak_kind = measured_peaks()
+    per_launch_ms = ms_step / main_res["launches_per_step"]
+    achieved = main_res["alg_bytes"] / main_res["launches_per_step"] / (per_launch_ms * 1e-3) / 1e9
+    extras = {}
+    if args.extra != "none" and rank == 0:
+        for nm in [s for s in args.extra.split(",") if s and s != args.workload]:
+            try:
+                r = gpu_measure(nm, 20, 3, device, e2e=False)
+                pl = r["ms_total"] / 20 / r["launches_per_step"]
+                a = r["alg_bytes"] / r["launches_per_step"] / (pl * 1e-3) / 1e9
+                extras[nm] = {"rows_per_s": r["rows"] / (r["ms_total"] / 20 * 1e-3),
+                              "us_per_step": r["ms_total"] / 20 * 1e3,
+                              "launches_per_step": r["launches_per_step"],
+                              "alg_bytes_per_step": r["alg_bytes"],
+                              "achieved_gbs": a, "frac_of_peak": a / peak,
+                              "tflops": r["alg_flops"] / (r["ms_total"] / 20 * 1e-3) / 1e12,
+                              "traffic": recorded_traffic(kernel_source(r["kind"]), nm),
+                              "l2": f"{r['sets']} rotating input sets of "
+                                    f"{r['set_bytes'] / 2**20:.0f} MiB"}
+            except Exception as ex:  # report, do not hide
+                extras[nm] = {"error": repr(ex)[:300]}
+    if rank != 0:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+        return 0
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        from lora_moe_expert_gb300 import synth
+
+        rps, desc = time_oracle(synth.NAMED[args.workload](), budget_s=10.0)
+        cpu = {"value": rps, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc}
+    e2e = main_res["e2e"]
+    line = {
+        "metric": METRIC,
+        "value": ws * main_res["rows"] / (ms_step * 1e-3),
+        "unit": "rows/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "description": WORKLOADS[args.workload],
+                   "rows_per_step": main_res["rows"], "folded_rows_per_step": main_res["folded_rows"],
+                   "l2": f"inputs rotate over {main_res['sets']} sets of "
+                         f"{main_res['set_bytes'] / 2**20:.1f} MiB (> L2 in total)",
+                   "timing": "CUDA events around one CUDA-graph replay of the timed steps",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "alg_bytes_per_launch": main_res["alg_bytes"] // main_res["launches_per_step"],
+                     "traffic": recorded_traffic(kernel_source(main_res["kind"]), args.workload)},
+        "tflops": main_res["alg_flops"] / (ms_step * 1e-3) / 1e12,
+        "cpu_baseline": cpu,
+        "e2e": {"value": ws * main_res["rows"] / e2e["s_per_step"], "unit": "rows/s",
+                "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},
+        "gpu_launches": args.steps * main_res["launches_per_step"],
+        "clocks": main_res["clocks"],
+        "workloads": extras,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -150,6 +150,22 @@ MLG_API mlg_status mlg_grouped_down(const mlg_bf16 *x, const int32_t *expert_off
                             int32_t top_k, int32_t n_experts, int32_t row_offset,
                             int32_t row_end, void *stream);
 
+/* All windows of grouped_down_windows(total_rows, cap) folded in ONE launch:
+ * the same result, bit for bit, as calling mlg_grouped_down for each window
+ * [i*cap, min((i+1)*cap, total_rows)) in turn, because every tile of the
+ * kernel lies inside one window and one expert span and each row's arithmetic
+ * does not depend on its tile.  One persistent launch instead of one per
+ * window removes the per-window pipeline fill and tail.  Arguments as for
+ * mlg_grouped_down with row_offset = 0, row_end = total_rows.  Errors as for
+ * mlg_grouped_down, plus CAP_ZERO for cap == 0. */
+MLG_API mlg_status mlg_grouped_down_all_windows(const mlg_bf16 *x, const int32_t *expert_offsets,
+                                                const int32_t *src, const int32_t *row_adapter,
+                                                const uint64_t *a_table, const uint64_t *b_table,
+                                                const float *scale_table, mlg_bf16 *base_out,
+                                                int32_t k_in, int32_t max_rank, int32_t n_out,
+                                                int32_t top_k, int32_t n_experts,
+                                                int32_t total_rows, uint32_t cap, void *stream);
+
 /* The router fold (MoeExpertRoute, moe_lora_grouped module index): a one-entry
  * route whose expert 0 is the router pair, so every token t folds
  * base_out[t] += scale_0 * (x[t] @ A_0^T) @ B_0^T.  The tables have one entry;

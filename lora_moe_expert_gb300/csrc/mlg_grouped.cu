@@ -36,14 +36,17 @@
 namespace mlg {
 namespace {
 
-constexpr int kGThreads = 256;
+constexpr int kGThreads = 384;      // 4 role warps + 8 epilogue warps
+constexpr int kEpiWarps = 8;
 constexpr int kTileM = MLG_M_TILE;   // 128 rows per tile
 constexpr int kBoxRows = 32;         // rows per TMA box (one epilogue warp)
 constexpr int kBoxCols = 64;         // bf16 columns per TMA box (128 bytes)
 constexpr int kMaxDepth = 8;         // base-ring stages per epilogue warp
-constexpr int kMaxStages = 4;        // operand ring stages
+constexpr int kMaxStages = 6;        // operand ring stages
+constexpr int kMyTilesMax = 16;      // per-CTA tile list capacity
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemH = 0, kTmemAcc0 = 128, kTmemAcc1 = 256;
+// TMEM columns: two h buffers (tile parity), two expand accumulators.
+constexpr uint32_t kTmemH0 = 0, kTmemH1 = 64, kTmemAcc0 = 128, kTmemAcc1 = 256;
 
 static __device__ uint32_t g_grouped_errors;
 
@@ -57,13 +60,16 @@ struct GroupedParams {
   const float *scale_table;
   uint8_t *base_out;             // bf16 [>= row_end, n_out]
   int32_t k_in, rank, n_out, top_k, n_experts, row_offset, row_end;
+  int32_t win;                   // window length (windows start at row_offset + i * win)
   int32_t r_pad;                 // rank rounded up to 16 (shrink N)
   int32_t k_exp;                 // expand K: [hi | lo] padded to a multiple of 64
   int32_t n_ch;                  // expand N per accumulator chunk (64 or 128)
   int32_t kc_count, nc_count, nbx;  // k chunks, n chunks, 64-column boxes per row
   int32_t nxa, nbs, depth;       // ring stages
+  int32_t xa_lag;                // X/A stages in flight before one is signalled
   uint32_t xa_stage, b_stage;    // bytes per stage
-  uint32_t off_xa, off_b, off_h, off_base, off_tab, smem_bytes;
+  uint32_t off_xa, off_b, off_h, off_base, off_tab, off_my, smem_bytes;
+  int32_t my_cap;                // tiles per CTA the tile list holds
 };
 
 // Byte offset of 16-byte chunk `c` (of 8 per 128-byte row) of row `row` in a
@@ -75,9 +81,9 @@ __device__ __forceinline__ uint32_t sw128(int row, int c) {
 struct Ctl {
   uint64_t xa_full[kMaxStages], xa_empty[kMaxStages];
   uint64_t b_full[kMaxStages], b_empty[kMaxStages];
-  uint64_t h_full, hs_full, hs_empty, drain;
+  uint64_t h_full[2], hs_full, hs_empty, drain;
   uint64_t acc_full[2], acc_empty[2];
-  uint64_t base_full[4][kMaxDepth];
+  uint64_t base_full[kEpiWarps][kMaxDepth];
   uint32_t tmem_base;
   volatile int abort_flag;
 };
@@ -111,8 +117,21 @@ __device__ __forceinline__ int span_hi(const GroupedParams &p, int e) {
   return min(hi, p.row_end);
 }
 
-// Tile t of the window: the expert owning it (tile_start is an exclusive
-// prefix over experts) and its rows [r0, r1).
+// Tiles of one expert span [lo, hi): runs of <= 128 rows that also never
+// cross a window boundary (boundaries at row_offset + i * win).
+__device__ __forceinline__ int span_tiles(const GroupedParams &p, int lo, int hi) {
+  if (hi <= lo) return 0;
+  const int ro = p.row_offset, W = p.win;
+  const int w0 = (lo - ro) / W, w1 = (hi - 1 - ro) / W;
+  if (w0 == w1) return (hi - lo + kTileM - 1) / kTileM;
+  const int first = ro + (w0 + 1) * W - lo;
+  const int last = hi - (ro + w1 * W);
+  return (first + kTileM - 1) / kTileM + (w1 - w0 - 1) * ((W + kTileM - 1) / kTileM) +
+         (last + kTileM - 1) / kTileM;
+}
+
+// Tile t: the expert owning it (tile_start is an exclusive prefix over
+// experts) and its rows [r0, r1).
 __device__ TileInfo tile_info(const GroupedParams &p, const int *tile_start, int n_e, int t) {
   int lo = 0, hi = n_e - 1;  // largest e with tile_start[e] <= t
   while (lo < hi) {
@@ -121,23 +140,47 @@ __device__ TileInfo tile_info(const GroupedParams &p, const int *tile_start, int
   }
   TileInfo ti;
   ti.e = lo;
-  ti.r0 = span_lo(p, lo) + (t - tile_start[lo]) * kTileM;
-  ti.r1 = min(ti.r0 + kTileM, span_hi(p, lo));
+  const int slo = span_lo(p, lo), shi = span_hi(p, lo);
+  const int ro = p.row_offset, W = p.win;
+  int u = t - tile_start[lo];
+  // walk the window pieces of the span (O(1) per piece type)
+  const int w0 = (slo - ro) / W;
+  int a = slo;
+  int b = min(shi, ro + (w0 + 1) * W);
+  int n = (b - a + kTileM - 1) / kTileM;
+  if (u >= n) {
+    u -= n;
+    const int per = (W + kTileM - 1) / kTileM;  // tiles of one whole window
+    const int w = w0 + 1 + u / per;
+    u %= per;
+    a = ro + w * W;
+    b = min(shi, a + W);
+  }
+  ti.r0 = a + u * kTileM;
+  ti.r1 = min(ti.r0 + kTileM, b);
   return ti;
 }
+
+// Per-CTA tile list entry, built once in the prologue: expert, rows, scale,
+// and a bitmask of the tile rows that fold.
+struct MyTile {
+  int e, r0, r1;
+  float scale;
+  uint32_t fold[4];
+};
 
 __device__ __forceinline__ bool cells_fold(uint64_t a, uint64_t b) {
   return a != 0 && b != 0 && ((a | b) & 15u) == 0;
 }
 
-__device__ __forceinline__ uint32_t pack8_add(const uint4 b, const float *v, uint4 &out) {
+// out = RNE_bf16(base + v) for 8 consecutive elements (base given as bf16 bits).
+__device__ __forceinline__ uint4 add8_bf16(const uint4 b, const float *v) {
   const uint32_t w[4] = {b.x, b.y, b.z, b.w};
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
     o[i] = pack_bf16x2(bf16lo_to_f32(w[i]) + v[2 * i], bf16hi_to_f32(w[i]) + v[2 * i + 1]);
-  out = make_uint4(o[0], o[1], o[2], o[3]);
-  return 0;
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 template <int RP>  // rank rounded up to a multiple of 16
@@ -156,20 +199,21 @@ __global__ void __launch_bounds__(kGThreads, 1)
   // ---- prologue: barriers, zeroed operand padding, tile table, TMEM ------
   if (tid == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(smem_addr(&ctl.xa_full[s]), 32);
+      mbar_init(smem_addr(&ctl.xa_full[s]), 64);
       mbar_init(smem_addr(&ctl.xa_empty[s]), 1);
       mbar_init(smem_addr(&ctl.b_full[s]), 32);
       mbar_init(smem_addr(&ctl.b_empty[s]), 1);
     }
-    mbar_init(smem_addr(&ctl.h_full), 1);
+    mbar_init(smem_addr(&ctl.h_full[0]), 1);
+    mbar_init(smem_addr(&ctl.h_full[1]), 1);
     mbar_init(smem_addr(&ctl.hs_full), 4);
     mbar_init(smem_addr(&ctl.hs_empty), 1);
     mbar_init(smem_addr(&ctl.drain), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_addr(&ctl.acc_full[s]), 1);
-      mbar_init(smem_addr(&ctl.acc_empty[s]), 4);
+      mbar_init(smem_addr(&ctl.acc_empty[s]), kEpiWarps);
     }
-    for (int w = 0; w < 4; ++w)
+    for (int w = 0; w < kEpiWarps; ++w)
       for (int s = 0; s < kMaxDepth; ++s) mbar_init(smem_addr(&ctl.base_full[w][s]), 1);
     ctl.abort_flag = 0;
     fence_mbar_init();
@@ -196,7 +240,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const int lo = span_lo(p, e), hi = span_hi(p, e);
           if (hi > lo && cells_fold(__ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + e),
                                     __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + e)))
-            n = (hi - lo + kTileM - 1) / kTileM;
+            n = span_tiles(p, lo, hi);
         }
         cnt[i] = n;
         sum += n;
@@ -228,6 +272,34 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
     if (tid == 0) tile_start[n_e] = carry;
   }
+  __syncthreads();
+  // This CTA's tiles (t = blockIdx.x + i * gridDim.x): expert, rows, scale,
+  // and which rows fold (a span row with src >= 0 whose token's row-map entry
+  // is not negative).  The epilogue reads only this list.
+  MyTile *my_tiles = reinterpret_cast<MyTile *>(smem + p.off_my);
+  const int n_tiles_all = tile_start[n_e];
+  int my_count = 0;
+  if (static_cast<int>(blockIdx.x) < n_tiles_all)
+    my_count = min(p.my_cap, (n_tiles_all - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1);
+  if (tid < my_count) {
+    const TileInfo ti = tile_info(p, tile_start, n_e, blockIdx.x + tid * gridDim.x);
+    my_tiles[tid].e = ti.e;
+    my_tiles[tid].r0 = ti.r0;
+    my_tiles[tid].r1 = ti.r1;
+    my_tiles[tid].scale = __ldg(p.scale_table + ti.e);
+  }
+  __syncthreads();
+  for (int i = warp; i < my_count * 4; i += kGThreads / 32) {  // one warp per 32 rows
+    const MyTile mt = my_tiles[i >> 2];
+    const int r = mt.r0 + (i & 3) * 32 + lane;
+    bool f = false;
+    if (r < mt.r1) {
+      const int sr = p.src ? __ldg(p.src + r) : r;
+      f = sr >= 0 && (p.row_adapter == nullptr || __ldg(p.row_adapter + sr / p.top_k) >= 0);
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) my_tiles[i >> 2].fold[i & 3] = m;
+  }
   if (warp == 0) {
     tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
     tmem_relinquish();
@@ -236,7 +308,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
-  const int n_tiles = tile_start[n_e];
+  const int n_tiles = my_count;  // tiles of this CTA, indexed 0 .. my_count-1
   const uint32_t idesc_shrink = umma_idesc_bf16(kTileM, RP);
   const uint32_t idesc_expand = umma_idesc_bf16(kTileM, p.n_ch);
   const uint32_t xa_base = smem_addr(smem + p.off_xa);
@@ -245,23 +317,36 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
   if (warp == 0) {
     // ================================================================ MMA issuer
+    // Shrink chunks of tile t+1 are issued, as their X / A_e stages arrive,
+    // between the expand chunks of tile t (h of consecutive tiles alternates
+    // between two TMEM buffers), so h is ready when the epilogue needs it.
     if (lane == 0) {
-      uint32_t xa_it = 0, b_it = 0, acc_it = 0, tile_it = 0;
-      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_it) {
-        for (int kc = 0; kc < p.kc_count; ++kc, ++xa_it) {
-          const int st = xa_it % p.nxa;
-          if (!wait_bar(ctl, ctl.xa_full[st], (xa_it / p.nxa) & 1)) goto mma_done;
-          tc_fence_after();
-          const uint32_t xs = xa_base + st * p.xa_stage;
-          const uint32_t as = xs + kTileM * 128;
+      uint32_t xa_it = 0, b_it = 0, acc_it = 0;
+      int sh_t = 0, sh_kc = 0;  // next shrink chunk to issue: tile, k chunk
+      auto issue_shrink_chunk = [&]() {
+        const int st = xa_it % p.nxa;
+        tc_fence_after();
+        const uint32_t xs = xa_base + st * p.xa_stage;
+        const uint32_t as = xs + kTileM * 128;
+        const uint32_t hd = tmem + ((sh_t & 1) ? kTmemH1 : kTmemH0);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_bf16(tmem + kTmemH, umma_desc_sw128(xs + k * 32), umma_desc_sw128(as + k * 32),
-                      idesc_shrink, (kc | k) != 0);
-          umma_commit(smem_addr(&ctl.xa_empty[st]));
+        for (int k = 0; k < 4; ++k)
+          umma_bf16(hd, umma_desc_sw128(xs + k * 32), umma_desc_sw128(as + k * 32), idesc_shrink,
+                    (sh_kc | k) != 0);
+        umma_commit(smem_addr(&ctl.xa_empty[st]));
+        ++xa_it;
+        if (++sh_kc == p.kc_count) {
+          umma_commit(smem_addr(&ctl.h_full[sh_t & 1]));
+          sh_kc = 0;
+          ++sh_t;
         }
-        umma_commit(smem_addr(&ctl.h_full));
-        if (!wait_bar(ctl, ctl.hs_full, tile_it & 1)) goto mma_done;
+      };
+      for (int t = 0; t < n_tiles; ++t) {
+        while (sh_t <= t) {  // finish tile t's shrink (blocking)
+          if (!wait_bar(ctl, ctl.xa_full[xa_it % p.nxa], (xa_it / p.nxa) & 1)) goto mma_done;
+          issue_shrink_chunk();
+        }
+        if (!wait_bar(ctl, ctl.hs_full, t & 1)) goto mma_done;
         tc_fence_after();
         for (int nc = 0; nc < p.nc_count; ++nc, ++b_it, ++acc_it) {
           const int st = b_it % p.nbs;
@@ -272,15 +357,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const uint32_t bs = b_base + st * p.b_stage;
           const uint32_t d = tmem + (ab ? kTmemAcc1 : kTmemAcc0);
 #pragma unroll
-          for (int k = 0; k < KEXP / 16; ++k) {
-            const uint32_t koff = (k & 3) * 32;
-            const uint32_t a_atom = h_base + (k >> 2) * (kTileM * 128);
-            const uint32_t b_atom = bs + (k >> 2) * (p.n_ch * 128);
-            umma_bf16(d, umma_desc_sw128(a_atom + koff), umma_desc_sw128(b_atom + koff),
-                      idesc_expand, k != 0);
+          for (int kk = 0; kk < RP; kk += 16) {
+            // hi half: H columns [0, RP); lo half: H columns [RP, 2 RP); both
+            // against B_e's rank columns kk .. kk+15.
+            const uint64_t bdesc = umma_desc_sw128(bs + kk * 2);
+            umma_bf16(d, umma_desc_sw128(h_base + (kk >> 6) * (kTileM * 128) + (kk & 63) * 2),
+                      bdesc, idesc_expand, kk != 0);
+            const int kl = RP + kk;
+            umma_bf16(d, umma_desc_sw128(h_base + (kl >> 6) * (kTileM * 128) + (kl & 63) * 2),
+                      bdesc, idesc_expand, true);
           }
           umma_commit(smem_addr(&ctl.b_empty[st]));
           umma_commit(smem_addr(&ctl.acc_full[ab]));
+          // next tile's shrink chunks that have already arrived (no blocking)
+          while (sh_t == t + 1 && sh_t < n_tiles &&
+                 mbar_try_wait(smem_addr(&ctl.xa_full[xa_it % p.nxa]), (xa_it / p.nxa) & 1))
+            issue_shrink_chunk();
         }
         umma_commit(smem_addr(&ctl.hs_empty));
       }
@@ -289,23 +381,45 @@ __global__ void __launch_bounds__(kGThreads, 1)
       mbar_wait_bounded(smem_addr(&ctl.drain), 0);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ================================================================ X / A_e producer
+  } else if (warp == 1 || warp == 3) {
+    // ================================================================ X / A_e producers
+    // Warp 1 gathers tile rows 0-63 and A_e rows 0-31, warp 3 rows 64-127 and
+    // A_e rows 32-63.  A stage is signalled xa_lag stages late (once the copies
+    // of the stages after it are issued), so xa_lag + 1 stages are in flight.
+    const int half = warp == 1 ? 0 : 1;
+    const uint64_t keep = l2_evict_last();  // x rows and A_e are re-read by other tiles
     uint32_t it = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      const TileInfo ti = tile_info(p, tile_start, n_e, t);
+    int q[4] = {-1, -1, -1, -1};  // issued, not yet signalled stages (q[0] oldest)
+    int nq = 0;
+    // x token of this lane's two rows, loaded one tile ahead
+    auto tokens = [&](int t, int (&tok)[2]) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        tok[u] = -1;
+        if (t >= n_tiles) continue;
+        const MyTile mt = my_tiles[t];
+        const int row = half * 64 + lane + 32 * u;
+        if ((mt.fold[row >> 5] >> (row & 31)) & 1u) {
+          const int r = mt.r0 + row;
+          tok[u] = (p.src ? __ldg(p.src + r) : r) / p.top_k;
+        }
+      }
+    };
+    int tok_next[2];
+    tokens(0, tok_next);
+    for (int t = 0; t < n_tiles; ++t) {
+      const MyTile ti = my_tiles[t];
       const uint8_t *A = reinterpret_cast<const uint8_t *>(
           __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + ti.e));
-      const uint8_t *xrow[4];
-      bool xv[4];
+      const uint8_t *xrow[2];
+      bool xv[2];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int r = ti.r0 + lane + 32 * q;
-        int s = -1;
-        if (r < ti.r1) s = p.src ? __ldg(p.src + r) : r;
-        xv[q] = s >= 0;
-        xrow[q] = p.x + static_cast<size_t>(s >= 0 ? s / p.top_k : 0) * p.k_in * 2;
+      for (int u = 0; u < 2; ++u) {
+        xv[u] = tok_next[u] >= 0;
+        xrow[u] = p.x + static_cast<size_t>(tok_next[u] >= 0 ? tok_next[u] : 0) * p.k_in * 2;
       }
+      tokens(t + 1, tok_next);
+      const int j = half * 32 + lane;  // A_e row of this lane
       for (int kc = 0; kc < p.kc_count; ++kc, ++it) {
         const int st = it % p.nxa;
         if (!wait_bar(ctl, ctl.xa_empty[st], ((it / p.nxa) & 1) ^ 1)) goto prod_a_done;
@@ -313,40 +427,58 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const uint32_t as = xs + kTileM * 128;
         const int k0 = kc * 64;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (!xv[q]) continue;
-          const int row = lane + 32 * q;
+        for (int u = 0; u < 2; ++u) {
+          if (!xv[u]) continue;
+          const int row = half * 64 + lane + 32 * u;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const int kk = k0 + 8 * c;
             const bool in = kk < p.k_in;
-            cp_async_16(xs + sw128(row, c), xrow[q] + (in ? kk * 2 : 0), in ? 16u : 0u);
+            cp_async_16_hint(xs + sw128(row, c), xrow[u] + (in ? kk * 2 : 0), in ? 16u : 0u, keep);
           }
         }
-        for (int j = lane; j < p.rank; j += 32) {
+        if (j < p.rank) {
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const int kk = k0 + 8 * c;
             const bool in = kk < p.k_in;
-            cp_async_16(as + sw128(j, c), A + (static_cast<size_t>(j) * p.k_in + (in ? kk : 0)) * 2,
-                        in ? 16u : 0u);
+            cp_async_16_hint(as + sw128(j, c),
+                             A + (static_cast<size_t>(j) * p.k_in + (in ? kk : 0)) * 2,
+                             in ? 16u : 0u, keep);
           }
         }
         cp_async_commit();
-        cp_async_wait_group<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(smem_addr(&ctl.xa_full[st]));
+        if (nq == p.xa_lag) {  // oldest pending stage: <= xa_lag newer groups remain
+          switch (p.xa_lag) {
+            case 1: cp_async_wait_group<1>(); break;
+            case 2: cp_async_wait_group<2>(); break;
+            default: cp_async_wait_group<3>(); break;
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(smem_addr(&ctl.xa_full[q[0]]));
+          q[0] = q[1];
+          q[1] = q[2];
+          q[2] = q[3];
+          --nq;
+        }
+        q[nq++] = st;
       }
     }
   prod_a_done:
     cp_async_wait_group<0>();
+    fence_proxy_async_smem();
+    for (int i = 0; i < nq; ++i) mbar_arrive(smem_addr(&ctl.xa_full[q[i]]));
   } else if (warp == 2) {
     // ================================================================ B_e producer
+    // One B_e tile [n_ch rows x rank] per accumulator chunk, signalled `lag`
+    // stages late so lag + 1 stages are in flight.
     uint32_t it = 0;
-    const int rc = p.rank / 8;           // 16-byte chunks per B_e row
-    constexpr int hi_chunks = RP / 8;    // position of the lo copy
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      const TileInfo ti = tile_info(p, tile_start, n_e, t);
+    const int rc = p.rank / 8;  // 16-byte chunks per B_e row
+    const uint64_t keep = l2_evict_last();
+    const int lag = p.nbs >= 3 ? 2 : 1;
+    int q0 = -1, q1 = -1, nq = 0;  // issued, not yet signalled stages (q0 oldest)
+    for (int t = 0; t < n_tiles; ++t) {
+      const MyTile ti = my_tiles[t];
       const uint8_t *B = reinterpret_cast<const uint8_t *>(
           __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ti.e));
       for (int nc = 0; nc < p.nc_count; ++nc, ++it) {
@@ -358,43 +490,52 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const int n = n0 + i;
           const bool in = n < p.n_out;
           const uint8_t *brow = B + static_cast<size_t>(in ? n : 0) * p.rank * 2;
-          for (int c = 0; c < rc; ++c) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const int kc16 = half * hi_chunks + c;  // 16-byte chunk index along K
-              const uint32_t dst = bs + (kc16 >> 3) * (p.n_ch * 128) + sw128(i, kc16 & 7);
-              cp_async_16(dst, brow + c * 16, in ? 16u : 0u);
-            }
-          }
+          for (int c = 0; c < rc; ++c)
+            cp_async_16_hint(bs + sw128(i, c), brow + c * 16, in ? 16u : 0u, keep);
         }
         cp_async_commit();
-        cp_async_wait_group<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(smem_addr(&ctl.b_full[st]));
+        if (nq == lag) {  // the oldest pending stage has landed once <= lag groups remain
+          if (lag == 2) cp_async_wait_group<2>(); else cp_async_wait_group<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(smem_addr(&ctl.b_full[q0]));
+          q0 = q1;
+          --nq;
+        }
+        if (nq == 0) q0 = st; else q1 = st;
+        ++nq;
       }
     }
   prod_b_done:
     cp_async_wait_group<0>();
+    fence_proxy_async_smem();
+    if (nq >= 1) mbar_arrive(smem_addr(&ctl.b_full[q0]));
+    if (nq >= 2) mbar_arrive(smem_addr(&ctl.b_full[q1]));
   } else if (warp >= 4) {
     // ================================================================ epilogue
-    const int ew = warp - 4;  // TMEM lanes [32 ew, 32 ew + 32)
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(ew * 32) << 16);
+    // Eight warps: warp w reads TMEM lanes [32 (w % 4), +32) (its tile rows);
+    // the two warps of a lane quarter split the 64-column boxes (even / odd).
+    const int ew = warp - 4;
+    const int quarter = warp & 3;
+    const int sub = ew >> 2;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint8_t *ring = smem + p.off_base + ew * p.depth * 4096;
     const uint32_t ring_addr = smem_addr(ring);
+    const uint64_t stream_policy = l2_evict_first();  // base_out is touched once
     uint32_t tile_it = 0, acc_it = 0;
-    // box sequence of this warp: (tile, box column) for tiles with rows here
-    int ld_t = blockIdx.x, ld_b = 0, ld_y = 0;
+    // box sequence of this warp: (tile, box column) over tiles with rows here
+    int ld_t = 0, ld_b = sub, ld_y = 0;
     uint32_t ld_count = 0, box_it = 0;
     auto ld_advance = [&](bool first) {
       if (!first) {
-        if (++ld_b < p.nbx) return;
-        ld_b = 0;
-        ld_t += gridDim.x;
+        ld_b += 2;
+        if (ld_b < p.nbx) return;
+        ld_b = sub;
+        ++ld_t;
       }
-      for (; ld_t < n_tiles; ld_t += gridDim.x) {
-        const TileInfo ti = tile_info(p, tile_start, n_e, ld_t);
-        if (ti.r1 > ti.r0 + ew * kBoxRows) {
-          ld_y = ti.r0 + ew * kBoxRows;
+      for (; ld_t < n_tiles; ++ld_t) {
+        const MyTile ti = my_tiles[ld_t];
+        if (ld_b < p.nbx && ti.r1 > ti.r0 + quarter * kBoxRows) {
+          ld_y = ti.r0 + quarter * kBoxRows;
           return;
         }
       }
@@ -404,7 +545,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const int st = ld_count % p.depth;
       const uint32_t bar = smem_addr(&ctl.base_full[ew][st]);
       mbar_arrive_expect_tx(bar, kBoxRows * kBoxCols * 2);
-      tma_load_2d(ring_addr + st * 4096, &tmap_base, ld_b * kBoxCols, ld_y, bar);
+      tma_load_2d_hint(ring_addr + st * 4096, &tmap_base, ld_b * kBoxCols, ld_y, bar,
+                       stream_policy);
       ++ld_count;
       ld_advance(false);
     };
@@ -412,37 +554,31 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (lane == 0)
       for (int i = 0; i < p.depth - 1; ++i) ld_issue();
 
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_it) {
-      const TileInfo ti = tile_info(p, tile_start, n_e, t);
-      const int row = ew * kBoxRows + lane;
+    for (int t = 0; t < n_tiles; ++t, ++tile_it) {
+      const MyTile ti = my_tiles[t];
+      const int row = quarter * kBoxRows + lane;
       const int rg = ti.r0 + row;
-      bool folds = false;
-      if (rg < ti.r1) {
-        const int s = p.src ? __ldg(p.src + rg) : rg;
-        folds = s >= 0 && (p.row_adapter == nullptr || __ldg(p.row_adapter + s / p.top_k) >= 0);
-      }
-      const float scale = __ldg(p.scale_table + ti.e);
-      const int owned = min(max(ti.r1 - (ti.r0 + ew * kBoxRows), 0), kBoxRows);
+      const bool folds = (ti.fold[row >> 5] >> (row & 31)) & 1u;
+      const float scale = ti.scale;
+      const int owned = min(max(ti.r1 - (ti.r0 + quarter * kBoxRows), 0), kBoxRows);
 
       // ---- h: tensor memory -> scaled, split into bf16 hi / lo -> shared memory
-      if (!wait_bar(ctl, ctl.h_full, tile_it & 1)) goto epi_done;
-      tc_fence_after();
-      float h[RP];
+      if (!wait_bar(ctl, ctl.h_full[tile_it & 1], (tile_it >> 1) & 1)) goto epi_done;
+      if (sub == 0) {
+        tc_fence_after();
+        float h[RP];
 #pragma unroll
-      for (int q = 0; q < RP / 16; ++q) {
-        float v[16];
-        tmem_ld16(lane_addr + kTmemH + q * 16, v);
+        for (int qq = 0; qq < RP / 16; ++qq) {
+          float v[16];
+          tmem_ld16(lane_addr + ((tile_it & 1) ? kTmemH1 : kTmemH0) + qq * 16, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) h[q * 16 + i] = v[i];
-      }
-      tmem_wait_ld();
-      if (!wait_bar(ctl, ctl.hs_empty, (tile_it & 1) ^ 1)) goto epi_done;
-      {
+          for (int i = 0; i < 16; ++i) h[qq * 16 + i] = v[i];
+        }
+        tmem_wait_ld();
+        if (!wait_bar(ctl, ctl.hs_empty, (tile_it & 1) ^ 1)) goto epi_done;
         float hi[RP], lo[RP];
 #pragma unroll
-        for (int j = 0; j < RP; ++j) {
-          split_hi_lo(folds ? h[j] * scale : 0.f, hi[j], lo[j]);
-        }
+        for (int jj = 0; jj < RP; ++jj) split_hi_lo(folds ? h[jj] * scale : 0.f, hi[jj], lo[jj]);
         uint8_t *hrow = smem + p.off_h;
 #pragma unroll
         for (int kk = 0; kk < KEXP; kk += 8) {
@@ -450,60 +586,66 @@ __global__ void __launch_bounds__(kGThreads, 1)
           if (kk < 2 * RP) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const int j = (kk < RP ? kk : kk - RP) + 2 * i;
-              w[i] = kk < RP ? pack_bf16x2(hi[j], hi[j + 1]) : pack_bf16x2(lo[j], lo[j + 1]);
+              const int jj = (kk < RP ? kk : kk - RP) + 2 * i;
+              w[i] = kk < RP ? pack_bf16x2(hi[jj], hi[jj + 1]) : pack_bf16x2(lo[jj], lo[jj + 1]);
             }
           }
           const uint32_t off = (kk >> 6) * (kTileM * 128) + sw128(row, (kk & 63) >> 3);
           *reinterpret_cast<uint4 *>(hrow + off) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ctl.hs_full));
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&ctl.hs_full));
 
       // ---- expand epilogue: base_out boxes of this warp's rows -------------
       for (int nc = 0; nc < p.nc_count; ++nc, ++acc_it) {
         const int ab = acc_it & 1;
         if (!wait_bar(ctl, ctl.acc_full[ab], (acc_it >> 1) & 1)) goto epi_done;
         tc_fence_after();
-        for (int j = 0; j < p.n_ch / kBoxCols; ++j) {
-          const int bcol = nc * (p.n_ch / kBoxCols) + j;
-          if (owned == 0 || bcol >= p.nbx) continue;
+        for (int jb = 0; jb < p.n_ch / kBoxCols; ++jb) {
+          const int bcol = nc * (p.n_ch / kBoxCols) + jb;
+          if ((bcol & 1) != sub || owned == 0 || bcol >= p.nbx) continue;
           const int st = box_it % p.depth;
           if (!wait_bar(ctl, ctl.base_full[ew][st], (box_it / p.depth) & 1)) goto epi_done;
           float v[64];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int qq = 0; qq < 4; ++qq) {
             float u[16];
-            tmem_ld16(lane_addr + (ab ? kTmemAcc1 : kTmemAcc0) + j * kBoxCols + q * 16, u);
+            tmem_ld16(lane_addr + (ab ? kTmemAcc1 : kTmemAcc0) + jb * kBoxCols + qq * 16, u);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[q * 16 + i] = u[i];
+            for (int i = 0; i < 16; ++i) v[qq * 16 + i] = u[i];
           }
           tmem_wait_ld();
           uint8_t *boxp = ring + st * 4096 + lane * 128;
           const bool whole = owned == kBoxRows;
           if (folds) {
             const int col0 = bcol * kBoxCols;
+            uint4 bb[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              uint4 *cp = reinterpret_cast<uint4 *>(boxp + ((c ^ (lane & 7)) << 4));
-              uint4 o;
-              pack8_add(*cp, v + 8 * c, o);
-              if (whole) {
-                *cp = o;
-              } else if (col0 + 8 * c < p.n_out) {
-                *reinterpret_cast<uint4 *>(p.base_out +
-                                           (static_cast<size_t>(rg) * p.n_out + col0 + 8 * c) * 2) = o;
-              }
+            for (int c = 0; c < 8; ++c)
+              bb[c] = *reinterpret_cast<const uint4 *>(boxp + ((c ^ (lane & 7)) << 4));
+#pragma unroll
+            for (int c = 0; c < 8; ++c) bb[c] = add8_bf16(bb[c], v + 8 * c);
+            if (whole) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4 *>(boxp + ((c ^ (lane & 7)) << 4)) = bb[c];
+            } else {
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                if (col0 + 8 * c < p.n_out)
+                  *reinterpret_cast<uint4 *>(
+                      p.base_out + (static_cast<size_t>(rg) * p.n_out + col0 + 8 * c) * 2) = bb[c];
             }
           }
           if (whole) fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (whole) tma_store_2d(&tmap_base, bcol * kBoxCols, ti.r0 + ew * kBoxRows,
-                                    ring_addr + st * 4096);
+            if (whole)
+              tma_store_2d_hint(&tmap_base, bcol * kBoxCols, ti.r0 + quarter * kBoxRows,
+                                ring_addr + st * 4096, stream_policy);
             bulk_commit();
             bulk_wait_read_1();  // the previous box's store has left its stage
             ld_issue();
@@ -567,7 +709,7 @@ uint32_t plan(GroupedParams &p, int n_ch, int nxa, int nbs, int depth, int n_e) 
   p.depth = depth;
   p.nc_count = (p.n_out + n_ch - 1) / n_ch;
   p.xa_stage = rup(kTileM * 128 + p.r_pad * 128, 1024);
-  p.b_stage = rup(static_cast<uint32_t>(n_ch * p.k_exp * 2), 1024);
+  p.b_stage = rup(static_cast<uint32_t>(n_ch * 128), 1024);  // K = rank, padded to 64
   uint32_t off = 0;
   p.off_xa = off;
   off += nxa * p.xa_stage;
@@ -576,9 +718,11 @@ uint32_t plan(GroupedParams &p, int n_ch, int nxa, int nbs, int depth, int n_e) 
   p.off_h = off;
   off += kTileM * p.k_exp * 2;
   p.off_base = off;
-  off += 4 * depth * 4096;
+  off += kEpiWarps * depth * 4096;
   p.off_tab = off;
   off += rup((n_e + 1) * 4, 16);
+  p.off_my = off;
+  off += rup(kMyTilesMax * sizeof(MyTile), 16);
   p.smem_bytes = off;
   return off + 1024;
 }
@@ -591,16 +735,26 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
   p.k_exp = static_cast<int>(rup(2 * p.r_pad, 64));
   p.kc_count = (p.k_in + 63) / 64;
   p.nbx = (p.n_out + kBoxCols - 1) / kBoxCols;
-  // Largest rings that fit: accumulator chunk, operand stages, base depth.
+  // Deepest rings that fit.  Rows whose x is wider than their base_out
+  // read-modify-write (router-like shapes) favour the X/A ring; the rest favour
+  // the base_out ring (HBM latency), then B_e stages (L2 latency).
+  static const int cand_base[][3] = {{2, 2, 4}, {3, 2, 4}, {3, 3, 3}, {2, 3, 3}, {2, 2, 3},
+                                     {2, 2, 2}};
+  static const int cand_x[][3] = {{6, 2, 2}, {5, 2, 3}, {5, 2, 2}, {4, 2, 3}, {4, 2, 2},
+                                  {3, 2, 2}, {2, 2, 2}};
+  const bool x_heavy = static_cast<int64_t>(p.k_in) * 2 > static_cast<int64_t>(p.n_out) * 4;
   bool ok = false;
   uint32_t total = 0;
   const int n_chs[2] = {128, 64};
-  for (int a = 0; a < 2 && !ok; ++a)
-    for (int depth = 6; depth >= 3 && !ok; --depth)
-      for (int nxa = 3; nxa >= 2 && !ok; --nxa) {
-        total = plan(p, n_chs[a], nxa, 2, depth, n_e);
-        ok = total <= kGSmemLimit;
-      }
+  for (int a = 0; a < 2 && !ok; ++a) {
+    const int(*cand)[3] = x_heavy ? cand_x : cand_base;
+    const int nc = x_heavy ? 7 : 6;
+    for (int i = 0; i < nc; ++i) {
+      total = plan(p, n_chs[a], cand[i][0], cand[i][1], cand[i][2], n_e);
+      if ((ok = total <= kGSmemLimit)) break;
+    }
+  }
+  p.xa_lag = p.nxa - 1 < 3 ? p.nxa - 1 : 3;
   if (!ok) return MLG_ERR_UNSUPPORTED;
 
   CUtensorMap tmap;
@@ -631,12 +785,20 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
     attr_err[d] = e;
   });
   if (attr_err[dev & 63] != cudaSuccess) return cuda_status(attr_err[dev & 63]);
-  // Persistent: one CTA per SM, or fewer when the window has fewer tiles.
-  const uint32_t window_rows = static_cast<uint32_t>(p.row_end - p.row_offset);
-  const uint32_t max_tiles = (window_rows + kTileM - 1) / kTileM + static_cast<uint32_t>(n_e);
+  // Persistent: one CTA per SM (more only when a CTA's tile list would
+  // overflow), fewer when there are fewer tiles.  Tile bound: whole-window
+  // tiles plus one split per expert span and per window boundary.
+  const int64_t rows = p.row_end - p.row_offset;
+  const int64_t n_win = (rows + p.win - 1) / p.win;
+  const int64_t full = rows / p.win, rest = rows % p.win;
+  const int64_t max_tiles = full * ((p.win + kTileM - 1) / kTileM) + (rest + kTileM - 1) / kTileM +
+                            n_e + n_win;
   int grid = sm_count();
   if (g_grouped_ctas > 0) grid = g_grouped_ctas;
-  if (static_cast<uint32_t>(grid) > max_tiles) grid = static_cast<int>(max_tiles);
+  const int64_t need = (max_tiles + kMyTilesMax - 1) / kMyTilesMax;
+  if (grid < need) grid = static_cast<int>(need);
+  if (grid > max_tiles) grid = static_cast<int>(max_tiles);
+  p.my_cap = kMyTilesMax;
   switch (p.r_pad) {
     case 16: grouped_fold_kernel<16><<<grid, kGThreads, total, stream>>>(tmap, p); break;
     case 32: grouped_fold_kernel<32><<<grid, kGThreads, total, stream>>>(tmap, p); break;
@@ -703,6 +865,31 @@ extern "C" mlg_status mlg_grouped_down(const mlg_bf16 *x, const int32_t *expert_
   p.n_experts = n_experts;
   p.row_offset = row_offset;
   p.row_end = row_end;
+  p.win = row_end - row_offset;  // one window
+  return launch_grouped(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mlg_status mlg_grouped_down_all_windows(
+    const mlg_bf16 *x, const int32_t *expert_offsets, const int32_t *src,
+    const int32_t *row_adapter, const uint64_t *a_table, const uint64_t *b_table,
+    const float *scale_table, mlg_bf16 *base_out, int32_t k_in, int32_t max_rank, int32_t n_out,
+    int32_t top_k, int32_t n_experts, int32_t total_rows, uint32_t cap, void *stream) {
+  using namespace mlg;
+  if (cap == 0) return MLG_ERR_CAP_ZERO;
+  if (top_k < 1 || n_experts < 0 || total_rows < 0) return MLG_ERR_INVALID_ARG;
+  GroupedParams p = {};
+  const mlg_status st = fill_common(p, x, row_adapter, a_table, b_table, scale_table, base_out,
+                                    k_in, max_rank, n_out);
+  if (st != MLG_OK) return st;
+  if (!expert_offsets || !src) return MLG_ERR_INVALID_ARG;
+  if (total_rows == 0 || n_experts == 0) return MLG_OK;
+  p.offsets = expert_offsets;
+  p.src = src;
+  p.top_k = top_k;
+  p.n_experts = n_experts;
+  p.row_offset = 0;
+  p.row_end = total_rows;
+  p.win = cap < static_cast<uint32_t>(total_rows) ? static_cast<int32_t>(cap) : total_rows;
   return launch_grouped(p, static_cast<cudaStream_t>(stream));
 }
 
@@ -724,5 +911,6 @@ extern "C" mlg_status mlg_router_fold(const mlg_bf16 *x, const int32_t *row_adap
   p.n_experts = 1;
   p.row_offset = 0;
   p.row_end = n_tokens;
+  p.win = n_tokens;
   return launch_grouped(p, static_cast<cudaStream_t>(stream));
 }

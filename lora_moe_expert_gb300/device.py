@@ -96,8 +96,12 @@ class FoldProblem:
     def _stream(self):
         return self.stream if self.stream is not None else torch.cuda.current_stream(self.device)
 
-    def run(self, stream=None, use_row_map: bool = True) -> None:
-        """Enqueue the fold (the whole hot path for this problem) on `stream`."""
+    def run(self, stream=None, use_row_map: bool = True, per_window: bool = False) -> None:
+        """Enqueue the fold (the whole hot path for this problem) on `stream`.
+
+        The grouped form folds all windows of grouped_down_windows(rows, cap)
+        in one launch; per_window=True launches mlg_grouped_down once per
+        window instead (same bits)."""
         w = self.w
         s = stream if stream is not None else self._stream()
         if w.kind == "gather":
@@ -106,11 +110,18 @@ class FoldProblem:
                                 w.max_rank, w.n_out, w.top_k, self.n_experts, stream=s)
         elif w.kind == "grouped":
             ra = self.row_adapter if use_row_map else None
-            for start, end in self.windows:
-                mlg.mlg_grouped_down(self.x, self.expert_offsets, self.src, ra, self.a_table,
-                                     self.b_table, self.scale_table, self.base, w.k_in,
-                                     w.max_rank, w.n_out, w.top_k, self.n_experts, start, end,
-                                     stream=s)
+            if per_window:
+                for start, end in self.windows:
+                    mlg.mlg_grouped_down(self.x, self.expert_offsets, self.src, ra,
+                                         self.a_table, self.b_table, self.scale_table, self.base,
+                                         w.k_in, w.max_rank, w.n_out, w.top_k, self.n_experts,
+                                         start, end, stream=s)
+            else:
+                mlg.mlg_grouped_down_all_windows(self.x, self.expert_offsets, self.src, ra,
+                                                 self.a_table, self.b_table, self.scale_table,
+                                                 self.base, w.k_in, w.max_rank, w.n_out,
+                                                 w.top_k, self.n_experts, w.rows, w.cap,
+                                                 stream=s)
         else:
             mlg.mlg_router_fold(self.x, None, self.a_table, self.b_table, self.scale_table,
                                 self.base, w.rows, w.k_in, w.max_rank, w.n_out, stream=s)

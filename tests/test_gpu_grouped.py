@@ -85,13 +85,31 @@ def test_window_split_is_bit_exact():
     for cap in (1 << 20, 128, 77, 5):
         w.cap = cap
         prob = FoldProblem(w)
-        prob.run()
+        prob.run(per_window=True)
         torch.cuda.synchronize()
         outs.append(prob.base_bits())
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
     ref, folded, _ = fh.oracle_reference(w)
     fh.check_fold(outs[0], w.base, ref, folded)
+
+
+@pytest.mark.parametrize("cap", [1 << 20, 8192, 300, 128, 77])
+def test_all_windows_launch_matches_per_window(cap):
+    """One launch over all windows gives the bits of one launch per window."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_grouped(14, [400, 700, 250], 8, 40, 256, 512, 32, cap=cap,
+                             adapted_frac=0.8, stream_base=[0, 0, 1])
+    outs = []
+    for per_window in (True, False):
+        prob = FoldProblem(w)
+        prob.run(per_window=per_window)
+        torch.cuda.synchronize()
+        outs.append(prob.base_bits())
+    assert np.array_equal(outs[0], outs[1])
+    ref, folded, _ = fh.oracle_reference(w)
+    fh.check_fold(outs[1], w.base, ref, folded)
 
 
 def test_negative_zero_and_repeat():

@@ -263,6 +263,20 @@ def test_fold_validation_on_host(L):
     assert grouped(k_in=4) == mlg.MLG_ERR_UNSUPPORTED
     assert grouped(row_offset=50, row_end=50) == mlg.MLG_OK
 
+    def all_windows(**kw):
+        args = {**ok, "expert_offsets": p, "src": p, "total_rows": 100, "cap": 32, **kw}
+        return L.mlg_grouped_down_all_windows(
+            args["x"], args["expert_offsets"], args["src"], args["row_adapter"], args["a_table"],
+            args["b_table"], args["scale_table"], args["base_out"], args["k_in"],
+            args["max_rank"], args["n_out"], args["top_k"], args["n_experts"],
+            args["total_rows"], args["cap"], 0)
+
+    assert all_windows(cap=0) == mlg.MLG_ERR_CAP_ZERO
+    assert all_windows(total_rows=-1) == mlg.MLG_ERR_INVALID_ARG
+    assert all_windows(src=None) == mlg.MLG_ERR_INVALID_ARG
+    assert all_windows(max_rank=20) == mlg.MLG_ERR_UNSUPPORTED
+    assert all_windows(total_rows=0) == mlg.MLG_OK
+
     def router(**kw):
         args = {**ok, "n_tokens": 16, **kw}
         return L.mlg_router_fold(args["x"], args["row_adapter"], args["a_table"],

@@ -282,11 +282,16 @@ MLG_API mlg_status mlg_read_device_errors(uint32_t *flags_out, int32_t clear);
 
 /* Launch-shape knobs for benchmarking sweeps; 0 restores the automatic
  * choice.  Process-wide; set them only while no other thread launches folds.
- *   MLG_TUNE_GATHER_CLUSTER   CTAs per expert cluster of mlg_gather_bgmv (1, 2, 4, 8)
- *   MLG_TUNE_GROUPED_CTAS     persistent CTAs of mlg_grouped_down / mlg_router_fold
+ *   MLG_TUNE_GATHER_CLUSTER   CTAs per expert cluster of mlg_gather_bgmv (1, 2, 4, 8):
+ *                             the cluster splits k_in (partial h summed on chip) and n_out
+ *   MLG_TUNE_GATHER_NSPLIT    independent CTAs per expert and cluster rank of
+ *                             mlg_gather_bgmv (1, 2, 4, 8): each computes all of h
+ *                             and folds its own n_out slice
+ *   MLG_TUNE_GROUPED_CTAS     persistent CTAs of the grouped and router folds
  * Errors: INVALID_ARG for an unknown knob or a value out of range. */
 #define MLG_TUNE_GATHER_CLUSTER 1
 #define MLG_TUNE_GROUPED_CTAS 2
+#define MLG_TUNE_GATHER_NSPLIT 3
 MLG_API mlg_status mlg_set_tuning(int32_t knob, int32_t value);
 
 #ifdef __cplusplus

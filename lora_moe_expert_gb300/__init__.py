@@ -31,6 +31,7 @@ MLG_ROUTE_FOLD, MLG_ROUTE_SKIP, MLG_ROUTE_REFUSE = 0, 1, 2
 MLG_MAX_RANK = 64
 MLG_TUNE_GATHER_CLUSTER = 1
 MLG_TUNE_GROUPED_CTAS = 2
+MLG_TUNE_GATHER_NSPLIT = 3
 
 
 class MlgError(RuntimeError):

@@ -4,24 +4,32 @@
 // skipping rows whose token has a negative row-map entry (moe_row_adapter.rs,
 // build_moe_row_adapter_decode) and experts that fold nothing.
 //
-// GB300 design (not the pages' two-launch shrink/expand layout):
-//  * one thread-block cluster of CS CTAs per expert: the expert's A_e and B_e
-//    leave HBM exactly once, split over the cluster -- rank q holds the k
-//    columns [q*ks, (q+1)*ks) of A_e and the n rows [q*ns, (q+1)*ns) of B_e;
-//  * every load and store is a TMA bulk copy (cp.async.bulk) issued by one
-//    warp, completion counted on an mbarrier, so all of a CTA's bytes are in
-//    flight at once; the weight copies are issued before the row scan;
-//  * rows of the expert are found on the device by a scan of `indices`
-//    (ordered ballot compaction, identical in every CTA of the cluster);
-//  * shrink h = x A_e^T and expand h B_e^T run on the tensor cores
-//    (mma.sync m16n8k16 bf16 -> fp32; decode M is 1..32 rows, below the
-//    smallest tcgen05 M), h stays fp32: each CTA's partial h over its k slice
-//    is summed across the cluster through distributed shared memory in a
-//    fixed rank order, and the expand multiplies B_e by h = hi + lo (two bf16
-//    halves, so h is carried to ~2^-17 relative precision);
-//  * epilogue: out = RNE_bf16(base + scale * (h B^T)), written in place in
-//    shared memory and bulk-stored; rows that do not fold are never loaded
-//    or stored.
+// GB300 design (not the pages' two-launch shrink/expand layout).  Decode is
+// bound by latency and by the bytes of the expert pairs, so each expert's A_e
+// and B_e leave HBM once and every CTA gets all of its bytes in flight at once:
+//  * work unit = (expert, n slice).  Two ways to split an expert over CTAs:
+//      - cs == 1 ("full shrink"): each CTA computes all of h (A_e is read once
+//        from HBM and again from L2 by the other n slices) and folds its own
+//        n slice -- no communication between CTAs; chosen when A_e is small
+//        next to B_e (down projections);
+//      - cs > 1 (a thread-block cluster of cs CTAs): rank q computes h over k
+//        columns [q*ks, (q+1)*ks); the partial h are summed through
+//        distributed shared memory in a fixed rank order; chosen when A_e
+//        dominates (gate / up projections);
+//  * loads and stores are TMA bulk copies issued by one warp with mbarrier
+//    completion; the weights are requested as soon as the table is read, and
+//    the B_e fragments of the expand are loaded straight into registers;
+//  * programmatic dependent launch: the table read and the weight requests
+//    happen before griddepcontrol.wait, so they overlap the preceding kernel;
+//    routing, x and base_out are read only after it;
+//  * shrink h = x A_e^T on the tensor cores (mma.sync m16n8k16 bf16 -> fp32,
+//    M = rank, N = rows; decode has 1..32 rows per expert, below any tcgen05
+//    M); expand with swapped operands (M = 16 rows of B_e, N = rows, K = rank)
+//    against h split into bf16 hi + lo halves, so h enters at ~2^-17
+//    relative precision (h stays fp32 in effect) and the expand cost does not
+//    depend on how many rows an expert has;
+//  * epilogue: out = RNE_bf16(base + scale * (h B^T)) in shared memory, then
+//    bulk-stored; rows that do not fold are never loaded or stored.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -34,7 +42,10 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxRowGroup = 32;  // most rows of one expert folded per pass
+constexpr int kMaxRowGroup = 32;                 // most rows of one expert folded per pass
+constexpr int kScanPer = 8;                      // rows per thread per scan chunk
+constexpr int kScanChunk = kScanPer * kThreads;  // 2048 rows
+constexpr int kMaxMtPerPass = 8;  // B_e m-tiles x k-steps a warp holds in registers
 
 static __device__ uint32_t g_gather_errors;
 
@@ -47,38 +58,56 @@ struct GatherParams {
   const float *scale_table;
   uint16_t *base_out;
   int32_t n_slots, k_in, rank, n_out, top_k, n_experts;
-  int32_t ks, ns;         // k columns / n rows per cluster rank
+  int32_t ns2;            // n slices per cluster rank (independent CTAs, full shrink each)
+  int32_t ks, ns;         // k columns per cluster rank, n columns per CTA
   int32_t rg;             // rows per pass (16 or 32)
   uint32_t stride_a;      // bytes per A_e / x row in shared memory
   uint32_t stride_base;   // bytes per base row in shared memory
-  uint32_t off_a, off_x, off_b, off_base, off_p, off_hloc, off_h, smem_bytes;
+  uint32_t off_a, off_x, off_base, off_p, off_hloc, hloc_bytes, smem_bytes;
 };
 
 __device__ __forceinline__ void record_error(uint32_t bit) { atomicOr(&g_gather_errors, bit); }
 
-constexpr int kScanPer = 8;                       // rows per thread per scan chunk
-constexpr int kScanChunk = kScanPer * kThreads;   // 2048 rows
+__device__ __forceinline__ uint32_t ld_nc_u32(const void *ptr) {
+  uint32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+  return v;
+}
+
+// Issue the index and row-map loads of one scan chunk (rows base + i*256 + tid).
+__device__ __forceinline__ void scan_load(const GatherParams &p, int base, int (&idx)[kScanPer],
+                                          int (&ra)[kScanPer]) {
+#pragma unroll
+  for (int i = 0; i < kScanPer; ++i) {
+    const int row = base + i * kThreads + threadIdx.x;
+    idx[i] = -1;
+    ra[i] = -1;
+    if (row < p.n_slots) {
+      idx[i] = __ldg(p.indices + row);
+      ra[i] = __ldg(p.row_adapter + row / p.top_k);
+    }
+  }
+}
 
 // Collect the rows [g0, g0 + rg) of the rows that fold through expert e, in
-// the order (chunk, i, warp, lane) -- the same in every CTA of a cluster --
-// and return the total number of such rows.  Block-uniform.  Each chunk's
-// index and row-map loads are all issued before any is used (one memory
-// round trip per chunk), and a chunk costs two block barriers.
-__device__ int scan_rows(const GatherParams &p, int e, int g0, int *s_rows,
+// the order (chunk, i, warp, lane) -- the same in every CTA -- and return the
+// total number of such rows.  Block-uniform; two barriers per 2048-row chunk.
+// When have0, chunk 0's loads are passed in (already issued).
+__device__ int scan_rows(const GatherParams &p, int e, int g0, const int (&idx0)[kScanPer],
+                         const int (&ra0)[kScanPer], bool have0, int *s_rows,
                          int (*s_cnt)[kWarps]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int count = 0;
   for (int base = 0; base < p.n_slots; base += kScanChunk) {
     int idx[kScanPer], ra[kScanPer];
+    if (base == 0 && have0) {
 #pragma unroll
-    for (int i = 0; i < kScanPer; ++i) {
-      const int row = base + i * kThreads + tid;
-      idx[i] = -1;
-      ra[i] = -1;
-      if (row < p.n_slots) {
-        idx[i] = __ldg(p.indices + row);
-        ra[i] = __ldg(p.row_adapter + row / p.top_k);
+      for (int i = 0; i < kScanPer; ++i) {
+        idx[i] = idx0[i];
+        ra[i] = ra0[i];
       }
+    } else {
+      scan_load(p, base, idx, ra);
     }
     unsigned mask[kScanPer];
 #pragma unroll
@@ -87,15 +116,6 @@ __device__ int scan_rows(const GatherParams &p, int e, int g0, int *s_rows,
       if (lane == 0) s_cnt[i][warp] = __popc(mask[i]);
     }
     __syncthreads();
-    int total = 0;
-#pragma unroll
-    for (int i = 0; i < kScanPer; ++i) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const int v = s_cnt[i][w];
-        total += v;
-      }
-    }
     int run = count;
 #pragma unroll
     for (int i = 0; i < kScanPer; ++i) {
@@ -108,10 +128,32 @@ __device__ int scan_rows(const GatherParams &p, int e, int g0, int *s_rows,
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) run += s_cnt[i][w];
     }
-    count += total;
+    count = run;
     __syncthreads();
   }
   return count;
+}
+
+// B_e fragments of one 16-row m-tile for the swapped expand (A operand of
+// m16n8k16): thread (g, c) holds B_e rows n and n+8, rank columns
+// c*q + 4*st .. c*q + 4*st + 3 of every k-step st (q = rank / 4).  The same
+// physical-column assignment is used for h, so the contraction covers every
+// rank column once; slots at or past q are zero.
+template <int KST>
+__device__ __forceinline__ void load_b_frags(const uint8_t *B, int n, int n_out, int r, int c,
+                                             uint32_t (&f)[KST][4]) {
+  const int q4 = r / 4;
+#pragma unroll
+  for (int st = 0; st < KST; ++st) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int row = n + hr * 8;
+      const bool in = row < n_out;
+      const uint8_t *base = B + (static_cast<size_t>(in ? row : 0) * r + c * q4 + 4 * st) * 2;
+      f[st][hr] = (in && 4 * st < q4) ? ld_nc_u32(base) : 0u;              // slots 0, 1
+      f[st][2 + hr] = (in && 4 * st + 2 < q4) ? ld_nc_u32(base + 4) : 0u;  // slots 2, 3
+    }
+  }
 }
 
 template <int RP>  // max_rank rounded up to a multiple of 16
@@ -124,6 +166,8 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
   constexpr int MT = RP / 16;   // rank m-tiles of the shrink
   constexpr int KST = RP / 16;  // k-steps of the expand
   constexpr int HS = RP + 4;    // fp32 row stride of the h buffers
+  constexpr int HB = RP + 8;    // bf16 row stride of the hi / lo buffers
+  constexpr int MPP = kMaxMtPerPass / KST > 0 ? kMaxMtPerPass / KST : 1;  // m-tiles per pass
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -132,23 +176,23 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
 
   const int k0 = static_cast<int>(q) * p.ks;
   const int ksv = max(0, min(p.ks, p.k_in - k0));
-  const int n0 = static_cast<int>(q) * p.ns;
-  const int nsv = max(0, min(p.ns, p.n_out - n0));
   const int r = p.rank;
-  const int q4 = r / 4;  // rank columns held by each MMA thread-column c
+  const int q4 = r / 4;
 
   uint8_t *sA = smem + p.off_a;
   uint8_t *sX = smem + p.off_x;
-  const uint8_t *sB = smem + p.off_b;
   uint8_t *sBase = smem + p.off_base;
   float *sP = reinterpret_cast<float *>(smem + p.off_p);
-  float *sHloc = reinterpret_cast<float *>(smem + p.off_hloc);
-  float *sH = reinterpret_cast<float *>(smem + p.off_h);
+  // hi / lo bf16 copies of h (B operand of the expand) reuse the partials' space
+  uint16_t *sHhi = reinterpret_cast<uint16_t *>(smem + p.off_p);
+  uint16_t *sHlo = sHhi + kMaxRowGroup * HB;
+  float *sHloc2[2] = {reinterpret_cast<float *>(smem + p.off_hloc),
+                      reinterpret_cast<float *>(smem + p.off_hloc + p.hloc_bytes)};
 
   // A_e rows >= rank and the k tail of the A / x rows (up to the next 32) are
   // read by the MMAs but never written by a copy: zero them once.
   if (r < RP || (ksv & 31) != 0) {
-    for (uint32_t i = tid * 16; i < p.off_b; i += kThreads * 16)
+    for (uint32_t i = tid * 16; i < p.off_base; i += kThreads * 16)
       *reinterpret_cast<uint4 *>(smem + i) = make_uint4(0, 0, 0, 0);
   }
   const uint32_t bar_w = smem_addr(&bars[0]), bar_x = smem_addr(&bars[1]);
@@ -158,24 +202,29 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
     fence_mbar_init();
   }
   __syncthreads();
-  uint32_t ph_w = 0, ph_x = 0;
+  // The next fold in the stream may start its own prologue now: it reads only
+  // tables and expert weights (never written by this kernel) before waiting.
+  griddep_launch_dependents();
+  uint32_t ph_w = 0, ph_x = 0, grp = 0;
   bool bad = false;
+  bool waited = false;  // griddep_wait() done (before the first routing / x / base read)
 
-  for (int e = static_cast<int>(cluster_id_x()); e < p.n_experts;
-       e += static_cast<int>(ncluster_x())) {
-    // Table loads first; the row scan's loads are issued before they are
-    // needed, so both memory round trips overlap.
+  const int n_units = p.n_experts * p.ns2;  // (expert, n slice) pairs
+  for (int unit = static_cast<int>(cluster_id_x()); unit < n_units;
+       unit += static_cast<int>(ncluster_x())) {
+    const int e = unit / p.ns2;
+    const int ni = (unit % p.ns2) * static_cast<int>(cs) + static_cast<int>(q);  // n slice
+    const int n0 = ni * p.ns;
+    const int nsv = max(0, min(p.ns, p.n_out - n0));
     const uint64_t a_addr = __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + e);
     const uint64_t b_addr = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + e);
     const float scale = __ldg(p.scale_table + e);
+    if (a_addr == 0 || b_addr == 0 || ((a_addr | b_addr) & 15u) != 0)
+      continue;  // the expert folds nothing (uniform in the cluster)
     fence_proxy_async_smem();  // earlier generic accesses before new async writes
-    int total = scan_rows(p, e, 0, s_rows, s_cnt);
-    if (total == 0 || a_addr == 0 || b_addr == 0 || ((a_addr | b_addr) & 15u) != 0)
-      continue;  // no folding row, or the expert folds nothing (uniform in the cluster)
-
-    // Weights: A_e k slice (one bulk copy per rank row), B_e n slice (one copy).
-    if (warp == 0 && !bad) {
-      const uint32_t bytes = (ksv > 0 ? r * ksv * 2u : 0u) + (nsv > 0 ? nsv * r * 2u : 0u);
+    __syncthreads();
+    if (warp == 0 && !bad) {  // A_e k slice: one bulk copy per rank row
+      const uint32_t bytes = ksv > 0 ? r * ksv * 2u : 0u;
       if (lane == 0) mbar_arrive_expect_tx(bar_w, bytes);
       __syncwarp();
       const uint8_t *A = reinterpret_cast<const uint8_t *>(a_addr);
@@ -183,15 +232,39 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
         for (int j = lane; j < r; j += 32)
           bulk_g2s(smem_addr(sA + j * p.stride_a), A + (static_cast<size_t>(j) * p.k_in + k0) * 2,
                    ksv * 2u, bar_w);
-      if (nsv > 0 && lane == 31)
-        bulk_g2s(smem_addr(const_cast<uint8_t *>(sB)),
-                 reinterpret_cast<const uint8_t *>(b_addr) + static_cast<size_t>(n0) * r * 2,
-                 nsv * r * 2u, bar_w);
+    }
+    // B_e fragments of this warp's first m-tiles, straight into registers
+    const uint8_t *B = reinterpret_cast<const uint8_t *>(b_addr);
+    const int mtn = (nsv + 15) / 16;
+    uint32_t bf[MPP][KST][4];
+    int bf_pass = 0;  // which pass of m-tiles bf holds
+#pragma unroll
+    for (int i = 0; i < MPP; ++i) {
+      const int m = warp + i * kWarps;
+      if (m < mtn) load_b_frags<KST>(B, n0 + m * 16 + g, p.n_out, r, c, bf[i]);
+    }
+
+    // Routing, x and base_out may be written by the preceding kernel.
+    if (!waited) {
+      griddep_wait();
+      waited = true;
+    }
+    int idx0[kScanPer], ra0[kScanPer];
+    scan_load(p, 0, idx0, ra0);
+    const int total = scan_rows(p, e, 0, idx0, ra0, true, s_rows, s_cnt);
+    if (total == 0) {  // an adapted expert with no folding row: let its weights land
+      const bool timed_out = !bad && !mbar_wait_bounded(bar_w, ph_w);
+      ph_w ^= 1u;
+      if (__syncthreads_or(timed_out)) {
+        if (!bad && tid == 0) record_error(kErrWaitTimeout);
+        bad = true;
+      }
+      continue;
     }
     bool have_weights = false;
 
-    for (int g0 = 0; g0 < total; g0 += p.rg) {
-      if (g0 > 0) scan_rows(p, e, g0, s_rows, s_cnt);
+    for (int g0 = 0; g0 < total; g0 += p.rg, ++grp) {
+      if (g0 > 0) scan_rows(p, e, g0, idx0, ra0, false, s_rows, s_cnt);
       const int n_g = min(p.rg, total - g0);
 
       // Rows of this group: x slices and base slices.
@@ -227,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
       // MMA M = rank (A_e rows), N = rows (x rows), K = k.  Each thread column
       // c feeds physical k = 8c .. 8c+7 of every 32-wide k block; A and B use
       // the same k assignment, so the contraction covers every k once.
+      float *sHloc = sHloc2[grp & 1];
       const int ntr = (n_g + 7) / 8;
       const int units = MT * ntr;
       int ksplit = 1;
@@ -276,93 +350,94 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
       __syncthreads();
       if (ksplit > 1) {  // fixed-order sum of the k-split partials
         for (int idx = tid; idx < ntr * 8 * HS; idx += kThreads) {
-          float s = 0.f;
-          for (int kk = 0; kk < ksplit; ++kk) s += sP[kk * (ntr * 8 * HS) + idx];
-          sHloc[idx] = s;
+          float sum = 0.f;
+          for (int kk = 0; kk < ksplit; ++kk) sum += sP[kk * (ntr * 8 * HS) + idx];
+          sHloc[idx] = sum;
         }
+        __syncthreads();
       }
-      // ---- h = sum over the cluster's k slices (distributed shared memory) --
-      cluster_sync();
+      // ---- h (summed over the cluster's k slices) -> bf16 hi / lo ----------
+      // sHloc alternates between two buffers, so a peer still reading this
+      // group's buffer is never overwritten before the next group's barrier.
+      if (cs > 1) cluster_sync();
       {
         const uint32_t local = smem_addr(sHloc);
-        const int n4 = ntr * 8 * HS / 4;
-        for (int i4 = tid; i4 < n4; i4 += kThreads) {
-          float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (uint32_t rk = 0; rk < cs; ++rk) {
-            const float4 v = ld_dsmem_f4(map_to_rank(local + i4 * 16, rk));
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
+        const int n2 = ntr * 8 * RP / 2;  // pairs of h values
+        for (int i2 = tid; i2 < n2; i2 += kThreads) {
+          const int row = (2 * i2) / RP, j = (2 * i2) % RP;
+          float h0 = 0.f, h1 = 0.f;
+          if (cs > 1) {
+            for (uint32_t rk = 0; rk < cs; ++rk) {  // fixed rank order
+              const uint32_t a = map_to_rank(local + (row * HS + j) * 4, rk);
+              float v0, v1;
+              asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                           : "=f"(v0), "=f"(v1)
+                           : "r"(a)
+                           : "memory");
+              h0 += v0;
+              h1 += v1;
+            }
+          } else {
+            h0 = sHloc[row * HS + j];
+            h1 = sHloc[row * HS + j + 1];
           }
-          reinterpret_cast<float4 *>(sH)[i4] = s;
+          float a0, b0, a1, b1;
+          split_hi_lo(h0, a0, b0);
+          split_hi_lo(h1, a1, b1);
+          *reinterpret_cast<uint32_t *>(sHhi + row * HB + j) = pack_bf16x2(a0, a1);
+          *reinterpret_cast<uint32_t *>(sHlo + row * HB + j) = pack_bf16x2(b0, b1);
         }
       }
-      cluster_sync();  // peers are done reading sHloc; sH is complete
+      __syncthreads();
 
-      // ---- expand + epilogue over this CTA's n slice ----------------------
-      // MMA M = rows, N = n, K = rank; A = h split into bf16 hi and lo halves.
-      const int mte = (n_g + 15) / 16;
-      const int ntn = nsv / 8;
-      if (!bad) {
-        uint32_t ah[2][KST][4], al[2][KST][4];
+      // ---- expand + epilogue (swapped operands: M = B_e rows, N = rows) ----
+      if (!bad && nsv > 0) {
+        const int nte = (n_g + 7) / 8;  // row n-tiles
+        for (int pass = 0; pass * MPP * kWarps < mtn; ++pass) {
+          if (pass != bf_pass) {  // later passes, or pass 0 again for a later row group
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-          for (int st = 0; st < KST; ++st) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-#pragma unroll
-              for (int hr = 0; hr < 2; ++hr) {
-                const int slot = st * 4 + half * 2;
-                const int row = mt * 16 + g + hr * 8;
-                float v0 = 0.f, v1 = 0.f;
-                if (slot < q4 && mt < mte) {
-                  v0 = sH[row * HS + c * q4 + slot];
-                  v1 = sH[row * HS + c * q4 + slot + 1];
-                }
-                float h0, l0, h1, l1;
-                split_hi_lo(v0, h0, l0);
-                split_hi_lo(v1, h1, l1);
-                ah[mt][st][half * 2 + hr] = pack_bf16x2(h0, h1);
-                al[mt][st][half * 2 + hr] = pack_bf16x2(l0, l1);
-              }
+            for (int i = 0; i < MPP; ++i) {
+              const int m = warp + (pass * MPP + i) * kWarps;
+              if (m < mtn) load_b_frags<KST>(B, n0 + m * 16 + g, p.n_out, r, c, bf[i]);
             }
+            bf_pass = pass;
           }
-        }
-        for (int nt = warp; nt < ntn; nt += kWarps) {
-          const int nl = nt * 8 + g;  // B_e row within the slice
-          const uint32_t *brow = reinterpret_cast<const uint32_t *>(sB + (nl * r + c * q4) * 2);
-          uint32_t b[KST][2];
-#pragma unroll
-          for (int st = 0; st < KST; ++st) {
-            b[st][0] = (st * 4 < q4) ? brow[st * 2] : 0u;
-            b[st][1] = (st * 4 + 2 < q4) ? brow[st * 2 + 1] : 0u;
-          }
-          float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            if (mt >= mte) continue;
+          for (int nt = 0; nt < nte; ++nt) {
+            // h^T fragments (B operand): rows nt*8 + g, same physical rank columns
+            uint32_t hh[KST][2], hl[KST][2];
+            const int hrow = nt * 8 + g;
 #pragma unroll
             for (int st = 0; st < KST; ++st) {
-              mma_bf16_16816(d[mt], ah[mt][st][0], ah[mt][st][1], ah[mt][st][2], ah[mt][st][3],
-                             b[st][0], b[st][1]);
-              mma_bf16_16816(d[mt], al[mt][st][0], al[mt][st][1], al[mt][st][2], al[mt][st][3],
-                             b[st][0], b[st][1]);
+              const int j = c * q4 + 4 * st;
+              const bool v0 = 4 * st < q4, v1 = 4 * st + 2 < q4;
+              hh[st][0] = v0 ? *reinterpret_cast<const uint32_t *>(sHhi + hrow * HB + j) : 0u;
+              hh[st][1] = v1 ? *reinterpret_cast<const uint32_t *>(sHhi + hrow * HB + j + 2) : 0u;
+              hl[st][0] = v0 ? *reinterpret_cast<const uint32_t *>(sHlo + hrow * HB + j) : 0u;
+              hl[st][1] = v1 ? *reinterpret_cast<const uint32_t *>(sHlo + hrow * HB + j + 2) : 0u;
             }
-          }
-          const int col = nt * 8 + 2 * c;
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
+            for (int i = 0; i < MPP; ++i) {
+              const int m = warp + (pass * MPP + i) * kWarps;
+              if (m >= mtn) continue;
+              float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-              const int row = mt * 16 + g + hr * 8;
-              if (mt >= mte || row >= n_g) continue;
-              uint32_t *w = reinterpret_cast<uint32_t *>(sBase + row * p.stride_base + col * 2);
-              const uint32_t bw = *w;
-              const float o0 = fmaf(scale, d[mt][hr * 2 + 0], bf16lo_to_f32(bw));
-              const float o1 = fmaf(scale, d[mt][hr * 2 + 1], bf16hi_to_f32(bw));
-              *w = pack_bf16x2(o0, o1);
+              for (int st = 0; st < KST; ++st) {
+                mma_bf16_16816(d, bf[i][st][0], bf[i][st][1], bf[i][st][2], bf[i][st][3],
+                               hh[st][0], hh[st][1]);
+                mma_bf16_16816(d, bf[i][st][0], bf[i][st][1], bf[i][st][2], bf[i][st][3],
+                               hl[st][0], hl[st][1]);
+              }
+              // d = (n m*16+g, row nt*8+2c), (n, row+1), (n+8, row), (n+8, row+1)
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int nl = m * 16 + g + (u >> 1) * 8;
+                const int row = nt * 8 + 2 * c + (u & 1);
+                if (nl < nsv && row < n_g) {
+                  uint16_t *bp = reinterpret_cast<uint16_t *>(sBase + row * p.stride_base) + nl;
+                  const float base = __uint_as_float(static_cast<uint32_t>(*bp) << 16);
+                  *bp = __bfloat16_as_ushort(__float2bfloat16_rn(fmaf(scale, d[u], base)));
+                }
+              }
             }
           }
         }
@@ -377,21 +452,18 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
       }
     }
   }
+  if (!waited) griddep_wait();  // complete only after the preceding kernel
   if (warp == 0) bulk_wait_all();
-  cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+  if (cs > 1) cluster_sync();  // no CTA leaves while a peer may still read its shared memory
 }
-
-struct Plan {
-  int cs, ks, ns, rp;
-  GatherParams p;
-};
 
 uint32_t round_up(uint32_t v, uint32_t m) { return (v + m - 1) / m * m; }
 
-// Shared-memory layout for a cluster size; returns total bytes.
-uint32_t layout(GatherParams &p, int cs, int rp) {
+// Shared-memory layout for a split (cs, ns2); returns total bytes.
+uint32_t layout(GatherParams &p, int cs, int ns2, int rp) {
+  p.ns2 = ns2;
   p.ks = static_cast<int>(round_up((p.k_in + cs - 1) / cs, 32));
-  p.ns = static_cast<int>(round_up((p.n_out + cs - 1) / cs, 8));
+  p.ns = static_cast<int>(round_up((p.n_out + cs * ns2 - 1) / (cs * ns2), 8));
   uint32_t sa = p.ks * 2;
   if (sa % 128 == 0) sa += 64;  // 16-byte MMA operand loads conflict-free
   p.stride_a = sa;
@@ -399,29 +471,31 @@ uint32_t layout(GatherParams &p, int cs, int rp) {
   sb += (16 + 128 - sb % 128) % 128;  // row stride = 16 (mod 128) bytes
   p.stride_base = sb;
   const uint32_t hbytes = p.rg * (rp + 4) * 4;
-  // k-split partials: ksplit * ntr <= 8 / (rp / 16) slots of ntr * 8 rows -> <= 1280 floats
-  const uint32_t pbytes = 1280 * 4 > hbytes ? 1280 * 4 : hbytes;
+  // k-split partials (<= 1280 floats), reused afterwards for the hi / lo h copies
+  uint32_t pbytes = 1280 * 4;
+  const uint32_t hilo = 2 * kMaxRowGroup * (rp + 8) * 2;
+  if (hilo > pbytes) pbytes = hilo;
   uint32_t off = 0;
   p.off_a = off;
   off += round_up(rp * sa, 128);
   p.off_x = off;
   off += round_up(p.rg * sa, 128);
-  p.off_b = off;
-  off += round_up(p.ns * p.rank * 2, 128);
   p.off_base = off;
   off += round_up(p.rg * sb, 128);
   p.off_p = off;
   off += round_up(pbytes, 128);
-  p.off_hloc = off;
-  off += round_up(hbytes, 128);
-  p.off_h = off;
-  off += round_up(hbytes, 128);
+  p.off_hloc = off;  // two buffers (alternating row groups)
+  p.hloc_bytes = round_up(hbytes, 128);
+  off += 2 * p.hloc_bytes;
   p.smem_bytes = off;
   return off;
 }
 
 int g_cluster_override = 0;
-constexpr uint32_t kSmemLimit = 227 * 1024 - 2048;  // leaves room for static shared memory
+int g_nsplit_override = 0;
+// Two CTAs per SM: each may use up to half of the 228 KB, less static memory.
+constexpr uint32_t kSmemTwoPerSm = 113 * 1024 - 1024;
+constexpr uint32_t kSmemLimit = 227 * 1024 - 2048;
 
 template <int RP>
 cudaError_t launch(const GatherParams &p, int cs, int clusters, cudaStream_t stream) {
@@ -440,13 +514,15 @@ cudaError_t launch(const GatherParams &p, int cs, int clusters, cudaStream_t str
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, gather_fold_kernel<RP>, p);
 }
 
@@ -477,6 +553,7 @@ uint32_t gather_read_errors(bool clear) {
 }
 
 void gather_set_cluster_override(int cs) { g_cluster_override = cs; }
+void gather_set_nsplit_override(int ns2) { g_nsplit_override = ns2; }
 
 }  // namespace mlg
 
@@ -513,18 +590,28 @@ extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
   // Rows per pass: decode batches spread ~n_slots / n_experts rows per expert.
   p.rg = (n_slots <= 8 * n_experts) ? 16 : 32;
 
-  // Cluster size: the smallest power of two that bounds one CTA's share of an
-  // expert's weights to ~48 KB, raised until the shared-memory layout fits.
-  const double pair_bytes = 2.0 * max_rank * (static_cast<double>(k_in) + n_out);
-  int cs = 1;
-  while (cs < 8 && pair_bytes / cs > 48.0 * 1024) cs *= 2;
+  // Split: when A_e is at most half of B_e, every CTA computes the whole
+  // shrink and the expert's n range is split over ns2 independent CTAs; else
+  // a cluster of cs CTAs splits k (partial h summed in shared memory) and n.
+  // Each CTA's share of the pair is bounded to ~64 KB, and the layout should
+  // leave room for two CTAs per SM.
+  const double a_bytes = 2.0 * max_rank * k_in, b_bytes = 2.0 * max_rank * n_out;
+  int cs = 1, ns2 = 1;
+  if (2.0 * a_bytes <= b_bytes) {
+    while (ns2 < 8 && a_bytes + b_bytes / ns2 > 64.0 * 1024) ns2 *= 2;
+  } else {
+    while (cs < 8 && (a_bytes + b_bytes) / cs > 64.0 * 1024) cs *= 2;
+  }
   if (g_cluster_override > 0) cs = g_cluster_override;
-  while (layout(p, cs, rp) > kSmemLimit && cs < 8) cs *= 2;
-  if (layout(p, cs, rp) > kSmemLimit) return MLG_ERR_UNSUPPORTED;
+  if (g_nsplit_override > 0) ns2 = g_nsplit_override;
+  if (g_cluster_override == 0)
+    while (layout(p, cs, ns2, rp) > kSmemTwoPerSm && cs < 8) cs *= 2;
+  if (layout(p, cs, ns2, rp) > kSmemLimit) return MLG_ERR_UNSUPPORTED;
 
-  // One cluster per expert, looping when the table is longer than the cap.
+  // One cluster per (expert, n slice), looping when there are more than fit.
+  const int64_t units = static_cast<int64_t>(n_experts) * ns2;
   const int max_clusters = (4 * sm_count()) / cs;
-  const int clusters = n_experts < max_clusters ? n_experts : max_clusters;
+  const int clusters = units < max_clusters ? static_cast<int>(units) : max_clusters;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   switch (rp) {

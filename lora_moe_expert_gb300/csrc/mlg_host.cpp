@@ -189,6 +189,7 @@ namespace mlg {
 uint32_t gather_read_errors(bool clear);
 uint32_t grouped_read_errors(bool clear);
 void gather_set_cluster_override(int cs);
+void gather_set_nsplit_override(int ns2);
 void grouped_set_ctas(int ctas);
 }  // namespace mlg
 
@@ -208,6 +209,11 @@ extern "C" mlg_status mlg_set_tuning(int32_t knob, int32_t value) {
       if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
         return MLG_ERR_INVALID_ARG;
       mlg::gather_set_cluster_override(value);
+      return MLG_OK;
+    case MLG_TUNE_GATHER_NSPLIT:
+      if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
+        return MLG_ERR_INVALID_ARG;
+      mlg::gather_set_nsplit_override(value);
       return MLG_OK;
     case MLG_TUNE_GROUPED_CTAS:
       if (value < 0 || value > 65535) return MLG_ERR_INVALID_ARG;

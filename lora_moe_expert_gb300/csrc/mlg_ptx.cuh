@@ -320,4 +320,14 @@ __device__ __forceinline__ void tma_store_2d_hint(const void *tmap, int32_t x, i
       : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Let the next kernel in the stream launch now (its CTAs still wait in
+// griddep_wait() before reading anything this kernel writes).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding kernel in the stream has completed and its memory
+// operations are visible (a no-op when it was not launched as a dependent).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace mlg

@@ -84,17 +84,20 @@ def test_smaller_true_rank_zero_padded():
     _run_and_check(w)
 
 
-@pytest.mark.parametrize("cs", [1, 2, 4, 8])
-def test_cluster_sizes(cs):
-    """Every cluster size meets the tolerance, and repeats of one size are bit-exact
-    (fixed-order reductions; only the k split, hence the fp32 summation order,
-    differs between sizes)."""
+@pytest.mark.parametrize("cs,ns2", [(1, 1), (2, 1), (4, 1), (8, 1), (1, 2), (1, 4), (1, 8),
+                                    (2, 2), (4, 2)])
+def test_split_configurations(cs, ns2):
+    """Every split of an expert over CTAs (cluster k split cs, independent n
+    split ns2) meets the tolerance, and repeats of one split are bit-exact
+    (fixed-order reductions; only the k split, hence the fp32 summation
+    order, differs between splits)."""
     from lora_moe_expert_gb300.device import FoldProblem
 
     w = synth.custom_gather(77, 24, 8, 32, 1024, 512, 32, adapted_frac=0.8, base_frac=0.2)
     ref, folded, _ = fh.oracle_reference(w)
     try:
         mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_CLUSTER, cs)
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_NSPLIT, ns2)
         prob = FoldProblem(w)
         outs = []
         for _ in range(2):
@@ -106,6 +109,7 @@ def test_cluster_sizes(cs):
         assert np.array_equal(outs[0], outs[1])
     finally:
         mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_CLUSTER, 0)
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_NSPLIT, 0)
 
 
 def test_repeat_is_deterministic_and_negative_zero_kept():

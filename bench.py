@@ -3,8 +3,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 A step is one pass of the hot path over one batch of synthetic input: one
-fold launch for the decode workloads, one launch per row window for the
-prefill workloads, one router-fold launch for the router.  The default
+fold launch for the decode workloads, one launch that folds every row window
+for the prefill workloads, one router-fold launch for the router.  The default
 workload is the decode gather BGMV at the down-projection shape (64 tokens,
 top-8, 128 experts at rank 16, k_in 768, n_out 2048).
 
@@ -359,6 +359,30 @@ def e2e_measure(prob, steps, device):
             "steps": steps}
 
 
+# ------------------------------------------------------------------ replicas
+def replica_seed_base(rank: int) -> int:
+    """Seed offset of a replica's rotating input sets (distinct per rank)."""
+    return 1000 + 97 * rank
+
+
+def max_over_ranks(value: float, device) -> float:
+    """The step time of the job: the maximum over ranks (timing only -- the
+    fold itself exchanges nothing between replicas)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(rows_per_step: int, world: int, ms_step: float) -> float:
+    """Whole-job throughput: every replica folds its own batch per step."""
+    return world * rows_per_step / (ms_step * 1e-3)
+
+
 # ------------------------------------------------------------------ main
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -430,15 +454,9 @@ def main():
     __graft_entry__.build()
 
     main_res = gpu_measure(args.workload, args.steps, args.warmup, device,
-                           seed_base=1000 + 97 * rank)
-    ms_step = main_res["ms_total"] / args.steps
-    if ws > 1:
-        t = torch.tensor([ms_step], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)  # timing only
-        ms_step = float(t.item())
-        e2e_s = torch.tensor([main_res["e2e"]["s_per_step"]], device=device)
-        torch.distributed.all_reduce(e2e_s, op=torch.distributed.ReduceOp.MAX)
-        main_res["e2e"]["s_per_step"] = float(e2e_s.item())
+                           seed_base=replica_seed_base(rank))
+    ms_step = max_over_ranks(main_res["ms_total"] / args.steps, device)
+    main_res["e2e"]["s_per_step"] = max_over_ranks(main_res["e2e"]["s_per_step"], device)
     peak, peak_kind = measured_peaks()
     per_launch_ms = ms_step / main_res["launches_per_step"]
     achieved = main_res["alg_bytes"] / main_res["launches_per_step"] / (per_launch_ms * 1e-3) / 1e9
@@ -474,7 +492,7 @@ def main():
     e2e = main_res["e2e"]
     line = {
         "metric": METRIC,
-        "value": ws * main_res["rows"] / (ms_step * 1e-3),
+        "value": job_rows_per_s(main_res["rows"], ws, ms_step),
         "unit": "rows/s",
         "n_gpus": ws,
         "steps": args.steps,
@@ -497,7 +515,8 @@ def main():
                      "traffic": recorded_traffic(kernel_source(main_res["kind"]), args.workload)},
         "tflops": main_res["alg_flops"] / (ms_step * 1e-3) / 1e12,
         "cpu_baseline": cpu,
-        "e2e": {"value": ws * main_res["rows"] / e2e["s_per_step"], "unit": "rows/s",
+        "e2e": {"value": job_rows_per_s(main_res["rows"], ws, e2e["s_per_step"] * 1e3),
+                "unit": "rows/s",
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},
         "gpu_launches": args.steps * main_res["launches_per_step"],

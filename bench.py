@@ -1,6 +1,7 @@
 """Benchmark of the MoE expert LoRA fold on GB300 (prints ONE JSON line).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+    python bench.py --workload NAME --profile-launches 2     (short untimed case for ncu)
 
 A step is one pass of the hot path over one batch of synthetic input: one
 fold launch for the decode workloads, one launch that folds every row window
@@ -43,6 +44,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE LoRA fold rows/s and achieved HBM GB/s (% of GB300 roofline), 1 GPU"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+SOAK_S = 0.8  # seconds of untimed replays under the clock sampler before the timed region
 
 # workload name -> (generator, description)
 WORKLOADS = {
@@ -69,9 +71,16 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_HEADERS = ("lora_moe_expert_gb300/csrc/mlg_ptx.cuh", "lora_moe_expert_gb300/csrc/mlg_internal.h")
+
+
 def source_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel source together with the headers it includes."""
+    h = hashlib.sha256()
+    for p in (path,) + tuple(os.path.join(ROOT, k) for k in KERNEL_HEADERS):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel_src, workload):
@@ -129,8 +138,9 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, settle_s=0.3):
         self.gpu = gpu_index
+        self.settle_s = settle_s
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_{os.getpid()}.csv")
 
@@ -142,7 +152,7 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            time.sleep(self.settle_s)
         except Exception:
             self.proc = None
         return self
@@ -273,12 +283,20 @@ def gpu_measure(name, steps, warmup, device, seed_base=1000, e2e=True):
             graph.replay()
         stream.synchronize()
     errors_before = mlg.mlg_read_device_errors(clear=True)
-    if torch.distributed.is_available() and torch.distributed.is_initialized():
-        torch.distributed.barrier()
-    torch.cuda.synchronize(device)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clocks:
+    # The clock sampler (100 ms period) runs from a soak of identical replays
+    # straight into the timed region, so its samples are taken under this load;
+    # a timed region of K short steps alone is shorter than one sample period.
+    with ClockSampler(torch.cuda.current_device(), settle_s=0.0) as clocks:
+        t_soak = time.perf_counter()
+        with torch.cuda.stream(stream):
+            while time.perf_counter() - t_soak < SOAK_S:
+                graph.replay()
+                stream.synchronize()
+        if torch.distributed.is_available() and torch.distributed.is_initialized():
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
         with torch.cuda.stream(stream):
             e0.record(stream)
             graph.replay()
@@ -423,6 +441,25 @@ def run_reference(args):
     return 0
 
 
+def profile_case(name, launches, device):
+    """A short, untimed run for profilers: one input set, the step `launches`
+    times (the first launch of a fresh process pays module loading)."""
+    import torch
+
+    import lora_moe_expert_gb300 as mlg
+    from lora_moe_expert_gb300 import synth
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    prob = FoldProblem(synth.NAMED[name](), device=device)
+    for _ in range(launches):
+        prob.run()
+    torch.cuda.synchronize(device)
+    if mlg.mlg_read_device_errors(clear=True):
+        raise RuntimeError("device error bits were set")
+    print(f"profile case {name}: {launches} launch(es) done", flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -434,6 +471,9 @@ def main():
                     help="other workloads measured in the same run (comma list, or 'none')")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=10.0)
+    ap.add_argument("--profile-launches", type=int, default=0,
+                    help="profiler case: run the workload's step this many times on cuda:0, "
+                         "untimed, and exit (no JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -452,6 +492,8 @@ def main():
     import __graft_entry__
 
     __graft_entry__.build()
+    if args.profile_launches > 0:
+        return profile_case(args.workload, args.profile_launches, device)
 
     main_res = gpu_measure(args.workload, args.steps, args.warmup, device,
                            seed_base=replica_seed_base(rank))

@@ -415,27 +415,53 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
               hl[st][0] = v0 ? *reinterpret_cast<const uint32_t *>(sHlo + hrow * HB + j) : 0u;
               hl[st][1] = v1 ? *reinterpret_cast<const uint32_t *>(sHlo + hrow * HB + j + 2) : 0u;
             }
+            // All MMAs of the pass first, then every base element is read, then
+            // every result written: the shared-memory round trips overlap instead
+            // of forming one load -> store chain per element.
+            float d[MPP][4];
 #pragma unroll
             for (int i = 0; i < MPP; ++i) {
               const int m = warp + (pass * MPP + i) * kWarps;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) d[i][u] = 0.f;
               if (m >= mtn) continue;
-              float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
               for (int st = 0; st < KST; ++st) {
-                mma_bf16_16816(d, bf[i][st][0], bf[i][st][1], bf[i][st][2], bf[i][st][3],
+                mma_bf16_16816(d[i], bf[i][st][0], bf[i][st][1], bf[i][st][2], bf[i][st][3],
                                hh[st][0], hh[st][1]);
-                mma_bf16_16816(d, bf[i][st][0], bf[i][st][1], bf[i][st][2], bf[i][st][3],
+                mma_bf16_16816(d[i], bf[i][st][0], bf[i][st][1], bf[i][st][2], bf[i][st][3],
                                hl[st][0], hl[st][1]);
               }
-              // d = (n m*16+g, row nt*8+2c), (n, row+1), (n+8, row), (n+8, row+1)
+            }
+            // d[i] = (n m*16+g, row nt*8+2c), (n, row+1), (n+8, row), (n+8, row+1)
+            constexpr int CH = MPP < 4 ? MPP : 4;  // m-tiles per batch of loads (registers)
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int nl = m * 16 + g + (u >> 1) * 8;
-                const int row = nt * 8 + 2 * c + (u & 1);
-                if (nl < nsv && row < n_g) {
-                  uint16_t *bp = reinterpret_cast<uint16_t *>(sBase + row * p.stride_base) + nl;
-                  const float base = __uint_as_float(static_cast<uint32_t>(*bp) << 16);
-                  *bp = __bfloat16_as_ushort(__float2bfloat16_rn(fmaf(scale, d[u], base)));
+            for (int i0 = 0; i0 < MPP; i0 += CH) {
+              uint32_t bv[CH][4];
+#pragma unroll
+              for (int i = 0; i < CH; ++i) {
+                const int m = warp + (pass * MPP + i0 + i) * kWarps;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int nl = m * 16 + g + (u >> 1) * 8;
+                  const int row = nt * 8 + 2 * c + (u & 1);
+                  bv[i][u] = 0u;
+                  if (m < mtn && nl < nsv && row < n_g)
+                    bv[i][u] = *(reinterpret_cast<const uint16_t *>(sBase + row * p.stride_base) + nl);
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < CH; ++i) {
+                const int m = warp + (pass * MPP + i0 + i) * kWarps;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int nl = m * 16 + g + (u >> 1) * 8;
+                  const int row = nt * 8 + 2 * c + (u & 1);
+                  if (m < mtn && nl < nsv && row < n_g) {
+                    const float base = __uint_as_float(bv[i][u] << 16);
+                    *(reinterpret_cast<uint16_t *>(sBase + row * p.stride_base) + nl) =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(fmaf(scale, d[i0 + i][u], base)));
+                  }
                 }
               }
             }

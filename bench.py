@@ -249,9 +249,16 @@ def n_sets_for(w_bytes):
     return max(1, min(32, int(np.ceil(2.0 * L2_BYTES / max(w_bytes, 1)))))
 
 
-def kernel_source(kind):
-    return "lora_moe_expert_gb300/csrc/" + ("mlg_gather.cu" if kind == "gather"
-                                            else "mlg_grouped.cu")
+# The kernel that folds each named workload (the decode fold takes expert
+# pairs of rank 16 or 32 that fit half an SM; other decode shapes go to the
+# cluster kernel).
+KERNEL_OF = {"decode_down": "mlg_decode.cu", "decode_gate_up": "mlg_gather.cu",
+             "tiny_decode": "mlg_gather.cu", "prefill_down": "mlg_grouped.cu",
+             "prefill_large": "mlg_grouped.cu", "router": "mlg_grouped.cu"}
+
+
+def kernel_source(workload):
+    return "lora_moe_expert_gb300/csrc/" + KERNEL_OF[workload]
 
 
 def gpu_measure(name, steps, warmup, device, seed_base=1000, e2e=True):
@@ -515,7 +522,7 @@ def main():
                               "alg_bytes_per_step": r["alg_bytes"],
                               "achieved_gbs": a, "frac_of_peak": a / peak,
                               "tflops": r["alg_flops"] / (r["ms_total"] / 20 * 1e-3) / 1e12,
-                              "traffic": recorded_traffic(kernel_source(r["kind"]), nm),
+                              "traffic": recorded_traffic(kernel_source(nm), nm),
                               "l2": f"{r['sets']} rotating input sets of "
                                     f"{r['set_bytes'] / 2**20:.0f} MiB"}
             except Exception as ex:  # report, do not hide
@@ -554,7 +561,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "alg_bytes_per_launch": main_res["alg_bytes"] // main_res["launches_per_step"],
-                     "traffic": recorded_traffic(kernel_source(main_res["kind"]), args.workload)},
+                     "traffic": recorded_traffic(kernel_source(args.workload), args.workload)},
         "tflops": main_res["alg_flops"] / (ms_step * 1e-3) / 1e12,
         "cpu_baseline": cpu,
         "e2e": {"value": job_rows_per_s(main_res["rows"], ws, e2e["s_per_step"] * 1e3),

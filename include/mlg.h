@@ -288,10 +288,21 @@ MLG_API mlg_status mlg_read_device_errors(uint32_t *flags_out, int32_t clear);
  *                             mlg_gather_bgmv (1, 2, 4, 8): each computes all of h
  *                             and folds its own n_out slice
  *   MLG_TUNE_GROUPED_CTAS     persistent CTAs of the grouped and router folds
+ *   MLG_TUNE_GATHER_PATH      kernel of mlg_gather_bgmv: 1 = one CTA per expert holding
+ *                             the whole pair (max_rank 16 or 32, n_out <= 2048, the pair in
+ *                             half an SM, n_experts <= SM count; else the fold returns
+ *                             UNSUPPORTED), 2 = the cluster kernel (any shape)
+ *   MLG_TUNE_GATHER_SPECULATION  row lists of the resident-pair kernel: 0 = scanned before
+ *                             the preceding kernel completes and checked after it, 1 = scanned
+ *                             after it only, 2 = the early scan reads another expert's rows so
+ *                             that every check fails and the rows are requested again (a test
+ *                             of that path; results are the same in all three modes)
  * Errors: INVALID_ARG for an unknown knob or a value out of range. */
 #define MLG_TUNE_GATHER_CLUSTER 1
 #define MLG_TUNE_GROUPED_CTAS 2
 #define MLG_TUNE_GATHER_NSPLIT 3
+#define MLG_TUNE_GATHER_PATH 4
+#define MLG_TUNE_GATHER_SPECULATION 5
 MLG_API mlg_status mlg_set_tuning(int32_t knob, int32_t value);
 
 #ifdef __cplusplus

@@ -32,6 +32,8 @@ MLG_MAX_RANK = 64
 MLG_TUNE_GATHER_CLUSTER = 1
 MLG_TUNE_GROUPED_CTAS = 2
 MLG_TUNE_GATHER_NSPLIT = 3
+MLG_TUNE_GATHER_PATH = 4
+MLG_TUNE_GATHER_SPECULATION = 5
 
 
 class MlgError(RuntimeError):

@@ -1,0 +1,663 @@
+// mlg_decode.cu -- decode-side MoE expert LoRA fold (moe_lora_gather_bgmv of
+// the moe_lora_grouped module index) for expert pairs that fit one CTA:
+//     base_out[row] += scale_e * (x[row / top_k] @ A_e^T) @ B_e^T,  e = indices[row],
+// rows whose token has a negative row-map entry skipped (moe_row_adapter.rs,
+// build_moe_row_adapter_decode), experts with a zero table cell or an id at or
+// above n_experts folding nothing.
+//
+// GB300 design.  A decode fold moves few bytes (a 64-token down projection is
+// ~16 MB), so its time is set by dependent round trips, not by bandwidth.  The
+// kernel is built so that consecutive folds in a stream overlap:
+//  * one CTA per expert holds the whole pair: A_e and B_e are bulk-copied into
+//    shared memory before griddepcontrol.wait (tables and weights are never
+//    written by the preceding kernel), and a CTA takes under half of an SM, so
+//    the next fold's CTAs are resident and load their pairs while this fold
+//    finishes (programmatic dependent launch);
+//  * the rows of the expert are found before the wait by a speculative scan of
+//    the routing (L2 loads only; the values may still change), and their x
+//    and base_out lines are prefetched into L2.  After the wait the x rows and
+//    base_out rows of that row list are requested at once, and the routing is
+//    scanned again; only if the fresh scan disagrees are they requested again.
+//    The round trip on the routing thus overlaps the one on x and base_out;
+//  * shrink h = x A_e^T with mma.sync m16n8k16 (M = rank, N = 8 rows, k split
+//    over the warps, partial sums added in a fixed order), h split into bf16
+//    hi + lo halves (h enters the expand at ~2^-17 relative precision);
+//  * expand with M = 8 rows (of 16), N = 8 columns of B_e, K = rank; each lane
+//    takes adjacent rank words of B_e and h (the same physical rank assignment
+//    for both operands), and the B_e rows are dealt to the MMA columns so that
+//    every lane ends with 8 adjacent output columns of one row: base_out is
+//    read (into registers, right after the wait) and written with 16-byte
+//    accesses, rounded once: RNE(base + scale * delta);
+//  * an expert with more than 8 rows gets a helper CTA (the SMs left over by
+//    the experts): owner and helper fold alternate passes of 8 rows, both
+//    deciding the split from the same per-expert row counts.
+// Rows are folded 8 at a time; an expert with more rows runs several passes.
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "mlg_internal.h"
+#include "mlg_ptx.cuh"
+
+namespace mlg {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRows = 8;         // rows per pass: expand M rows g = 0..7
+constexpr int kMaxQuads = 8;     // 32-column output quads per warp (n_out <= 2048)
+constexpr int kScanPer = 8;      // rows per thread per scan chunk
+constexpr int kScanChunk = kScanPer * kThreads;
+constexpr int kSpecRows = 32;    // rows of the speculative scan kept for L2 prefetch
+constexpr int kMaxCtas = 160;    // owner + helper CTAs (and table entries) at most
+
+static __device__ uint32_t g_decode_errors;
+
+struct DecodeParams {
+  const uint16_t *x;
+  const int32_t *indices;
+  const int32_t *row_adapter;
+  const uint64_t *a_table;
+  const uint64_t *b_table;
+  const float *scale_table;
+  uint16_t *base_out;
+  int32_t n_slots, k_in, n_out, top_k, n_experts;
+  int32_t spec_mode;  // 0: speculative row scan, 1: none, 2: scan a different expert (tests)
+  uint32_t stride_a;  // bytes per A_e / x row in shared memory
+  uint32_t off_a, off_x, off_b, off_p, off_h, zero_bytes, smem_bytes;
+};
+
+__device__ __forceinline__ void record_error(uint32_t bit) { atomicOr(&g_decode_errors, bit); }
+
+// L2-only loads: never served from a line this SM cached before the wait.
+__device__ __forceinline__ int ld_cg_s32(const int32_t *p) {
+  int v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_cg_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_v4(void *p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Issue the routing loads of one scan chunk (rows base + i*256 + tid).
+__device__ __forceinline__ void scan_load(const DecodeParams &p, int base, int (&idx)[kScanPer],
+                                          int (&ra)[kScanPer]) {
+#pragma unroll
+  for (int i = 0; i < kScanPer; ++i) {
+    const int row = base + i * kThreads + threadIdx.x;
+    idx[i] = -1;
+    ra[i] = -1;
+    if (row < p.n_slots) {
+      idx[i] = ld_cg_s32(p.indices + row);
+      ra[i] = ld_cg_s32(p.row_adapter + row / p.top_k);
+    }
+  }
+}
+
+// Ordered list of the rows that fold through expert e: writes ranks
+// [g0, g0 + cap) of the list to s_rows and returns the list's length.  The
+// order (chunk, i, warp, lane) is the same in every call.  Block-uniform.
+// When have0, the loads of the first chunk were issued by the caller.  With
+// s_hist, also adds every folding row to its expert's count (e = -1 collects
+// only the counts).
+__device__ int scan_expert_rows(const DecodeParams &p, int e, int g0, int cap, int *s_rows,
+                                int (*s_cnt)[kWarps], const int (&idx0)[kScanPer],
+                                const int (&ra0)[kScanPer], bool have0, int *s_hist) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int count = 0;
+  for (int base = 0; base < p.n_slots; base += kScanChunk) {
+    int idx[kScanPer], ra[kScanPer];
+    if (base == 0 && have0) {
+#pragma unroll
+      for (int i = 0; i < kScanPer; ++i) {
+        idx[i] = idx0[i];
+        ra[i] = ra0[i];
+      }
+    } else {
+      scan_load(p, base, idx, ra);
+    }
+    if (s_hist != nullptr) {  // folding rows per expert (ids in the table only)
+#pragma unroll
+      for (int i = 0; i < kScanPer; ++i)
+        if (ra[i] >= 0 && idx[i] >= 0 && idx[i] < p.n_experts) atomicAdd(&s_hist[idx[i]], 1);
+    }
+    unsigned mask[kScanPer];
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+      mask[i] = __ballot_sync(0xffffffffu, e >= 0 && idx[i] == e && ra[i] >= 0);
+      if (lane == 0) s_cnt[i][warp] = __popc(mask[i]);
+    }
+    __syncthreads();
+    int run = count;
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+      int mine = run;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) mine += (w < warp) ? s_cnt[i][w] : 0;
+      const int rank = mine + __popc(mask[i] & ((1u << lane) - 1u));
+      if (((mask[i] >> lane) & 1u) && rank >= g0 && rank < g0 + cap)
+        s_rows[rank - g0] = base + i * kThreads + tid;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) run += s_cnt[i][w];
+    }
+    count = run;
+    __syncthreads();
+  }
+  return count;
+}
+
+// One pass's x rows into shared memory: warp 0, bulk copies on bar_x.
+__device__ __forceinline__ void request_x(const DecodeParams &p, int warp, int lane, int n_g,
+                                          uint32_t row_bytes_x, bool bad, const int *s_rows,
+                                          uint8_t *sX, uint32_t bar_x) {
+  if (warp == 0 && !bad) {
+    if (lane == 0) mbar_arrive_expect_tx(bar_x, n_g * row_bytes_x);
+    __syncwarp();
+    if (lane < n_g)
+      bulk_g2s(smem_addr(sX + lane * p.stride_a),
+               p.x + static_cast<size_t>(s_rows[lane] / p.top_k) * p.k_in, row_bytes_x, bar_x);
+  }
+}
+
+// This lane's base_out row (row g of the pass) in 16-byte chunks: columns
+// quad*32 + 8c .. +7 of the warp's quads, into registers.
+__device__ __forceinline__ void request_base(const DecodeParams &p, int warp, int g, int c,
+                                             int n_g, int n_tiles, const int *s_rows,
+                                             uint4 (&base_v)[kMaxQuads], int &my_row) {
+  my_row = g < n_g ? s_rows[g] : -1;
+#pragma unroll
+  for (int qi = 0; qi < kMaxQuads; ++qi) {
+    const int tile = (warp + qi * kWarps) * 4 + c;
+    base_v[qi] = make_uint4(0, 0, 0, 0);
+    if (my_row >= 0 && tile < n_tiles)
+      base_v[qi] = ld_cg_v4(p.base_out + static_cast<size_t>(my_row) * p.n_out + tile * 8);
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void load_words(uint32_t (&w)[N], const uint8_t *s) {
+  if constexpr (N == 2) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(s);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4 *>(s);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  }
+}
+
+__device__ __forceinline__ uint32_t fold_pair(uint32_t base2, float d0, float d1, float scale) {
+  const float r0 = fmaf(scale, d0, __uint_as_float(base2 << 16));
+  const float r1 = fmaf(scale, d1, __uint_as_float(base2 & 0xffff0000u));
+  uint32_t o;  // round both to nearest even; r1 into the upper half
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o) : "f"(r1), "f"(r0));
+  return o;
+}
+
+// The expand of one 32-column quad: M = the 8 rows (of 16), N = 8 columns per
+// tile, K = rank, h as hi + lo.  Tile t's MMA column n takes B_e row
+// quad*32 + 8*(n/2) + 2t + n%2, so lane (g, c) -- whose D holds MMA columns
+// 2c, 2c+1 of row g -- ends with row g, output columns quad*32 + 8c .. +7
+// (tile t gives columns 8c + 2t, 8c + 2t + 1): no transpose before the
+// 16-byte base_out access.  B_e rows at or past n_out read as zero.
+template <int RP>
+__device__ __forceinline__ void expand_quad(float (&d)[4][4], const uint8_t *sB,
+                                            const uint32_t (&hh)[RP / 8],
+                                            const uint32_t (&hl)[RP / 8], int quad, int n_out) {
+  constexpr int WPL = RP / 8, KST = RP / 16;
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int col_base = quad * 32 + 8 * (g >> 1) + (g & 1);  // + 2t: this lane's B_e row
+  const bool full = quad * 32 + 32 <= n_out;                  // warp-uniform
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int col = col_base + 2 * t;
+    uint32_t bw[WPL];
+#pragma unroll
+    for (int w = 0; w < WPL; ++w) bw[w] = 0u;
+    if (full || col < n_out) load_words<WPL>(bw, sB + (col * RP + c * WPL * 2) * 2);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) d[t][u] = 0.f;
+#pragma unroll
+    for (int st = 0; st < KST; ++st) {
+      mma_bf16_16816(d[t], hh[2 * st], 0u, hh[2 * st + 1], 0u, bw[2 * st], bw[2 * st + 1]);
+      mma_bf16_16816(d[t], hl[2 * st], 0u, hl[2 * st + 1], 0u, bw[2 * st], bw[2 * st + 1]);
+    }
+  }
+}
+
+// Which expert a helper CTA takes, or whether an owner has a helper, from the
+// per-expert counts of folding rows: an expert with more than kRows rows is
+// "heavy"; the i-th heavy expert (by id) gets helper CTA i, if there is one.
+// Warp 0 computes it; the result is in *s_out after the next barrier.
+__device__ __forceinline__ void assign_helper(const int *s_hist, int n_experts, int n_helpers,
+                                              bool helper, int who, int *s_out) {
+  const int lane = threadIdx.x & 31;
+  if ((threadIdx.x >> 5) != 0) return;
+  int run = 0, found = helper ? -1 : 0;
+  for (int b = 0; b < n_experts; b += 32) {
+    const int e = b + lane;
+    const bool heavy = e < n_experts && s_hist[e] > kRows;
+    const unsigned mask = __ballot_sync(0xffffffffu, heavy);
+    const int rank = run + __popc(mask & ((1u << lane) - 1u));
+    if (heavy && rank < n_helpers) {
+      if (helper && rank == who) found = e;
+      if (!helper && e == who) found = 1;
+    }
+    run += __popc(mask);
+  }
+  // at most one lane found something; combine over the warp
+  const int v = __reduce_max_sync(0xffffffffu, found);
+  if (lane == 0) *s_out = v;
+}
+
+template <int RP>  // max_rank: 16 or 32
+__global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[2];  // 0: the pair, 1: x rows
+  __shared__ int s_spec[kSpecRows];
+  __shared__ int s_rows[kSpecRows];  // ranks [list0, list0 + 32) of the row list
+  __shared__ int s_cnt[kScanPer][kWarps];
+  __shared__ int s_hist[kMaxCtas];   // folding rows per expert
+  __shared__ int s_role;
+
+  constexpr int MT = RP / 16;   // rank m-tiles of the shrink
+  constexpr int WPL = RP / 8;   // rank words (bf16 pairs) per lane in the expand
+  constexpr int PS = RP + 4;    // fp32 row stride of the shrink partials
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+
+  uint8_t *sA = smem + p.off_a;
+  uint8_t *sX = smem + p.off_x;
+  const uint8_t *sB = smem + p.off_b;
+  float *sP = reinterpret_cast<float *>(smem + p.off_p);
+  uint8_t *sHhi = smem + p.off_h;
+  uint8_t *sHlo = sHhi + kRows * RP * 2;
+
+  // The k tail of the A_e / x rows (up to the next 32 columns) is read by the
+  // MMAs but never written by a copy: zero it once.
+  for (uint32_t i = tid * 16; i < p.zero_bytes; i += kThreads * 16)
+    *reinterpret_cast<uint4 *>(smem + i) = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < kMaxCtas; i += kThreads) s_hist[i] = 0;
+  const uint32_t bar_w = smem_addr(&bars[0]), bar_x = smem_addr(&bars[1]);
+  if (tid == 0) {
+    mbar_init(bar_w, 1);
+    mbar_init(bar_x, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // The next fold in the stream may start its prologue now: before its own
+  // wait it reads tables and weights, and the routing through L2 only.
+  griddep_launch_dependents();
+
+  const int n_tiles = p.n_out / 8;
+  const int no_idx[kScanPer] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const int kblocks = (p.k_in + 31) / 32;
+  const uint32_t row_bytes_x = static_cast<uint32_t>(p.k_in) * 2u;
+  uint32_t ph_w = 0, ph_x = 0;
+  bool bad = false;
+
+  // Owner CTA e folds expert e; helper CTA h (blockIdx >= n_experts) folds the
+  // odd passes of the h-th heavy expert, whose owner then folds the even ones.
+  const bool helper = static_cast<int>(blockIdx.x) >= p.n_experts;
+  const int who = helper ? static_cast<int>(blockIdx.x) - p.n_experts : static_cast<int>(blockIdx.x);
+  const int n_helpers = static_cast<int>(gridDim.x) - p.n_experts;
+  const int first = helper ? 1 : 0;  // first pass of this CTA
+  const bool spec = p.spec_mode != 1;
+  int e = helper ? -1 : who;
+  int total = 0;
+  float scale = 0.f;
+  bool pair = false;  // the pair of expert e was requested on bar_w
+
+  // Table entry of expert ex; on a foldable pair, request it (CTA-uniform).
+  auto request_pair = [&](int ex) -> bool {
+    const uint64_t a_addr = __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + ex);
+    const uint64_t b_addr = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ex);
+    scale = __ldg(p.scale_table + ex);
+    if (a_addr == 0 || b_addr == 0 || ((a_addr | b_addr) & 15u) != 0) return false;
+    if (warp == 0 && !bad) {  // the whole pair: one copy per A_e row, one for B_e
+      const uint32_t b_bytes = static_cast<uint32_t>(p.n_out) * RP * 2u;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_w, RP * row_bytes_x + b_bytes);
+        bulk_g2s(smem_addr(sB), reinterpret_cast<const void *>(b_addr), b_bytes, bar_w);
+      }
+      __syncwarp();
+      const uint8_t *A = reinterpret_cast<const uint8_t *>(a_addr);
+      for (int j = lane; j < RP; j += 32)
+        bulk_g2s(smem_addr(sA + j * p.stride_a), A + static_cast<size_t>(j) * row_bytes_x,
+                 row_bytes_x, bar_w);
+    }
+    return true;
+  };
+  auto spec_target = [&](int ex) { return p.spec_mode == 2 ? (ex + 1) % p.n_experts : ex; };
+
+  // ---- before the wait: the pair, and a speculative row list (L2 loads only)
+  if (spec) {
+    total = scan_expert_rows(p, helper ? -1 : spec_target(e), 0, kSpecRows, s_spec, s_cnt, no_idx,
+                             no_idx, false, s_hist);
+    if (helper) {
+      // (spec_mode 2: a different heavy expert, so that the check after the wait fails)
+      assign_helper(s_hist, p.n_experts, n_helpers + 1, true, p.spec_mode == 2 ? who + 1 : who,
+                    &s_role);
+      __syncthreads();
+      e = s_role;
+      if (e >= 0)
+        total = scan_expert_rows(p, spec_target(e), 0, kSpecRows, s_spec, s_cnt, no_idx, no_idx,
+                                 false, nullptr);
+    }
+  }
+  if (e >= 0) pair = request_pair(e);
+  const int spec_g0 = kRows * first;
+  int n_spec = (spec && pair) ? max(0, min(kRows, total - spec_g0)) : 0;
+  if (warp == 1 && lane < n_spec) {
+    const int row = s_spec[spec_g0 + lane];
+    prefetch_l2(p.x + static_cast<size_t>(row / p.top_k) * p.k_in, row_bytes_x);
+    prefetch_l2(p.base_out + static_cast<size_t>(row) * p.n_out, static_cast<uint32_t>(p.n_out) * 2u);
+  }
+  for (int i = tid; i < kMaxCtas; i += kThreads) s_hist[i] = 0;
+  __syncthreads();
+  griddep_wait();  // routing, x and base_out may be written by the preceding kernel
+
+  // ---- after the wait: the speculative first pass's x and base_out rows, the
+  // fresh scan's loads and its base_out loads are all in flight together.
+  uint4 base_v[kMaxQuads];
+  int my_row = -1;
+  if (n_spec > 0) request_x(p, warp, lane, n_spec, row_bytes_x, bad, s_spec + spec_g0, sX, bar_x);
+  int idx0[kScanPer], ra0[kScanPer];
+  scan_load(p, 0, idx0, ra0);
+  if (n_spec > 0) request_base(p, warp, g, c, n_spec, n_tiles, s_spec + spec_g0, base_v, my_row);
+  int fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, idx0, ra0, true, s_hist);
+  assign_helper(s_hist, p.n_experts, n_helpers, helper, who, &s_role);
+  __syncthreads();
+  const int role = s_role;  // helper: its expert; owner: 1 if it has a helper
+  bool timed_out = false;
+  if (helper && role != e) {  // the speculation picked another expert (or none)
+    if (n_spec > 0) {
+      timed_out = !bad && !mbar_wait_bounded(bar_x, ph_x);
+      ph_x ^= 1u;
+    }
+    if (pair) {
+      timed_out = (!bad && !mbar_wait_bounded(bar_w, ph_w)) || timed_out;
+      ph_w ^= 1u;
+    }
+    if (__syncthreads_or(timed_out)) {
+      if (!bad && tid == 0) record_error(kErrWaitTimeout);
+      bad = true;
+    }
+    n_spec = 0;
+    my_row = -1;
+    e = role;
+    pair = false;
+    if (e >= 0 && !bad) {
+      fence_proxy_async_smem();  // the old pair's buffers were read by no one; order anyway
+      pair = request_pair(e);
+      if (pair) fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false, nullptr);
+    }
+  } else if (n_spec > 0) {
+    // The speculative rows stand if the fresh scan agrees.
+    bool differ = tid == 0 && fresh != total;
+    if (tid < n_spec && s_rows[spec_g0 + tid] != s_spec[spec_g0 + tid]) differ = true;
+    if (__syncthreads_or(differ)) {  // let the copies of the stale rows land first
+      timed_out = !bad && !mbar_wait_bounded(bar_x, ph_x);
+      ph_x ^= 1u;
+      if (__syncthreads_or(timed_out)) {
+        if (!bad && tid == 0) record_error(kErrWaitTimeout);
+        bad = true;
+      }
+      n_spec = 0;
+      my_row = -1;
+    }
+  }
+  total = pair ? fresh : 0;
+  const int stride = (helper || role == 1) ? 2 : 1;  // passes of 8 rows this CTA folds
+  bool issued = n_spec > 0;  // the first pass's x copies and base_out loads are in flight
+  bool have_pair = false;
+  int list0 = 0;             // rank of s_rows[0] in the row list
+
+  for (int g0 = kRows * first; g0 < total && !bad; g0 += kRows * stride) {
+    if (g0 >= list0 + kSpecRows) {
+      scan_expert_rows(p, e, g0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false, nullptr);
+      list0 = g0;
+    }
+    const int *rows = s_rows + (g0 - list0);
+    const int n_g = min(kRows, total - g0);
+    if (!issued) {
+      request_x(p, warp, lane, n_g, row_bytes_x, bad, rows, sX, bar_x);
+      request_base(p, warp, g, c, n_g, n_tiles, rows, base_v, my_row);
+    }
+    issued = false;
+    timed_out = false;
+    if (!have_pair) timed_out = !mbar_wait_bounded(bar_w, ph_w);
+    if (!timed_out) timed_out = !mbar_wait_bounded(bar_x, ph_x);
+    if (!have_pair) ph_w ^= 1u;
+    ph_x ^= 1u;
+    have_pair = true;
+    if (__syncthreads_or(timed_out)) {
+      if (tid == 0) record_error(kErrWaitTimeout);
+      bad = true;
+      break;
+    }
+
+    // ---- shrink: h[row][j] = sum_k x[row][k] A_e[j][k], k split over warps
+    // Lane column c feeds physical k = 8c .. 8c+7 of every 32-wide k block
+    // to both operands, so the contraction covers every k once.
+    float acc[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    for (int kb = warp; kb < kblocks; kb += kWarps) {
+      const uint32_t kbyte = (kb * 32 + 8 * c) * 2;
+      const uint4 sx = *reinterpret_cast<const uint4 *>(sX + g * p.stride_a + kbyte);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const uint4 pa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g) * p.stride_a + kbyte);
+        const uint4 qa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g + 8) * p.stride_a + kbyte);
+        mma_bf16_16816(acc[mt], pa.x, qa.x, pa.y, qa.y, sx.x, sx.y);
+        mma_bf16_16816(acc[mt], pa.z, qa.z, pa.w, qa.w, sx.z, sx.w);
+      }
+    }
+    // acc[mt] = (j mt*16+g, row 2c), (j, row 2c+1), (j+8, row 2c), (j+8, row 2c+1)
+    float *part = sP + warp * (kRows * PS);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int j = mt * 16 + g, row = 2 * c;
+      part[row * PS + j] = acc[mt][0];
+      part[(row + 1) * PS + j] = acc[mt][1];
+      part[row * PS + j + 8] = acc[mt][2];
+      part[(row + 1) * PS + j + 8] = acc[mt][3];
+    }
+    __syncthreads();
+    // The next pass of this CTA (its rows already in s_rows): its x rows are
+    // requested now that sX is free, its base_out rows as the quads of this
+    // pass retire, so neither round trip is exposed.
+    const int g1 = g0 + kRows * stride;
+    const bool pre = g1 < total && g1 < list0 + kSpecRows;  // CTA-uniform
+    const int *rows1 = s_rows + (g1 - list0);
+    const int n_g1 = pre ? min(kRows, total - g1) : 0;
+    const int my_row1 = g < n_g1 ? rows1[g] : -1;
+    if (pre) request_x(p, warp, lane, n_g1, row_bytes_x, bad, rows1, sX, bar_x);
+    // Sum the warps' partials in warp order; split h into bf16 hi + lo.
+    if (tid < kRows * RP / 2) {
+      const int row = (2 * tid) / RP, j = (2 * tid) % RP;
+      float h0 = 0.f, h1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        h0 += sP[w * (kRows * PS) + row * PS + j];
+        h1 += sP[w * (kRows * PS) + row * PS + j + 1];
+      }
+      float a0, b0, a1, b1;
+      split_hi_lo(h0, a0, b0);
+      split_hi_lo(h1, a1, b1);
+      *reinterpret_cast<uint32_t *>(sHhi + (row * RP + j) * 2) = pack_bf16x2(a0, a1);
+      *reinterpret_cast<uint32_t *>(sHlo + (row * RP + j) * 2) = pack_bf16x2(b0, b1);
+    }
+    __syncthreads();
+
+    // ---- expand + epilogue (see expand_quad).  Lane c takes rank words
+    // c*WPL .. c*WPL+WPL-1 of h and of B_e: k-step st uses word c*WPL + 2st
+    // (logical k 2c, 2c+1) and the next (logical 2c+8, 2c+9).
+    {
+      uint32_t hh[WPL], hl[WPL];
+      load_words<WPL>(hh, sHhi + (g * RP + c * WPL * 2) * 2);
+      load_words<WPL>(hl, sHlo + (g * RP + c * WPL * 2) * 2);
+      uint16_t *orow = p.base_out + static_cast<size_t>(my_row < 0 ? 0 : my_row) * p.n_out + 8 * c;
+      const uint16_t *nrow =
+          p.base_out + static_cast<size_t>(my_row1 < 0 ? 0 : my_row1) * p.n_out + 8 * c;
+#pragma unroll
+      for (int qi = 0; qi < kMaxQuads; ++qi) {
+        const int quad = warp + qi * kWarps;
+        if (quad * 4 < n_tiles) {  // warp-uniform
+          float d[4][4];
+          expand_quad<RP>(d, sB, hh, hl, quad, p.n_out);
+          const bool col_ok = quad * 32 + 8 * c < p.n_out;
+          if (my_row >= 0 && col_ok) {
+            const uint4 b = base_v[qi];
+            uint4 o;
+            o.x = fold_pair(b.x, d[0][0], d[0][1], scale);
+            o.y = fold_pair(b.y, d[1][0], d[1][1], scale);
+            o.z = fold_pair(b.z, d[2][0], d[2][1], scale);
+            o.w = fold_pair(b.w, d[3][0], d[3][1], scale);
+            st_v4(orow + quad * 32, o);
+          }
+          if (pre)
+            base_v[qi] = (my_row1 >= 0 && col_ok) ? ld_cg_v4(nrow + quad * 32) : make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    __syncthreads();  // sP / sH are rewritten by the next pass
+    if (pre) {
+      my_row = my_row1;
+      issued = true;
+    }
+  }
+  // A pair requested but never waited for (no pass ran): let it land before exit.
+  if (pair && !have_pair && !bad) {
+    const bool t = !mbar_wait_bounded(bar_w, ph_w);
+    if (t && tid == 0) record_error(kErrWaitTimeout);
+  }
+}
+
+int g_path_override = 0;  // 0 auto, 1 this kernel, 2 the cluster kernel
+int g_spec_mode = 0;
+constexpr uint32_t kSmemTwoPerSm = 113 * 1024 - 2048;  // with ~1.3 KB static and 1 KB reserved
+
+uint32_t round_up(uint32_t v, uint32_t m) { return (v + m - 1) / m * m; }
+
+int decode_grid() { return sm_count() < kMaxCtas ? sm_count() : kMaxCtas; }
+
+uint32_t layout(DecodeParams &p, int rp) {
+  const uint32_t kpad = round_up(static_cast<uint32_t>(p.k_in), 32) * 2;
+  uint32_t sa = kpad;
+  if (sa % 128 == 0) sa += 64;  // 16-byte operand loads of 8 rows conflict-free
+  p.stride_a = sa;
+  uint32_t off = 0;
+  p.off_a = off;
+  off += rp * sa;
+  p.off_x = off;
+  off += kRows * sa;
+  p.zero_bytes = round_up(off, 16);
+  off = round_up(off, 128);
+  p.off_b = off;
+  off += round_up(static_cast<uint32_t>(p.n_out) * rp * 2, 128);
+  p.off_p = off;  // shrink partials
+  off += kWarps * kRows * (rp + 4) * 4;
+  p.off_h = off;
+  off += 2 * kRows * rp * 2;
+  p.smem_bytes = round_up(off, 128);
+  return p.smem_bytes;
+}
+
+template <int RP>
+cudaError_t launch(const DecodeParams &p, int grid, cudaStream_t stream) {
+  static std::once_flag once[64];
+  static cudaError_t attr_err[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(once[dev & 63], [d = dev & 63] {
+    attr_err[d] = cudaFuncSetAttribute(decode_fold_kernel<RP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemTwoPerSm));
+  });
+  if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_fold_kernel<RP>, p);
+}
+
+}  // namespace
+
+uint32_t decode_read_errors(bool clear) {
+  uint32_t v = 0;
+  cudaMemcpyFromSymbol(&v, g_decode_errors, sizeof v);
+  if (clear) {
+    const uint32_t z = 0;
+    cudaMemcpyToSymbol(g_decode_errors, &z, sizeof z);
+  }
+  return v;
+}
+
+void gather_set_path_override(int path) { g_path_override = path; }
+void gather_set_speculation(int mode) { g_spec_mode = mode; }
+int gather_path_override() { return g_path_override; }
+
+// Whether the resident-pair kernel takes this problem (shapes already
+// validated): rank 16 or 32, n_out <= 2048, the pair, 8 x rows and the
+// buffers within half an SM, and at most one expert per SM.
+bool decode_fold_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t n_experts) {
+  if (max_rank != 16 && max_rank != 32) return false;
+  if (n_out > kMaxQuads * kWarps * 32) return false;
+  if (n_experts > decode_grid()) return false;
+  DecodeParams p = {};
+  p.k_in = k_in;
+  p.n_out = n_out;
+  return layout(p, max_rank) <= kSmemTwoPerSm;
+}
+
+cudaError_t decode_fold_launch(const uint16_t *x, const int32_t *indices,
+                               const int32_t *row_adapter, const uint64_t *a_table,
+                               const uint64_t *b_table, const float *scale_table,
+                               uint16_t *base_out, int32_t n_slots, int32_t k_in,
+                               int32_t max_rank, int32_t n_out, int32_t top_k,
+                               int32_t n_experts, cudaStream_t stream) {
+  DecodeParams p = {};
+  p.x = x;
+  p.indices = indices;
+  p.row_adapter = row_adapter;
+  p.a_table = a_table;
+  p.b_table = b_table;
+  p.scale_table = scale_table;
+  p.base_out = base_out;
+  p.n_slots = n_slots;
+  p.k_in = k_in;
+  p.n_out = n_out;
+  p.top_k = top_k;
+  p.n_experts = n_experts;
+  p.spec_mode = g_spec_mode;
+  layout(p, max_rank);
+  const int grid = decode_grid();  // owners, then helpers for experts with many rows
+  return max_rank == 16 ? launch<16>(p, grid, stream) : launch<32>(p, grid, stream);
+}
+
+}  // namespace mlg

@@ -598,6 +598,15 @@ extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
     return MLG_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(base_out)) return MLG_ERR_UNSUPPORTED;
 
+  // Expert pairs that fit half an SM go to the resident-pair kernel.
+  const int path = gather_path_override();
+  const bool resident = decode_fold_eligible(k_in, max_rank, n_out, n_experts);
+  if (path == 1 && !resident) return MLG_ERR_UNSUPPORTED;
+  if (path != 2 && resident)
+    return cuda_status(decode_fold_launch(x, indices, row_adapter, a_table, b_table, scale_table,
+                                          base_out, n_slots, k_in, max_rank, n_out, top_k,
+                                          n_experts, static_cast<cudaStream_t>(stream)));
+
   GatherParams p = {};
   p.x = x;
   p.indices = indices;

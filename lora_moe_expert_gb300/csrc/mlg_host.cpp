@@ -191,12 +191,16 @@ uint32_t grouped_read_errors(bool clear);
 void gather_set_cluster_override(int cs);
 void gather_set_nsplit_override(int ns2);
 void grouped_set_ctas(int ctas);
+uint32_t decode_read_errors(bool clear);
+void gather_set_path_override(int path);
+void gather_set_speculation(int mode);
 }  // namespace mlg
 
 extern "C" mlg_status mlg_read_device_errors(uint32_t *flags_out, int32_t clear) {
   if (flags_out == nullptr) return MLG_ERR_INVALID_ARG;
   cudaGetLastError();
-  const uint32_t v = mlg::gather_read_errors(clear != 0) | mlg::grouped_read_errors(clear != 0);
+  const uint32_t v = mlg::gather_read_errors(clear != 0) | mlg::grouped_read_errors(clear != 0) |
+                     mlg::decode_read_errors(clear != 0);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return mlg::cuda_status(err);
   *flags_out = v;
@@ -214,6 +218,14 @@ extern "C" mlg_status mlg_set_tuning(int32_t knob, int32_t value) {
       if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
         return MLG_ERR_INVALID_ARG;
       mlg::gather_set_nsplit_override(value);
+      return MLG_OK;
+    case MLG_TUNE_GATHER_PATH:
+      if (value < 0 || value > 2) return MLG_ERR_INVALID_ARG;
+      mlg::gather_set_path_override(value);
+      return MLG_OK;
+    case MLG_TUNE_GATHER_SPECULATION:
+      if (value < 0 || value > 2) return MLG_ERR_INVALID_ARG;
+      mlg::gather_set_speculation(value);
       return MLG_OK;
     case MLG_TUNE_GROUPED_CTAS:
       if (value < 0 || value > 65535) return MLG_ERR_INVALID_ARG;

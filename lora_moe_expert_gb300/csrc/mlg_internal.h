@@ -34,4 +34,14 @@ inline mlg_status check_shapes(int32_t k_in, int32_t max_rank, int32_t n_out) {
 
 int sm_count();  // multiprocessors of the current device (cached per device)
 
+// The resident-pair decode fold (mlg_decode.cu): eligibility and launch.
+int gather_path_override();  // 0 auto, 1 resident-pair kernel, 2 cluster kernel
+bool decode_fold_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t n_experts);
+cudaError_t decode_fold_launch(const uint16_t *x, const int32_t *indices,
+                               const int32_t *row_adapter, const uint64_t *a_table,
+                               const uint64_t *b_table, const float *scale_table,
+                               uint16_t *base_out, int32_t n_slots, int32_t k_in,
+                               int32_t max_rank, int32_t n_out, int32_t top_k,
+                               int32_t n_experts, cudaStream_t stream);
+
 }  // namespace mlg

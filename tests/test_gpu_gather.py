@@ -163,3 +163,93 @@ def test_device_side_errors_are_status_codes():
                             w.max_rank, w.n_out, w.top_k, prob.n_experts)
     assert ei.value.status == mlg.MLG_ERR_UNSUPPORTED
     assert np.array_equal(prob.base_bits(), w.base)
+
+
+# Shapes the resident-pair kernel takes (max_rank 16 or 32, n_out <= 2048, at
+# most one expert per SM); each runs through both kernels.
+RESIDENT_SHAPES = [
+    # (tokens, top_k, experts, k_in, n_out, max_rank, adapted, base, pad, bad_ids)
+    (33, 4, 4, 776, 136, 16, 1.0, 0.2, 0, 0),  # > 32 rows per expert, k and n tails
+    (40, 6, 12, 200, 1000, 32, 0.7, 0.2, 3, 2),  # zero cells, skipped and padded tokens
+    (3, 2, 152, 64, 2048, 16, 1.0, 0.0, 0, 0),  # one expert per SM, most without rows
+    (50, 4, 9, 1032, 40, 32, 0.5, 0.3, 1, 1),  # one partial 32-column quad
+    (1, 1, 1, 32, 8, 16, 1.0, 0.0, 0, 0),  # smallest
+    (96, 8, 128, 1024, 512, 16, 0.9, 0.1, 2, 3),  # long k, many rows
+    (64, 2, 8, 256, 512, 16, 1.0, 0.0, 0, 0),  # 16 rows per expert: a helper CTA each
+    (96, 4, 6, 128, 264, 32, 0.8, 0.1, 1, 1),  # ~64 rows per expert: many passes
+]
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("shape", RESIDENT_SHAPES, ids=lambda s: "x".join(map(str, s[:6])))
+def test_resident_and_cluster_kernels(shape, path):
+    T, K, E, k_in, n_out, r, adapted, base, pad, bad = shape
+    w = synth.custom_gather(300 + T, T, K, E, k_in, n_out, r, adapted_frac=adapted,
+                            base_frac=base, pad=pad, bad_ids=bad)
+    try:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, path)
+        _run_and_check(w)
+    finally:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_speculation_modes_give_the_same_bits(mode):
+    """Row lists scanned before the preceding kernel completes are checked
+    after it: with no early scan (1) or an early scan that always disagrees
+    (2, every row requested again) the bits are those of the default mode."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_gather(21, 48, 8, 64, 768, 1024, 16, adapted_frac=0.9, base_frac=0.2)
+    outs = []
+    try:
+        for m in (0, mode):
+            mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_SPECULATION, m)
+            prob = FoldProblem(w)
+            prob.run()
+            torch.cuda.synchronize()
+            outs.append(prob.base_bits())
+    finally:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_SPECULATION, 0)
+    assert np.array_equal(outs[0], outs[1])
+    ref, folded, _ = fh.oracle_reference(w)
+    fh.check_fold(outs[1], w.base, ref, folded)
+
+
+def test_routing_written_by_the_preceding_kernel():
+    """The routing is rewritten on the stream right before the fold (by a
+    kernel the fold may overlap): the fold uses the new routing."""
+    import copy
+
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_gather(22, 64, 8, 128, 768, 2048, 16)
+    w2 = copy.deepcopy(w)
+    w2.indices = np.roll(w.indices, 8 * 5).copy()  # another token order
+    prob = FoldProblem(w)
+    new_idx = torch.from_numpy(w2.indices.astype(np.int32)).cuda()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        prob.reset()
+        prob.indices.fill_(-1)
+        prob.indices.copy_(new_idx)
+        prob.run(stream=s)
+    torch.cuda.synchronize()
+    ref, folded, _ = fh.oracle_reference(w2)
+    fh.check_fold(prob.base_bits(), w2.base, ref, folded)
+
+
+def test_resident_kernel_rejects_other_shapes():
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_gather(23, 8, 2, 4, 128, 128, 64)
+    prob = FoldProblem(w)
+    try:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 1)
+        with pytest.raises(mlg.MlgError) as ei:
+            prob.run()
+        assert ei.value.status == mlg.MLG_ERR_UNSUPPORTED
+    finally:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+    assert np.array_equal(prob.base_bits(), w.base)

@@ -300,3 +300,7 @@ def test_status_strings_and_tuning(L):
     with pytest.raises(mlg.MlgError):
         mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_CLUSTER, 3)
     mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_CLUSTER, 0)
+    for knob in (mlg.MLG_TUNE_GATHER_PATH, mlg.MLG_TUNE_GATHER_SPECULATION):
+        with pytest.raises(mlg.MlgError):
+            mlg.mlg_set_tuning(knob, 3)
+        mlg.mlg_set_tuning(knob, 0)

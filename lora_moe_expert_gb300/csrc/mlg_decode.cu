@@ -22,12 +22,13 @@
 //  * shrink h = x A_e^T with mma.sync m16n8k16 (M = rank, N = 8 rows, k split
 //    over the warps, partial sums added in a fixed order), h split into bf16
 //    hi + lo halves (h enters the expand at ~2^-17 relative precision);
-//  * expand with M = 8 rows (of 16), N = 8 columns of B_e, K = rank; each lane
-//    takes adjacent rank words of B_e and h (the same physical rank assignment
-//    for both operands), and the B_e rows are dealt to the MMA columns so that
-//    every lane ends with 8 adjacent output columns of one row: base_out is
-//    read (into registers, right after the wait) and written with 16-byte
-//    accesses, rounded once: RNE(base + scale * delta);
+//  * expand with swapped operands, M = 16 rows of B_e, N = the 8 rows, K =
+//    rank; each lane takes adjacent rank words of B_e and h (the same physical
+//    rank assignment for both operands), and the B_e rows are dealt to the M
+//    rows so that every lane ends with 8 adjacent output columns of two rows:
+//    base_out is read (into registers, right after the wait) and written with
+//    16-byte accesses, rounded once: RNE(base + scale * delta).  B_e sits in
+//    shared memory with its rows XOR-permuted for conflict-free loads;
 //  * an expert with more than 8 rows gets a helper CTA (the SMs left over by
 //    the experts): owner and helper fold alternate passes of 8 rows, both
 //    deciding the split from the same per-expert row counts.
@@ -45,8 +46,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRows = 8;         // rows per pass: expand M rows g = 0..7
-constexpr int kMaxQuads = 8;     // 32-column output quads per warp (n_out <= 2048)
-constexpr int kScanPer = 8;      // rows per thread per scan chunk
+constexpr int kMaxBlocks = 4;    // 64-column output blocks per warp (n_out <= 2048)
+constexpr int kScanPer = 2;      // rows per thread per scan chunk (small code)
 constexpr int kScanChunk = kScanPer * kThreads;
 constexpr int kSpecRows = 32;    // rows of the speculative scan kept for L2 prefetch
 constexpr int kMaxCtas = 160;    // owner + helper CTAs (and table entries) at most
@@ -171,18 +172,22 @@ __device__ __forceinline__ void request_x(const DecodeParams &p, int warp, int l
   }
 }
 
-// This lane's base_out row (row g of the pass) in 16-byte chunks: columns
-// quad*32 + 8c .. +7 of the warp's quads, into registers.
+// This lane's base_out rows (rows 2c and 2c+1 of the pass) in 16-byte chunks:
+// columns blk*64 + 8g .. +7 of the warp's 64-column blocks, into registers.
 __device__ __forceinline__ void request_base(const DecodeParams &p, int warp, int g, int c,
-                                             int n_g, int n_tiles, const int *s_rows,
-                                             uint4 (&base_v)[kMaxQuads], int &my_row) {
-  my_row = g < n_g ? s_rows[g] : -1;
+                                             int n_g, const int *s_rows,
+                                             uint4 (&base_v)[kMaxBlocks][2], int (&my_row)[2]) {
+  my_row[0] = 2 * c < n_g ? s_rows[2 * c] : -1;
+  my_row[1] = 2 * c + 1 < n_g ? s_rows[2 * c + 1] : -1;
 #pragma unroll
-  for (int qi = 0; qi < kMaxQuads; ++qi) {
-    const int tile = (warp + qi * kWarps) * 4 + c;
-    base_v[qi] = make_uint4(0, 0, 0, 0);
-    if (my_row >= 0 && tile < n_tiles)
-      base_v[qi] = ld_cg_v4(p.base_out + static_cast<size_t>(my_row) * p.n_out + tile * 8);
+  for (int i = 0; i < kMaxBlocks; ++i) {
+    const int col = (warp + i * kWarps) * 64 + 8 * g;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      base_v[i][r] = make_uint4(0, 0, 0, 0);
+      if (my_row[r] >= 0 && col < p.n_out)
+        base_v[i][r] = ld_cg_v4(p.base_out + static_cast<size_t>(my_row[r]) * p.n_out + col);
+    }
   }
 }
 
@@ -209,33 +214,64 @@ __device__ __forceinline__ uint32_t fold_pair(uint32_t base2, float d0, float d1
   return o;
 }
 
-// The expand of one 32-column quad: M = the 8 rows (of 16), N = 8 columns per
-// tile, K = rank, h as hi + lo.  Tile t's MMA column n takes B_e row
-// quad*32 + 8*(n/2) + 2t + n%2, so lane (g, c) -- whose D holds MMA columns
-// 2c, 2c+1 of row g -- ends with row g, output columns quad*32 + 8c .. +7
-// (tile t gives columns 8c + 2t, 8c + 2t + 1): no transpose before the
-// 16-byte base_out access.  B_e rows at or past n_out read as zero.
+// Row slot of B_e row r in shared memory: within each 128-byte group of rows,
+// the slots are XOR-permuted by bits 3.. of r, so that the rows one expand
+// load touches (8g + 2t for g = 0..7) fall on distinct banks.
 template <int RP>
-__device__ __forceinline__ void expand_quad(float (&d)[4][4], const uint8_t *sB,
-                                            const uint32_t (&hh)[RP / 8],
-                                            const uint32_t (&hl)[RP / 8], int quad, int n_out) {
+__device__ __forceinline__ int b_slot(int r) {
+  constexpr int RPC = 64 / RP;  // rows per 128 bytes
+  return r ^ ((r >> 3) & (RPC - 1));
+}
+
+// Permute B_e (bulk-copied row-major into sB) into the slots of b_slot, in
+// place: each warp moves 256-byte spans, 8 bytes per lane.
+template <int RP>
+__device__ __forceinline__ void permute_b(uint8_t *sB, int n_out) {
+  constexpr int RB = 2 * RP;  // bytes per B_e row
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int spans = n_out * RB / 256;  // n_out % 8 == 0 and RB >= 32
+  for (int sp = warp; sp < spans; sp += kWarps) {
+    const int byte = sp * 256 + lane * 8;
+    const int r = byte / RB, off = byte % RB;
+    const uint2 v = *reinterpret_cast<const uint2 *>(sB + byte);
+    __syncwarp();
+    *reinterpret_cast<uint2 *>(sB + b_slot<RP>(r) * RB + off) = v;
+    __syncwarp();
+  }
+}
+
+// The expand of one 64-column block: swapped operands, M = 16 B_e rows, N =
+// the 8 rows of the pass, K = rank, h as hi + lo, four m-tiles t.  M-row g of
+// tile t takes B_e row blk*64 + 8g + 2t and M-row g+8 the next one, so lane
+// (g, c) -- whose D holds M-rows g, g+8 of rows 2c, 2c+1 -- ends with output
+// columns blk*64 + 8g .. +7 of both rows: tile t gives columns 8g + 2t (d[t][0]
+// row 2c, d[t][1] row 2c+1) and 8g + 2t + 1 (d[t][2], d[t][3]).  No transpose
+// before the 16-byte base_out accesses.  B_e rows at or past n_out read as 0.
+template <int RP>
+__device__ __forceinline__ void expand_block(float (&d)[4][4], const uint8_t *sB,
+                                             const uint32_t (&hh)[RP / 8],
+                                             const uint32_t (&hl)[RP / 8], int blk, int n_out) {
   constexpr int WPL = RP / 8, KST = RP / 16;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  const int col_base = quad * 32 + 8 * (g >> 1) + (g & 1);  // + 2t: this lane's B_e row
-  const bool full = quad * 32 + 32 <= n_out;                  // warp-uniform
+  const int row0 = blk * 64 + 8 * g;
+  const bool ok = row0 < n_out;  // n_out % 8 == 0: all 8 rows or none
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const int col = col_base + 2 * t;
-    uint32_t bw[WPL];
+    uint32_t b0[WPL], b1[WPL];
 #pragma unroll
-    for (int w = 0; w < WPL; ++w) bw[w] = 0u;
-    if (full || col < n_out) load_words<WPL>(bw, sB + (col * RP + c * WPL * 2) * 2);
+    for (int w = 0; w < WPL; ++w) b0[w] = b1[w] = 0u;
+    if (ok) {
+      load_words<WPL>(b0, sB + (b_slot<RP>(row0 + 2 * t) * RP + c * WPL * 2) * 2);
+      load_words<WPL>(b1, sB + (b_slot<RP>(row0 + 2 * t + 1) * RP + c * WPL * 2) * 2);
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u) d[t][u] = 0.f;
 #pragma unroll
     for (int st = 0; st < KST; ++st) {
-      mma_bf16_16816(d[t], hh[2 * st], 0u, hh[2 * st + 1], 0u, bw[2 * st], bw[2 * st + 1]);
-      mma_bf16_16816(d[t], hl[2 * st], 0u, hl[2 * st + 1], 0u, bw[2 * st], bw[2 * st + 1]);
+      mma_bf16_16816(d[t], b0[2 * st], b1[2 * st], b0[2 * st + 1], b1[2 * st + 1], hh[2 * st],
+                     hh[2 * st + 1]);
+      mma_bf16_16816(d[t], b0[2 * st], b1[2 * st], b0[2 * st + 1], b1[2 * st + 1], hl[2 * st],
+                     hl[2 * st + 1]);
     }
   }
 }
@@ -305,8 +341,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
   // wait it reads tables and weights, and the routing through L2 only.
   griddep_launch_dependents();
 
-  const int n_tiles = p.n_out / 8;
-  const int no_idx[kScanPer] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const int no_idx[kScanPer] = {};
   const int kblocks = (p.k_in + 31) / 32;
   const uint32_t row_bytes_x = static_cast<uint32_t>(p.k_in) * 2u;
   uint32_t ph_w = 0, ph_x = 0;
@@ -370,17 +405,31 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     prefetch_l2(p.base_out + static_cast<size_t>(row) * p.n_out, static_cast<uint32_t>(p.n_out) * 2u);
   }
   for (int i = tid; i < kMaxCtas; i += kThreads) s_hist[i] = 0;
+  // The pair lands while the preceding kernel runs; B_e into its bank-spread
+  // row slots.
+  bool have_pair = false;
+  if (pair) {  // one thread polls, pausing; the others sleep in the barrier
+    const bool t = tid == 0 && !mbar_wait_bounded_sleep(bar_w, ph_w, 128);
+    ph_w ^= 1u;
+    have_pair = true;
+    if (__syncthreads_or(t)) {
+      if (tid == 0) record_error(kErrWaitTimeout);
+      bad = true;
+    } else {
+      permute_b<RP>(smem + p.off_b, p.n_out);
+    }
+  }
   __syncthreads();
   griddep_wait();  // routing, x and base_out may be written by the preceding kernel
 
   // ---- after the wait: the speculative first pass's x and base_out rows, the
   // fresh scan's loads and its base_out loads are all in flight together.
-  uint4 base_v[kMaxQuads];
-  int my_row = -1;
+  uint4 base_v[kMaxBlocks][2];
+  int my_row[2] = {-1, -1};
   if (n_spec > 0) request_x(p, warp, lane, n_spec, row_bytes_x, bad, s_spec + spec_g0, sX, bar_x);
   int idx0[kScanPer], ra0[kScanPer];
   scan_load(p, 0, idx0, ra0);
-  if (n_spec > 0) request_base(p, warp, g, c, n_spec, n_tiles, s_spec + spec_g0, base_v, my_row);
+  if (n_spec > 0) request_base(p, warp, g, c, n_spec, s_spec + spec_g0, base_v, my_row);
   int fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, idx0, ra0, true, s_hist);
   assign_helper(s_hist, p.n_experts, n_helpers, helper, who, &s_role);
   __syncthreads();
@@ -388,19 +437,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
   bool timed_out = false;
   if (helper && role != e) {  // the speculation picked another expert (or none)
     if (n_spec > 0) {
-      timed_out = !bad && !mbar_wait_bounded(bar_x, ph_x);
+      timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
       ph_x ^= 1u;
     }
-    if (pair) {
-      timed_out = (!bad && !mbar_wait_bounded(bar_w, ph_w)) || timed_out;
+    if (pair && !have_pair) {
+      timed_out = (!bad && tid == 0 && !mbar_wait_bounded(bar_w, ph_w)) || timed_out;
       ph_w ^= 1u;
     }
+    have_pair = false;
     if (__syncthreads_or(timed_out)) {
       if (!bad && tid == 0) record_error(kErrWaitTimeout);
       bad = true;
     }
     n_spec = 0;
-    my_row = -1;
+    my_row[0] = my_row[1] = -1;
     e = role;
     pair = false;
     if (e >= 0 && !bad) {
@@ -413,20 +463,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     bool differ = tid == 0 && fresh != total;
     if (tid < n_spec && s_rows[spec_g0 + tid] != s_spec[spec_g0 + tid]) differ = true;
     if (__syncthreads_or(differ)) {  // let the copies of the stale rows land first
-      timed_out = !bad && !mbar_wait_bounded(bar_x, ph_x);
+      timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
       ph_x ^= 1u;
       if (__syncthreads_or(timed_out)) {
         if (!bad && tid == 0) record_error(kErrWaitTimeout);
         bad = true;
       }
       n_spec = 0;
-      my_row = -1;
+      my_row[0] = my_row[1] = -1;
     }
   }
   total = pair ? fresh : 0;
   const int stride = (helper || role == 1) ? 2 : 1;  // passes of 8 rows this CTA folds
   bool issued = n_spec > 0;  // the first pass's x copies and base_out loads are in flight
-  bool have_pair = false;
   int list0 = 0;             // rank of s_rows[0] in the row list
 
   for (int g0 = kRows * first; g0 < total && !bad; g0 += kRows * stride) {
@@ -438,16 +487,25 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     const int n_g = min(kRows, total - g0);
     if (!issued) {
       request_x(p, warp, lane, n_g, row_bytes_x, bad, rows, sX, bar_x);
-      request_base(p, warp, g, c, n_g, n_tiles, rows, base_v, my_row);
+      request_base(p, warp, g, c, n_g, rows, base_v, my_row);
     }
     issued = false;
     timed_out = false;
-    if (!have_pair) timed_out = !mbar_wait_bounded(bar_w, ph_w);
-    if (!timed_out) timed_out = !mbar_wait_bounded(bar_x, ph_x);
-    if (!have_pair) ph_w ^= 1u;
+    if (!have_pair) {  // the pair lands; B_e into its bank-spread row slots
+      timed_out = tid == 0 && !mbar_wait_bounded(bar_w, ph_w);
+      ph_w ^= 1u;
+      have_pair = true;
+      if (__syncthreads_or(timed_out)) {
+        if (tid == 0) record_error(kErrWaitTimeout);
+        bad = true;
+        break;
+      }
+      permute_b<RP>(smem + p.off_b, p.n_out);
+    }
+    // One thread polls; the barrier passes what it observed to the others.
+    timed_out = tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
     ph_x ^= 1u;
-    have_pair = true;
-    if (__syncthreads_or(timed_out)) {
+    if (__syncthreads_or(timed_out)) {  // (also orders the permuted B_e before its reads)
       if (tid == 0) record_error(kErrWaitTimeout);
       bad = true;
       break;
@@ -488,7 +546,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     const bool pre = g1 < total && g1 < list0 + kSpecRows;  // CTA-uniform
     const int *rows1 = s_rows + (g1 - list0);
     const int n_g1 = pre ? min(kRows, total - g1) : 0;
-    const int my_row1 = g < n_g1 ? rows1[g] : -1;
+    int my_row1[2];
+    my_row1[0] = 2 * c < n_g1 ? rows1[2 * c] : -1;
+    my_row1[1] = 2 * c + 1 < n_g1 ? rows1[2 * c + 1] : -1;
     if (pre) request_x(p, warp, lane, n_g1, row_bytes_x, bad, rows1, sX, bar_x);
     // Sum the warps' partials in warp order; split h into bf16 hi + lo.
     if (tid < kRows * RP / 2) {
@@ -507,46 +567,64 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     }
     __syncthreads();
 
-    // ---- expand + epilogue (see expand_quad).  Lane c takes rank words
+    // ---- expand + epilogue (see expand_block).  Lane c takes rank words
     // c*WPL .. c*WPL+WPL-1 of h and of B_e: k-step st uses word c*WPL + 2st
     // (logical k 2c, 2c+1) and the next (logical 2c+8, 2c+9).
     {
       uint32_t hh[WPL], hl[WPL];
       load_words<WPL>(hh, sHhi + (g * RP + c * WPL * 2) * 2);
       load_words<WPL>(hl, sHlo + (g * RP + c * WPL * 2) * 2);
-      uint16_t *orow = p.base_out + static_cast<size_t>(my_row < 0 ? 0 : my_row) * p.n_out + 8 * c;
-      const uint16_t *nrow =
-          p.base_out + static_cast<size_t>(my_row1 < 0 ? 0 : my_row1) * p.n_out + 8 * c;
-#pragma unroll
-      for (int qi = 0; qi < kMaxQuads; ++qi) {
-        const int quad = warp + qi * kWarps;
-        if (quad * 4 < n_tiles) {  // warp-uniform
+      // One loop body for all blocks (small code: the instruction cache is
+      // cold in a CTA that runs once); base_v[0] is always the current block,
+      // the registers rotate down and the next pass's loads enter at the top.
+#pragma unroll 1
+      for (int i = 0; i < kMaxBlocks; ++i) {
+        const int blk = warp + i * kWarps;
+        uint4 nv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (blk * 64 < p.n_out) {  // warp-uniform
           float d[4][4];
-          expand_quad<RP>(d, sB, hh, hl, quad, p.n_out);
-          const bool col_ok = quad * 32 + 8 * c < p.n_out;
-          if (my_row >= 0 && col_ok) {
-            const uint4 b = base_v[qi];
-            uint4 o;
-            o.x = fold_pair(b.x, d[0][0], d[0][1], scale);
-            o.y = fold_pair(b.y, d[1][0], d[1][1], scale);
-            o.z = fold_pair(b.z, d[2][0], d[2][1], scale);
-            o.w = fold_pair(b.w, d[3][0], d[3][1], scale);
-            st_v4(orow + quad * 32, o);
+          expand_block<RP>(d, sB, hh, hl, blk, p.n_out);
+          const int col = blk * 64 + 8 * g;
+          const bool col_ok = col < p.n_out;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            if (my_row[r] >= 0 && col_ok) {
+              const uint4 b = base_v[0][r];
+              uint4 o;
+              o.x = fold_pair(b.x, d[0][r], d[0][r + 2], scale);
+              o.y = fold_pair(b.y, d[1][r], d[1][r + 2], scale);
+              o.z = fold_pair(b.z, d[2][r], d[2][r + 2], scale);
+              o.w = fold_pair(b.w, d[3][r], d[3][r + 2], scale);
+              st_v4(p.base_out + static_cast<size_t>(my_row[r]) * p.n_out + col, o);
+            }
+            if (pre && my_row1[r] >= 0 && col_ok)
+              nv[r] = ld_cg_v4(p.base_out + static_cast<size_t>(my_row1[r]) * p.n_out + col);
           }
-          if (pre)
-            base_v[qi] = (my_row1 >= 0 && col_ok) ? ld_cg_v4(nrow + quad * 32) : make_uint4(0, 0, 0, 0);
         }
+#pragma unroll
+        for (int k = 0; k + 1 < kMaxBlocks; ++k) {
+          base_v[k][0] = base_v[k + 1][0];
+          base_v[k][1] = base_v[k + 1][1];
+        }
+        base_v[kMaxBlocks - 1][0] = nv[0];
+        base_v[kMaxBlocks - 1][1] = nv[1];
       }
     }
     __syncthreads();  // sP / sH are rewritten by the next pass
     if (pre) {
-      my_row = my_row1;
+      my_row[0] = my_row1[0];
+      my_row[1] = my_row1[1];
       issued = true;
     }
   }
-  // A pair requested but never waited for (no pass ran): let it land before exit.
-  if (pair && !have_pair && !bad) {
-    const bool t = !mbar_wait_bounded(bar_w, ph_w);
+  // Let every copy still in flight land before exit (a pair requested but
+  // never waited for when no pass ran; after a timeout, whatever was issued).
+  if (pair && !have_pair) {
+    const bool t = tid == 0 && !mbar_wait_bounded(bar_w, ph_w);
+    if (t && tid == 0) record_error(kErrWaitTimeout);
+  }
+  if (issued) {
+    const bool t = tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
     if (t && tid == 0) record_error(kErrWaitTimeout);
   }
 }
@@ -627,7 +705,7 @@ int gather_path_override() { return g_path_override; }
 // buffers within half an SM, and at most one expert per SM.
 bool decode_fold_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t n_experts) {
   if (max_rank != 16 && max_rank != 32) return false;
-  if (n_out > kMaxQuads * kWarps * 32) return false;
+  if (n_out > kMaxBlocks * kWarps * 64) return false;
   if (n_experts > decode_grid()) return false;
   DecodeParams p = {};
   p.k_in = k_in;

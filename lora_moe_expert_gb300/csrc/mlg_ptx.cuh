@@ -64,6 +64,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   }
 }
 
+// The same with a pause between polls, for a waiter that is not on the
+// critical path (it leaves issue slots to the warps that are).
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t parity,
+                                                        uint32_t pause_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(pause_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // ---------------------------------------------------------------- bulk copies
 // Global -> this CTA's shared memory, completion counted on `bar` in bytes.
 // Both addresses 16-byte aligned, size a multiple of 16.

@@ -88,9 +88,6 @@ __device__ __forceinline__ void st_v4(void *p, uint4 v) {
                "r"(v.w)
                : "memory");
 }
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // Issue the routing loads of one scan chunk (rows base + i*256 + tid).
 __device__ __forceinline__ void scan_load(const DecodeParams &p, int base, int (&idx)[kScanPer],

@@ -225,28 +225,21 @@ __global__ void __launch_bounds__(kGThreads, 1)
   for (uint32_t i = tid * 16; i < p.off_h; i += kGThreads * 16)
     *reinterpret_cast<uint4 *>(smem + i) = make_uint4(0, 0, 0, 0);
   // Tile table: tiles of expert e = ceil(rows of e in the window / 128), 0 if
-  // the expert folds nothing; exclusive prefix over experts.
+  // the expert folds nothing; exclusive prefix over experts.  One expert per
+  // thread per pass, its four loads issued together.
   {
-    constexpr int kPer = 16;  // experts per thread per pass
     int carry = 0;
-    for (int base = 0; base < n_e; base += kGThreads * kPer) {
-      int cnt[kPer];
-      int sum = 0;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = base + tid * kPer + i;
-        int n = 0;
-        if (e < n_e) {
-          const int lo = span_lo(p, e), hi = span_hi(p, e);
-          if (hi > lo && cells_fold(__ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + e),
-                                    __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + e)))
-            n = span_tiles(p, lo, hi);
-        }
-        cnt[i] = n;
-        sum += n;
+    for (int base = 0; base < n_e; base += kGThreads) {
+      const int e = base + tid;
+      int n = 0;
+      if (e < n_e) {
+        const int lo = span_lo(p, e), hi = span_hi(p, e);
+        const uint64_t a = __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + e);
+        const uint64_t b = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + e);
+        if (hi > lo && cells_fold(a, b)) n = span_tiles(p, lo, hi);
       }
-      // block exclusive scan of the per-thread sums
-      int incl = sum;
+      // block exclusive scan
+      int incl = n;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, d);
@@ -256,17 +249,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
       if (lane == 31) warp_tot[warp] = incl;
       __syncthreads();
       int before = carry, total = 0;
+#pragma unroll
       for (int w = 0; w < kGThreads / 32; ++w) {
         before += (w < warp) ? warp_tot[w] : 0;
         total += warp_tot[w];
       }
-      int run = before + incl - sum;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = base + tid * kPer + i;
-        if (e < n_e) tile_start[e] = run;
-        run += cnt[i];
-      }
+      if (e < n_e) tile_start[e] = before + incl - n;
       carry += total;
       __syncthreads();
     }
@@ -289,7 +277,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     my_tiles[tid].scale = __ldg(p.scale_table + ti.e);
   }
   __syncthreads();
-  for (int i = warp; i < my_count * 4; i += kGThreads / 32) {  // one warp per 32 rows
+  // Fold bitmasks, one warp per 32 rows.
+  for (int i = warp; i < my_count * 4; i += kGThreads / 32) {
     const MyTile mt = my_tiles[i >> 2];
     const int r = mt.r0 + (i & 3) * 32 + lane;
     bool f = false;

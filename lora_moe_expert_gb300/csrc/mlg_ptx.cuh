@@ -77,6 +77,11 @@ __device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t p
   }
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned address and size).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- bulk copies
 // Global -> this CTA's shared memory, completion counted on `bar` in bytes.
 // Both addresses 16-byte aligned, size a multiple of 16.

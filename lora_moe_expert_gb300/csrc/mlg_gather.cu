@@ -46,6 +46,7 @@ constexpr int kMaxRowGroup = 32;                 // most rows of one expert fold
 constexpr int kScanPer = 8;                      // rows per thread per scan chunk
 constexpr int kScanChunk = kScanPer * kThreads;  // 2048 rows
 constexpr int kMaxMtPerPass = 8;  // B_e m-tiles x k-steps a warp holds in registers
+constexpr int kMaxCompact = 512;  // tables up to this length are compacted to foldable experts
 
 static __device__ uint32_t g_gather_errors;
 
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
   __shared__ __align__(8) uint64_t bars[2];  // 0: weights, 1: rows
   __shared__ int s_rows[kMaxRowGroup];
   __shared__ int s_cnt[kScanPer][kWarps];
+  __shared__ int s_ex[kMaxCompact];  // foldable experts, in id order
 
   constexpr int MT = RP / 16;   // rank m-tiles of the shrink
   constexpr int KST = RP / 16;  // k-steps of the expand
@@ -209,10 +211,39 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
   bool bad = false;
   bool waited = false;  // griddep_wait() done (before the first routing / x / base read)
 
-  const int n_units = p.n_experts * p.ns2;  // (expert, n slice) pairs
+  // Units are (expert, n slice) pairs over the experts whose cells fold
+  // (tables are never written by the preceding kernel: read before the wait),
+  // so no cluster spends a round on an expert that folds nothing.
+  const bool compact = p.n_experts <= kMaxCompact;
+  int n_fold = p.n_experts;
+  if (compact) {
+    n_fold = 0;
+    for (int b = 0; b < p.n_experts; b += kThreads) {
+      const int ex = b + tid;
+      bool f = false;
+      if (ex < p.n_experts) {
+        const uint64_t a = __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + ex);
+        const uint64_t bb = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ex);
+        f = a != 0 && bb != 0 && ((a | bb) & 15u) == 0;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, f);
+      if (lane == 0) s_cnt[0][warp] = __popc(m);
+      __syncthreads();
+      int before = n_fold, tot = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        before += (w < warp) ? s_cnt[0][w] : 0;
+        tot += s_cnt[0][w];
+      }
+      if (f) s_ex[before + __popc(m & ((1u << lane) - 1u))] = ex;
+      n_fold += tot;
+      __syncthreads();
+    }
+  }
+  const int n_units = n_fold * p.ns2;
   for (int unit = static_cast<int>(cluster_id_x()); unit < n_units;
        unit += static_cast<int>(ncluster_x())) {
-    const int e = unit / p.ns2;
+    const int e = compact ? s_ex[unit / p.ns2] : unit / p.ns2;
     const int ni = (unit % p.ns2) * static_cast<int>(cs) + static_cast<int>(q);  // n slice
     const int n0 = ni * p.ns;
     const int nsv = max(0, min(p.ns, p.n_out - n0));
@@ -519,9 +550,10 @@ uint32_t layout(GatherParams &p, int cs, int ns2, int rp) {
 
 int g_cluster_override = 0;
 int g_nsplit_override = 0;
-// Two CTAs per SM: each may use up to half of the 228 KB, less static memory.
-constexpr uint32_t kSmemTwoPerSm = 113 * 1024 - 1024;
-constexpr uint32_t kSmemLimit = 227 * 1024 - 2048;
+// Two CTAs per SM: each may use up to half of the 228 KB, less its ~2.5 KB of
+// static shared memory and the 1 KB the driver reserves per CTA.
+constexpr uint32_t kSmemTwoPerSm = 113 * 1024 - 3072;
+constexpr uint32_t kSmemLimit = 227 * 1024 - 3072;  // leaves room for the static part
 
 template <int RP>
 cudaError_t launch(const GatherParams &p, int cs, int clusters, cudaStream_t stream) {
@@ -623,19 +655,17 @@ extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
   p.n_experts = n_experts;
   const int rp = static_cast<int>(round_up(max_rank, 16));
   // Rows per pass: decode batches spread ~n_slots / n_experts rows per expert.
-  p.rg = (n_slots <= 8 * n_experts) ? 16 : 32;
+  p.rg = (n_slots <= 16 * n_experts) ? 16 : 32;
 
   // Split: when A_e is at most half of B_e, every CTA computes the whole
-  // shrink and the expert's n range is split over ns2 independent CTAs; else
-  // a cluster of cs CTAs splits k (partial h summed in shared memory) and n.
-  // Each CTA's share of the pair is bounded to ~64 KB, and the layout should
-  // leave room for two CTAs per SM.
+  // shrink and the expert's n range is split over ns2 independent CTAs
+  // (each CTA's share of the pair bounded to ~64 KB); else a cluster of cs
+  // CTAs splits k (partial h summed in shared memory) and n, cs the smallest
+  // that leaves room for two CTAs per SM.
   const double a_bytes = 2.0 * max_rank * k_in, b_bytes = 2.0 * max_rank * n_out;
   int cs = 1, ns2 = 1;
   if (2.0 * a_bytes <= b_bytes) {
     while (ns2 < 8 && a_bytes + b_bytes / ns2 > 64.0 * 1024) ns2 *= 2;
-  } else {
-    while (cs < 8 && (a_bytes + b_bytes) / cs > 64.0 * 1024) cs *= 2;
   }
   if (g_cluster_override > 0) cs = g_cluster_override;
   if (g_nsplit_override > 0) ns2 = g_nsplit_override;
@@ -643,9 +673,11 @@ extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
     while (layout(p, cs, ns2, rp) > kSmemTwoPerSm && cs < 8) cs *= 2;
   if (layout(p, cs, ns2, rp) > kSmemLimit) return MLG_ERR_UNSUPPORTED;
 
-  // One cluster per (expert, n slice), looping when there are more than fit.
+  // One cluster per (expert, n slice), looping when there are more than fit;
+  // the grid is what can be resident at once (no second wave of CTAs).
   const int64_t units = static_cast<int64_t>(n_experts) * ns2;
-  const int max_clusters = (4 * sm_count()) / cs;
+  const int per_sm = layout(p, cs, ns2, rp) <= kSmemTwoPerSm ? 2 : 1;
+  const int max_clusters = (per_sm * sm_count()) / cs > 0 ? (per_sm * sm_count()) / cs : 1;
   const int clusters = units < max_clusters ? static_cast<int>(units) : max_clusters;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;

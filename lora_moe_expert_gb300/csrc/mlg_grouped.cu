@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int half = warp == 1 ? 0 : 1;
     const uint64_t keep = l2_evict_last();  // x rows and A_e are re-read by other tiles
     uint32_t it = 0;
-    int q[4] = {-1, -1, -1, -1};  // issued, not yet signalled stages (q[0] oldest)
+    int q[6] = {-1, -1, -1, -1, -1, -1};  // issued, not yet signalled stages (q[0] oldest)
     int nq = 0;
     // x token of this lane's two rows, loaded one tile ahead
     auto tokens = [&](int t, int (&tok)[2]) {
@@ -408,46 +408,46 @@ __global__ void __launch_bounds__(kGThreads, 1)
         xrow[u] = p.x + static_cast<size_t>(tok_next[u] >= 0 ? tok_next[u] : 0) * p.k_in * 2;
       }
       tokens(t + 1, tok_next);
-      const int j = half * 32 + lane;  // A_e row of this lane
       for (int kc = 0; kc < p.kc_count; ++kc, ++it) {
         const int st = it % p.nxa;
         if (!wait_bar(ctl, ctl.xa_empty[st], ((it / p.nxa) & 1) ^ 1)) goto prod_a_done;
         const uint32_t xs = xa_base + st * p.xa_stage;
         const uint32_t as = xs + kTileM * 128;
         const int k0 = kc * 64;
+        // Each copy instruction takes 4 whole 128-byte row segments (8 lanes
+        // per row), so every request is a full line.
+        const int c = lane & 7;
+        const int kk = k0 + 8 * c;
+        const bool in = kk < p.k_in;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (!xv[u]) continue;
-          const int row = half * 64 + lane + 32 * u;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int kk = k0 + 8 * c;
-            const bool in = kk < p.k_in;
-            cp_async_16_hint(xs + sw128(row, c), xrow[u] + (in ? kk * 2 : 0), in ? 16u : 0u, keep);
-          }
+        for (int i = 0; i < 16; ++i) {
+          const int rl = 4 * i + (lane >> 3);  // row of this warp's 64
+          const uint8_t *xr = reinterpret_cast<const uint8_t *>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(xrow[rl >> 5]), rl & 31));
+          const bool v = __shfl_sync(0xffffffffu, xv[rl >> 5], rl & 31);
+          if (v) cp_async_16_hint(xs + sw128(half * 64 + rl, c), xr + (in ? kk * 2 : 0), in ? 16u : 0u, keep);
         }
-        if (j < p.rank) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int kk = k0 + 8 * c;
-            const bool in = kk < p.k_in;
-            cp_async_16_hint(as + sw128(j, c),
-                             A + (static_cast<size_t>(j) * p.k_in + (in ? kk : 0)) * 2,
+        for (int i = 0; i < 8; ++i) {
+          const int ja = half * 32 + 4 * i + (lane >> 3);  // A_e row
+          if (ja < p.rank)
+            cp_async_16_hint(as + sw128(ja, c),
+                             A + (static_cast<size_t>(ja) * p.k_in + (in ? kk : 0)) * 2,
                              in ? 16u : 0u, keep);
-          }
         }
         cp_async_commit();
         if (nq == p.xa_lag) {  // oldest pending stage: <= xa_lag newer groups remain
           switch (p.xa_lag) {
             case 1: cp_async_wait_group<1>(); break;
             case 2: cp_async_wait_group<2>(); break;
-            default: cp_async_wait_group<3>(); break;
+            case 3: cp_async_wait_group<3>(); break;
+            case 4: cp_async_wait_group<4>(); break;
+            default: cp_async_wait_group<5>(); break;
           }
           fence_proxy_async_smem();
           mbar_arrive(smem_addr(&ctl.xa_full[q[0]]));
-          q[0] = q[1];
-          q[1] = q[2];
-          q[2] = q[3];
+#pragma unroll
+          for (int i = 0; i < 5; ++i) q[i] = q[i + 1];
           --nq;
         }
         q[nq++] = st;
@@ -475,12 +475,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (!wait_bar(ctl, ctl.b_empty[st], ((it / p.nbs) & 1) ^ 1)) goto prod_b_done;
         const uint32_t bs = b_base + st * p.b_stage;
         const int n0 = nc * p.n_ch;
-        for (int i = lane; i < p.n_ch; i += 32) {
-          const int n = n0 + i;
-          const bool in = n < p.n_out;
-          const uint8_t *brow = B + static_cast<size_t>(in ? n : 0) * p.rank * 2;
-          for (int c = 0; c < rc; ++c)
+        // Lanes take whole B_e rows: rc lanes per row, 32 / rc rows per copy.
+        {
+          const int per = 32 / rc, c = lane % rc;
+          for (int i = lane / rc; lane < per * rc && i < p.n_ch; i += per) {
+            const int n = n0 + i;
+            const bool in = n < p.n_out;
+            const uint8_t *brow = B + static_cast<size_t>(in ? n : 0) * p.rank * 2;
             cp_async_16_hint(bs + sw128(i, c), brow + c * 16, in ? 16u : 0u, keep);
+          }
         }
         cp_async_commit();
         if (nq == lag) {  // the oldest pending stage has landed once <= lag groups remain

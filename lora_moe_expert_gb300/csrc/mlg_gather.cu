@@ -90,11 +90,11 @@ __device__ __forceinline__ void scan_load(const GatherParams &p, int base, int (
   }
 }
 
-// Collect the rows [g0, g0 + rg) of the rows that fold through expert e, in
+// Collect the rows [g0, g0 + cap) of the rows that fold through expert e, in
 // the order (chunk, i, warp, lane) -- the same in every CTA -- and return the
 // total number of such rows.  Block-uniform; two barriers per 2048-row chunk.
 // When have0, chunk 0's loads are passed in (already issued).
-__device__ int scan_rows(const GatherParams &p, int e, int g0, const int (&idx0)[kScanPer],
+__device__ int scan_rows(const GatherParams &p, int e, int g0, int cap, const int (&idx0)[kScanPer],
                          const int (&ra0)[kScanPer], bool have0, int *s_rows,
                          int (*s_cnt)[kWarps]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -124,7 +124,7 @@ __device__ int scan_rows(const GatherParams &p, int e, int g0, const int (&idx0)
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) mine += (w < warp) ? s_cnt[i][w] : 0;
       const int rank = mine + __popc(mask[i] & ((1u << lane) - 1u));
-      if (((mask[i] >> lane) & 1u) && rank >= g0 && rank < g0 + p.rg)
+      if (((mask[i] >> lane) & 1u) && rank >= g0 && rank < g0 + cap)
         s_rows[rank - g0] = base + i * kThreads + tid;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) run += s_cnt[i][w];
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
     }
     int idx0[kScanPer], ra0[kScanPer];
     scan_load(p, 0, idx0, ra0);
-    const int total = scan_rows(p, e, 0, idx0, ra0, true, s_rows, s_cnt);
+    const int total = scan_rows(p, e, 0, kMaxRowGroup, idx0, ra0, true, s_rows, s_cnt);
     if (total == 0) {  // an adapted expert with no folding row: let its weights land
       const bool timed_out = !bad && !mbar_wait_bounded(bar_w, ph_w);
       ph_w ^= 1u;
@@ -293,10 +293,15 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
       continue;
     }
     bool have_weights = false;
+    int list0 = 0;  // s_rows holds ranks [list0, list0 + kMaxRowGroup) of the row list
 
     for (int g0 = 0; g0 < total; g0 += p.rg, ++grp) {
-      if (g0 > 0) scan_rows(p, e, g0, idx0, ra0, false, s_rows, s_cnt);
       const int n_g = min(p.rg, total - g0);
+      if (g0 + n_g > list0 + kMaxRowGroup) {
+        scan_rows(p, e, g0, kMaxRowGroup, idx0, ra0, false, s_rows, s_cnt);
+        list0 = g0;
+      }
+      const int *rows = s_rows + (g0 - list0);
 
       // Rows of this group: x slices and base slices.
       if (warp == 0 && !bad) {
@@ -305,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
         if (lane == 0) mbar_arrive_expect_tx(bar_x, bytes);
         __syncwarp();
         if (lane < n_g) {
-          const int row = s_rows[lane];
+          const int row = rows[lane];
           const int t = row / p.top_k;
           if (ksv > 0)
             bulk_g2s(smem_addr(sX + lane * p.stride_a),
@@ -347,14 +352,17 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
         kq = warp / units;
       }
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // A warp with one unit splits its k blocks over both accumulators (two
+      // independent MMA chains), added in a fixed order afterwards.
+      const bool dual = my_units[1] < 0;
       if (!bad && my_units[0] >= 0) {
         const int kb_lo = kq * kblocks / ksplit, kb_hi = (kq + 1) * kblocks / ksplit;
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           const uint32_t kbyte = (kb * 32 + 8 * c) * 2;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            const int u = my_units[i];
-            if (u < 0) continue;
+            const int u = dual ? my_units[0] : my_units[i];
+            if (u < 0 || (dual && i != ((kb - kb_lo) & 1))) continue;
             const int mt = u % MT, nt = u / MT;
             const uint4 pa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g) * p.stride_a + kbyte);
             const uint4 qa =
@@ -364,6 +372,10 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
             mma_bf16_16816(acc[i], pa.z, qa.z, pa.w, qa.w, sx.z, sx.w);
           }
         }
+      }
+      if (dual) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[0][v] += acc[1][v];
       }
       // acc[i] = (rank mt*16+g, row nt*8+2c), (.., +1), (rank +8, row), (rank +8, row +1)
       float *dst = (ksplit == 1) ? sHloc : sP + kq * (ntr * 8 * HS);
@@ -502,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
       fence_proxy_async_smem();
       __syncthreads();
       if (warp == 0 && !bad && nsv > 0 && lane < n_g) {
-        const int row = s_rows[lane];
+        const int row = rows[lane];
         bulk_s2g(p.base_out + static_cast<size_t>(row) * p.n_out + n0,
                  smem_addr(sBase + lane * p.stride_base), nsv * 2u);
         bulk_commit();

@@ -29,9 +29,10 @@
 //    base_out is read (into registers, right after the wait) and written with
 //    16-byte accesses, rounded once: RNE(base + scale * delta).  B_e sits in
 //    shared memory with its rows XOR-permuted for conflict-free loads;
-//  * an expert with more than 8 rows gets a helper CTA (the SMs left over by
-//    the experts): owner and helper fold alternate passes of 8 rows, both
-//    deciding the split from the same per-expert row counts.
+//  * an expert with more than 6 rows gets a helper CTA (the SMs left over by
+//    the experts): the owner folds the first half of its rows, the helper the
+//    second, both deciding the split from the same per-expert row counts
+//    (the rows a CTA stores bound its time: one SM writes ~32 B per cycle).
 // Rows are folded 8 at a time; an expert with more rows runs several passes.
 #include <cuda_bf16.h>
 
@@ -51,6 +52,7 @@ constexpr int kScanPer = 2;      // rows per thread per scan chunk (small code)
 constexpr int kScanChunk = kScanPer * kThreads;
 constexpr int kSpecRows = 32;    // rows of the speculative scan kept for L2 prefetch
 constexpr int kMaxCtas = 160;    // owner + helper CTAs (and table entries) at most
+constexpr int kSplitRows = 6;    // an expert with more folding rows than this gets a helper
 
 static __device__ uint32_t g_decode_errors;
 
@@ -274,8 +276,8 @@ __device__ __forceinline__ void expand_block(float (&d)[4][4], const uint8_t *sB
 }
 
 // Which expert a helper CTA takes, or whether an owner has a helper, from the
-// per-expert counts of folding rows: an expert with more than kRows rows is
-// "heavy"; the i-th heavy expert (by id) gets helper CTA i, if there is one.
+// per-expert counts of folding rows: an expert with more than kSplitRows rows
+// is "heavy"; the i-th heavy expert (by id) gets helper CTA i, if there is one.
 // Warp 0 computes it; the result is in *s_out after the next barrier.
 __device__ __forceinline__ void assign_helper(const int *s_hist, int n_experts, int n_helpers,
                                               bool helper, int who, int *s_out) {
@@ -284,7 +286,7 @@ __device__ __forceinline__ void assign_helper(const int *s_hist, int n_experts, 
   int run = 0, found = helper ? -1 : 0;
   for (int b = 0; b < n_experts; b += 32) {
     const int e = b + lane;
-    const bool heavy = e < n_experts && s_hist[e] > kRows;
+    const bool heavy = e < n_experts && s_hist[e] > kSplitRows;
     const unsigned mask = __ballot_sync(0xffffffffu, heavy);
     const int rank = run + __popc(mask & ((1u << lane) - 1u));
     if (heavy && rank < n_helpers) {
@@ -345,11 +347,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
   bool bad = false;
 
   // Owner CTA e folds expert e; helper CTA h (blockIdx >= n_experts) folds the
-  // odd passes of the h-th heavy expert, whose owner then folds the even ones.
+  // second half of the rows of the h-th heavy expert, whose owner folds the first.
   const bool helper = static_cast<int>(blockIdx.x) >= p.n_experts;
   const int who = helper ? static_cast<int>(blockIdx.x) - p.n_experts : static_cast<int>(blockIdx.x);
   const int n_helpers = static_cast<int>(gridDim.x) - p.n_experts;
-  const int first = helper ? 1 : 0;  // first pass of this CTA
   const bool spec = p.spec_mode != 1;
   int e = helper ? -1 : who;
   int total = 0;
@@ -393,9 +394,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
                                  false, nullptr);
     }
   }
+  int spec_role = 0;  // owner: 1 if the speculative counts give it a helper
+  if (spec && !helper) {
+    assign_helper(s_hist, p.n_experts, n_helpers, false, who, &s_role);
+    __syncthreads();
+    spec_role = s_role;
+  }
   if (e >= 0) pair = request_pair(e);
-  const int spec_g0 = kRows * first;
-  int n_spec = (spec && pair) ? max(0, min(kRows, total - spec_g0)) : 0;
+  // Rows of a split expert: the owner folds ranks [0, half), the helper
+  // [half, total), half = ceil(total / 2); passes of up to 8 rows each.
+  const bool spec_split = helper || spec_role == 1;
+  const int spec_g0 = helper ? (total + 1) / 2 : 0;
+  const int spec_end = (spec_split && !helper) ? (total + 1) / 2 : total;
+  int n_spec = (spec && pair && spec_g0 < kSpecRows - kRows)
+                   ? max(0, min(kRows, spec_end - spec_g0)) : 0;
   if (warp == 1 && lane < n_spec) {
     const int row = s_spec[spec_g0 + lane];
     prefetch_l2(p.x + static_cast<size_t>(row / p.top_k) * p.k_in, row_bytes_x);
@@ -457,7 +469,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     }
   } else if (n_spec > 0) {
     // The speculative rows stand if the fresh scan agrees.
-    bool differ = tid == 0 && fresh != total;
+    // (equal totals and roles give the same first pass [spec_g0, spec_g0 + n_spec))
+    bool differ = tid == 0 && (fresh != total || (!helper && role != spec_role));
     if (tid < n_spec && s_rows[spec_g0 + tid] != s_spec[spec_g0 + tid]) differ = true;
     if (__syncthreads_or(differ)) {  // let the copies of the stale rows land first
       timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
@@ -471,17 +484,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     }
   }
   total = pair ? fresh : 0;
-  const int stride = (helper || role == 1) ? 2 : 1;  // passes of 8 rows this CTA folds
+  const bool split = helper || role == 1;
+  const int g_begin = helper ? (total + 1) / 2 : 0;
+  const int g_end = (split && !helper) ? (total + 1) / 2 : total;
   bool issued = n_spec > 0;  // the first pass's x copies and base_out loads are in flight
   int list0 = 0;             // rank of s_rows[0] in the row list
 
-  for (int g0 = kRows * first; g0 < total && !bad; g0 += kRows * stride) {
-    if (g0 >= list0 + kSpecRows) {
+  for (int g0 = g_begin; g0 < g_end && !bad; g0 += kRows) {
+    if (g0 + kRows > list0 + kSpecRows) {  // this pass's rows are past the list
       scan_expert_rows(p, e, g0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false, nullptr);
       list0 = g0;
     }
     const int *rows = s_rows + (g0 - list0);
-    const int n_g = min(kRows, total - g0);
+    const int n_g = min(kRows, g_end - g0);
     if (!issued) {
       request_x(p, warp, lane, n_g, row_bytes_x, bad, rows, sX, bar_x);
       request_base(p, warp, g, c, n_g, rows, base_v, my_row);
@@ -539,10 +554,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     // The next pass of this CTA (its rows already in s_rows): its x rows are
     // requested now that sX is free, its base_out rows as the quads of this
     // pass retire, so neither round trip is exposed.
-    const int g1 = g0 + kRows * stride;
-    const bool pre = g1 < total && g1 < list0 + kSpecRows;  // CTA-uniform
+    const int g1 = g0 + kRows;
+    const bool pre = g1 < g_end && g1 + kRows <= list0 + kSpecRows;  // CTA-uniform
     const int *rows1 = s_rows + (g1 - list0);
-    const int n_g1 = pre ? min(kRows, total - g1) : 0;
+    const int n_g1 = pre ? min(kRows, g_end - g1) : 0;
     int my_row1[2];
     my_row1[0] = 2 * c < n_g1 ? rows1[2 * c] : -1;
     my_row1[1] = 2 * c + 1 < n_g1 ? rows1[2 * c + 1] : -1;

@@ -161,12 +161,13 @@ __device__ TileInfo tile_info(const GroupedParams &p, const int *tile_start, int
   return ti;
 }
 
-// Per-CTA tile list entry, built once in the prologue: expert, rows, scale,
-// and a bitmask of the tile rows that fold.
+// Per-CTA tile list entry, built once in the prologue: expert, rows, scale.
+// Which rows fold is decided where it is needed: the X producers gather every
+// row of the tile (no round trip on the row map before the first copy), and
+// each epilogue lane reads its own rows' row-map entries once, up front.
 struct MyTile {
   int e, r0, r1;
   float scale;
-  uint32_t fold[4];
 };
 
 __device__ __forceinline__ bool cells_fold(uint64_t a, uint64_t b) {
@@ -261,9 +262,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (tid == 0) tile_start[n_e] = carry;
   }
   __syncthreads();
-  // This CTA's tiles (t = blockIdx.x + i * gridDim.x): expert, rows, scale,
-  // and which rows fold (a span row with src >= 0 whose token's row-map entry
-  // is not negative).  The epilogue reads only this list.
+  // This CTA's tiles (t = blockIdx.x + i * gridDim.x): expert, rows, scale.
   MyTile *my_tiles = reinterpret_cast<MyTile *>(smem + p.off_my);
   const int n_tiles_all = tile_start[n_e];
   int my_count = 0;
@@ -277,18 +276,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
     my_tiles[tid].scale = __ldg(p.scale_table + ti.e);
   }
   __syncthreads();
-  // Fold bitmasks, one warp per 32 rows.
-  for (int i = warp; i < my_count * 4; i += kGThreads / 32) {
-    const MyTile mt = my_tiles[i >> 2];
-    const int r = mt.r0 + (i & 3) * 32 + lane;
-    bool f = false;
-    if (r < mt.r1) {
-      const int sr = p.src ? __ldg(p.src + r) : r;
-      f = sr >= 0 && (p.row_adapter == nullptr || __ldg(p.row_adapter + sr / p.top_k) >= 0);
-    }
-    const uint32_t m = __ballot_sync(0xffffffffu, f);
-    if (lane == 0) my_tiles[i >> 2].fold[i & 3] = m;
-  }
   if (warp == 0) {
     tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
     tmem_relinquish();
@@ -388,9 +375,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (t >= n_tiles) continue;
         const MyTile mt = my_tiles[t];
         const int row = half * 64 + lane + 32 * u;
-        if ((mt.fold[row >> 5] >> (row & 31)) & 1u) {
-          const int r = mt.r0 + row;
-          tok[u] = (p.src ? __ldg(p.src + r) : r) / p.top_k;
+        const int r = mt.r0 + row;
+        if (r < mt.r1) {
+          const int sr = p.src ? __ldg(p.src + r) : r;
+          tok[u] = sr >= 0 ? sr / p.top_k : -1;
         }
       }
     };
@@ -545,12 +533,34 @@ __global__ void __launch_bounds__(kGThreads, 1)
     ld_advance(true);
     if (lane == 0)
       for (int i = 0; i < p.depth - 1; ++i) ld_issue();
+    // Which of this lane's rows fold, one bit per tile of this CTA: a row of
+    // the tile whose src is valid and whose token's row-map entry is not
+    // negative.  Loads of all tiles issued together (two round trips in all).
+    uint32_t fold_bits = 0;
+    {
+      int sr[kMyTilesMax];
+#pragma unroll
+      for (int t = 0; t < kMyTilesMax; ++t) {
+        sr[t] = -1;
+        if (t < n_tiles) {
+          const MyTile mt = my_tiles[t];
+          const int r = mt.r0 + quarter * kBoxRows + lane;
+          if (r < mt.r1) sr[t] = p.src ? __ldg(p.src + r) : r;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kMyTilesMax; ++t) {
+        const bool f = sr[t] >= 0 && (p.row_adapter == nullptr ||
+                                      __ldg(p.row_adapter + sr[t] / p.top_k) >= 0);
+        fold_bits |= f ? (1u << t) : 0u;
+      }
+    }
 
     for (int t = 0; t < n_tiles; ++t, ++tile_it) {
       const MyTile ti = my_tiles[t];
       const int row = quarter * kBoxRows + lane;
       const int rg = ti.r0 + row;
-      const bool folds = (ti.fold[row >> 5] >> (row & 31)) & 1u;
+      const bool folds = (fold_bits >> t) & 1u;
       const float scale = ti.scale;
       const int owned = min(max(ti.r1 - (ti.r0 + quarter * kBoxRows), 0), kBoxRows);
 

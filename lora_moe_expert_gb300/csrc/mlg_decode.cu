@@ -586,10 +586,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       uint32_t hh[WPL], hl[WPL];
       load_words<WPL>(hh, sHhi + (g * RP + c * WPL * 2) * 2);
       load_words<WPL>(hl, sHlo + (g * RP + c * WPL * 2) * 2);
-      // One loop body for all blocks (small code: the instruction cache is
-      // cold in a CTA that runs once); base_v[0] is always the current block,
-      // the registers rotate down and the next pass's loads enter at the top.
-#pragma unroll 1
+      // base_v[0] is always the current block: the registers rotate down and
+      // the next pass's loads enter at the top.
+#pragma unroll
       for (int i = 0; i < kMaxBlocks; ++i) {
         const int blk = warp + i * kWarps;
         uint4 nv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};

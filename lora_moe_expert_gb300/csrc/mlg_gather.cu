@@ -93,10 +93,11 @@ __device__ __forceinline__ void scan_load(const GatherParams &p, int base, int (
 // Collect the rows [g0, g0 + cap) of the rows that fold through expert e, in
 // the order (chunk, i, warp, lane) -- the same in every CTA -- and return the
 // total number of such rows.  Block-uniform; two barriers per 2048-row chunk.
-// When have0, chunk 0's loads are passed in (already issued).
+// When have0, chunk 0's loads are passed in (already issued).  With s_hist,
+// every folding row is also counted for its expert (e = -1 only counts).
 __device__ int scan_rows(const GatherParams &p, int e, int g0, int cap, const int (&idx0)[kScanPer],
                          const int (&ra0)[kScanPer], bool have0, int *s_rows,
-                         int (*s_cnt)[kWarps]) {
+                         int (*s_cnt)[kWarps], int *s_hist = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int count = 0;
   for (int base = 0; base < p.n_slots; base += kScanChunk) {
@@ -110,10 +111,15 @@ __device__ int scan_rows(const GatherParams &p, int e, int g0, int cap, const in
     } else {
       scan_load(p, base, idx, ra);
     }
+    if (s_hist != nullptr) {  // folding rows per expert (ids in the table only)
+#pragma unroll
+      for (int i = 0; i < kScanPer; ++i)
+        if (ra[i] >= 0 && idx[i] >= 0 && idx[i] < p.n_experts) atomicAdd(&s_hist[idx[i]], 1);
+    }
     unsigned mask[kScanPer];
 #pragma unroll
     for (int i = 0; i < kScanPer; ++i) {
-      mask[i] = __ballot_sync(0xffffffffu, idx[i] == e && ra[i] >= 0);
+      mask[i] = __ballot_sync(0xffffffffu, e >= 0 && idx[i] == e && ra[i] >= 0);
       if (lane == 0) s_cnt[i][warp] = __popc(mask[i]);
     }
     __syncthreads();
@@ -133,6 +139,31 @@ __device__ int scan_rows(const GatherParams &p, int e, int g0, int cap, const in
     __syncthreads();
   }
   return count;
+}
+
+// Experts with more folding rows than one pass takes (rg) are "heavy"; the
+// i-th heavy expert by id gets the i-th helper cluster, if there is one.
+// who >= 0: the expert helper `who` takes (-1 if none); who < 0: whether
+// expert -1 - who has a helper (1 / 0).  Warp 0 computes, *s_out holds the
+// result after the next barrier.
+__device__ void heavy_assign(const int *s_hist, int n_experts, int rg, int n_helpers, int who,
+                             int *s_out) {
+  const int lane = threadIdx.x & 31;
+  if ((threadIdx.x >> 5) != 0) return;
+  int run = 0, found = who >= 0 ? -1 : 0;
+  for (int b = 0; b < n_experts; b += 32) {
+    const int ex = b + lane;
+    const bool heavy = ex < n_experts && s_hist[ex] > rg;
+    const unsigned m = __ballot_sync(0xffffffffu, heavy);
+    const int rank = run + __popc(m & ((1u << lane) - 1u));
+    if (heavy && rank < n_helpers) {
+      if (who >= 0 && rank == who) found = ex;
+      if (who < 0 && ex == -1 - who) found = 1;
+    }
+    run += __popc(m);
+  }
+  const int v = __reduce_max_sync(0xffffffffu, found);
+  if (lane == 0) *s_out = v;
 }
 
 // B_e fragments of one 16-row m-tile for the swapped expand (A operand of
@@ -241,9 +272,31 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
     }
   }
   const int n_units = n_fold * p.ns2;
-  for (int unit = static_cast<int>(cluster_id_x()); unit < n_units;
-       unit += static_cast<int>(ncluster_x())) {
-    const int e = compact ? s_ex[unit / p.ns2] : unit / p.ns2;
+  // Clusters left over once every unit has one become helpers: the i-th takes
+  // the second half of the rows of the i-th heavy expert (its owner folds the
+  // first half), so no cluster runs a second pass while others idle.  Both
+  // sides decide from the same per-expert row counts, read after the wait.
+  const int ncl = static_cast<int>(ncluster_x());
+  const int n_helpers = (compact && p.ns2 == 1 && n_units < ncl) ? ncl - n_units : 0;
+  int *s_hist = reinterpret_cast<int *>(smem + p.off_p);  // counts; free until a shrink
+  const int no_idx[kScanPer] = {};
+  for (int unit = static_cast<int>(cluster_id_x()); unit < n_units + n_helpers; unit += ncl) {
+    const bool help = unit >= n_units;
+    int e = help ? -1 : (compact ? s_ex[unit / p.ns2] : unit / p.ns2);
+    if (help) {
+      if (!waited) {
+        griddep_wait();
+        waited = true;
+      }
+      for (int i = tid; i < p.n_experts; i += kThreads) s_hist[i] = 0;
+      __syncthreads();
+      scan_rows(p, -1, 0, 0, no_idx, no_idx, false, s_rows, s_cnt, s_hist);
+      heavy_assign(s_hist, p.n_experts, p.rg, n_helpers, unit - n_units, &s_cnt[0][0]);
+      __syncthreads();
+      e = s_cnt[0][0];
+      __syncthreads();  // s_cnt is rewritten by the next scan
+      if (e < 0) continue;
+    }
     const int ni = (unit % p.ns2) * static_cast<int>(cs) + static_cast<int>(q);  // n slice
     const int n0 = ni * p.ns;
     const int nsv = max(0, min(p.ns, p.n_out - n0));
@@ -280,10 +333,26 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
       griddep_wait();
       waited = true;
     }
+    const bool count = n_helpers > 0 && !help;  // an owner also counts every expert's rows
+    if (count) {
+      for (int i = tid; i < p.n_experts; i += kThreads) s_hist[i] = 0;
+      __syncthreads();
+    }
     int idx0[kScanPer], ra0[kScanPer];
     scan_load(p, 0, idx0, ra0);
-    const int total = scan_rows(p, e, 0, kMaxRowGroup, idx0, ra0, true, s_rows, s_cnt);
-    if (total == 0) {  // an adapted expert with no folding row: let its weights land
+    const int total = scan_rows(p, e, 0, kMaxRowGroup, idx0, ra0, true, s_rows, s_cnt,
+                                count ? s_hist : nullptr);
+    // Rows of this unit: [0, total), or a half of them when the expert is split.
+    int lo = 0, hi = total;
+    if (help) {
+      lo = (total + 1) / 2;
+    } else if (count) {
+      heavy_assign(s_hist, p.n_experts, p.rg, n_helpers, -1 - e, &s_cnt[0][0]);
+      __syncthreads();
+      if (s_cnt[0][0] == 1) hi = (total + 1) / 2;
+      __syncthreads();
+    }
+    if (hi <= lo) {  // an adapted expert with no folding row here: let its weights land
       const bool timed_out = !bad && !mbar_wait_bounded(bar_w, ph_w);
       ph_w ^= 1u;
       if (__syncthreads_or(timed_out)) {
@@ -295,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
     bool have_weights = false;
     int list0 = 0;  // s_rows holds ranks [list0, list0 + kMaxRowGroup) of the row list
 
-    for (int g0 = 0; g0 < total; g0 += p.rg, ++grp) {
-      const int n_g = min(p.rg, total - g0);
+    for (int g0 = lo; g0 < hi; g0 += p.rg, ++grp) {
+      const int n_g = min(p.rg, hi - g0);
       if (g0 + n_g > list0 + kMaxRowGroup) {
         scan_rows(p, e, g0, kMaxRowGroup, idx0, ra0, false, s_rows, s_cnt);
         list0 = g0;

@@ -69,7 +69,7 @@ def _check_exact(w, run):
 
 @pytest.mark.parametrize("path", [0, 1, 2])
 @pytest.mark.parametrize("shape", [(64, 8, 128, 256, 512, 16), (40, 4, 24, 192, 264, 32),
-                                   (24, 4, 8, 128, 96, 64)],
+                                   (24, 4, 8, 128, 96, 64), (64, 4, 8, 128, 96, 64)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_gather_exact(shape, path):
     T, K, E, k_in, n_out, r = shape

@@ -68,6 +68,7 @@ SHAPES = [
     (20, 6, 40, 4104, 48, 64, 0.6, 0.1, 3, 2),
     (9, 1, 4, 2048, 8200, 32, 1.0, 0.0, 0, 0),
     (1, 1, 1, 64, 64, 8, 1.0, 0.0, 0, 0),
+    (64, 4, 8, 512, 256, 64, 1.0, 0.1, 0, 0),  # ~30 rows per expert: helper clusters
 ]
 
 

@@ -426,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
       const bool dual = my_units[1] < 0;
       if (!bad && my_units[0] >= 0) {
         const int kb_lo = kq * kblocks / ksplit, kb_hi = (kq + 1) * kblocks / ksplit;
+#pragma unroll 4
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           const uint32_t kbyte = (kb * 32 + 8 * c) * 2;
 #pragma unroll

@@ -273,6 +273,40 @@ int32_t oracle_grouped_fold(const uint16_t *x, const int32_t *expert_offsets, co
     return OR_OK;
 }
 
+/* Per-row x variant of the grouped fold.  [P2] moe_lora_grouped_down leaves
+ * the x row of a sorted row undefined; the token reading above takes
+ * x[src[r] / top_k].  In a real down projection the input is the expert's
+ * intermediate activation, one row per sorted row, so this variant takes
+ * x_rows[r] ([total_rows, k_in]) for sorted row r.  Everything else -- spans,
+ * window, zero cells, the row map read through src[r] / top_k -- is the
+ * grouped fold's. */
+int32_t oracle_grouped_fold_xrows(const uint16_t *x_rows, const int32_t *expert_offsets,
+                                  const int32_t *src, const int32_t *row_adapter,
+                                  const uint64_t *a_table, const uint64_t *b_table,
+                                  const float *scale_table, const uint16_t *base_in,
+                                  double *ref_out, uint8_t *folded, int64_t total_rows,
+                                  int32_t k_in, int32_t max_rank, int32_t n_out, int32_t top_k,
+                                  int32_t n_experts, int32_t row_offset, int32_t row_end) {
+    if (max_rank > 1024 || top_k < 1) return OR_NONE;
+    for (int64_t r = 0; r < total_rows; ++r) {
+        copy_row(base_in + r * n_out, ref_out + r * n_out, n_out);
+        folded[r] = 0;
+    }
+    for (int32_t e = 0; e < n_experts; ++e) {
+        int64_t lo = expert_offsets[e] > row_offset ? expert_offsets[e] : row_offset;
+        int64_t hi = expert_offsets[e + 1] < row_end ? expert_offsets[e + 1] : row_end;
+        if (!expert_folds(e, n_experts, a_table, b_table)) continue;
+        for (int64_t r = lo; r < hi; ++r) {
+            if (row_adapter != NULL && row_adapter[src[r] / top_k] < 0) continue;
+            fold_one_row(x_rows + r * k_in, (const uint16_t *)(uintptr_t)a_table[e],
+                         (const uint16_t *)(uintptr_t)b_table[e], (double)scale_table[e],
+                         base_in + r * n_out, ref_out + r * n_out, k_in, max_rank, n_out);
+            folded[r] = 1;
+        }
+    }
+    return OR_OK;
+}
+
 /* [P2] MoeExpertRoute: the router fold is a one-entry route whose expert 0 is
  * the router pair, so every token t folds x[t] through entry 0 (top_k = 1,
  * identity rows).  A row map, when given, skips tokens with a negative entry. */

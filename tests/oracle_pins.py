@@ -324,6 +324,39 @@ def pin_sampled_rows_match_full(o):
     assert np.array_equal(ref_s, ref[rows]) and np.array_equal(fold_s, fold[rows])
 
 
+def pin_xrows_forms(o):
+    """The per-row x grouped fold (sorted row r reads x_rows[r]) equals the
+    token form when x_rows[r] is the row's token, and equals a top_k = 1 gather
+    fold over the sorted rows (row r as its own token, its span's expert as its
+    id, its token's row-map entry as its entry) for arbitrary x_rows."""
+    w = synth.custom_grouped(14, [11, 23, 6], top_k=3, n_experts=10, k_in=40, n_out=32,
+                             max_rank=8, cap=19, adapted_frac=0.7, stream_base=[0, 1, 0])
+    he = HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
+    at, bt, st = he.tables(o)
+    n_exp = at.size
+    ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+    R = w.rows
+    tok_rows = w.x[w.src // w.top_k]
+    for s, e in [(0, R), (5, 40), (R - 3, R)]:
+        ref_t, fold_t = o.grouped_fold(w.x, w.expert_offsets, w.src, ra, at, bt, st, w.base,
+                                       w.k_in, w.max_rank, w.n_out, w.top_k, s, e)
+        ref_x, fold_x = o.grouped_fold_xrows(tok_rows, w.expert_offsets, w.src, ra, at, bt, st,
+                                             w.base, w.k_in, w.max_rank, w.n_out, w.top_k, s, e)
+        assert np.array_equal(fold_x, fold_t) and np.array_equal(ref_x, ref_t)
+    rng = np.random.default_rng(3)
+    x_rows = _bits(rng.standard_normal((R, w.k_in)))
+    ids = np.full(R, n_exp + 7, np.int32)
+    for e in range(n_exp):
+        ids[w.expert_offsets[e]:w.expert_offsets[e + 1]] = e
+    ra_rows = ra[w.src // w.top_k]
+    ref_g, fold_g = o.gather_fold(x_rows, ids, ra_rows, at, bt, st, w.base, w.k_in, w.max_rank,
+                                  w.n_out, 1)
+    ref_x, fold_x = o.grouped_fold_xrows(x_rows, w.expert_offsets, w.src, ra, at, bt, st,
+                                         w.base, w.k_in, w.max_rank, w.n_out, w.top_k, 0, R)
+    assert fold_x.any() and (~fold_x).any()
+    assert np.array_equal(fold_x, fold_g) and np.array_equal(ref_x, ref_g)
+
+
 ALL_PINS = [
     pin_route_truth_table,
     pin_decode_maps,
@@ -341,4 +374,5 @@ ALL_PINS = [
     pin_window_split,
     pin_router_is_one_entry_route,
     pin_sampled_rows_match_full,
+    pin_xrows_forms,
 ]

@@ -41,6 +41,9 @@ MUTANTS = {
                              "for (int64_t i = n - 1; i >= 0; --i) { /* in input order"),
     "window not clipped": ("if (end > total_rows) end = total_rows;", ";"),
     "wc not at least 1": ("return wc < 1 ? 1u : (uint32_t)wc;", "return (uint32_t)wc;"),
+    "x_rows read by token": ("fold_one_row(x_rows + r * k_in", "fold_one_row(x_rows + (int64_t)(src[r] / top_k) * k_in"),
+    "x_rows row map by sorted row": ("row_adapter[src[r] / top_k] < 0) continue;\n            fold_one_row(x_rows",
+                                     "row_adapter[r / top_k] < 0) continue;\n            fold_one_row(x_rows"),
     "padding gets active": ("        } else {\n            out[i] = -1;\n        }",
                             "        } else {\n            out[i] = active;\n        }"),
 }

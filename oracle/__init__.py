@@ -90,6 +90,8 @@ class Oracle:
         L.oracle_grouped_fold.restype = _i32
         L.oracle_grouped_fold_xrows.argtypes = [_p] * 10 + [_i64] + [_i32] * 7
         L.oracle_grouped_fold_xrows.restype = _i32
+        L.oracle_grouped_fold_xrows_rows.argtypes = [_p] * 9 + [_i32, _p, _p] + [_i32] * 7
+        L.oracle_grouped_fold_xrows_rows.restype = _i32
         L.oracle_router_fold.argtypes = [_p] * 8 + [_i32] * 4
         L.oracle_router_fold.restype = _i32
         L.oracle_gather_fold_rows.argtypes = [_p] * 8 + [_i32, _p, _p] + [_i32] * 5
@@ -273,6 +275,27 @@ class Oracle:
                                                rows.size, _ptr(ref), _ptr(folded), k_in,
                                                max_rank, n_out, top_k, at.size, row_offset,
                                                row_end)
+        assert st == OK, st
+        return ref, folded.astype(bool)
+
+    def grouped_fold_xrows_rows(self, x_rows, expert_offsets, src, row_adapter, a_table,
+                                b_table, scale_table, base_rows, rows, k_in, max_rank, n_out,
+                                top_k, row_offset, row_end):
+        """Fold only the sorted `rows` of the per-row x form."""
+        x, base_rows = self._u16(x_rows), self._u16(base_rows)
+        off = np.ascontiguousarray(expert_offsets, np.int32)
+        src = np.ascontiguousarray(src, np.int32)
+        ra = None if row_adapter is None else np.ascontiguousarray(row_adapter, np.int32)
+        rows = np.ascontiguousarray(rows, np.int32)
+        at, bt = np.ascontiguousarray(a_table, np.uint64), np.ascontiguousarray(b_table, np.uint64)
+        st_ = np.ascontiguousarray(scale_table, np.float32)
+        ref = np.empty((rows.size, n_out), np.float64)
+        folded = np.empty(rows.size, np.uint8)
+        st = self.lib.oracle_grouped_fold_xrows_rows(_ptr(x), _ptr(off), _ptr(src), _ptr(ra),
+                                                     _ptr(at), _ptr(bt), _ptr(st_),
+                                                     _ptr(base_rows), _ptr(rows), rows.size,
+                                                     _ptr(ref), _ptr(folded), k_in, max_rank,
+                                                     n_out, top_k, at.size, row_offset, row_end)
         assert st == OK, st
         return ref, folded.astype(bool)
 

@@ -396,3 +396,38 @@ int32_t oracle_grouped_fold_rows(const uint16_t *x, const int32_t *expert_offset
     }
     return OR_OK;
 }
+
+/* Sampled variant of the per-row x grouped fold: the listed sorted rows only,
+ * row r reading x_rows[r]. */
+int32_t oracle_grouped_fold_xrows_rows(const uint16_t *x_rows, const int32_t *expert_offsets,
+                                       const int32_t *src, const int32_t *row_adapter,
+                                       const uint64_t *a_table, const uint64_t *b_table,
+                                       const float *scale_table, const uint16_t *base_rows,
+                                       const int32_t *rows, int32_t n_rows, double *ref_out,
+                                       uint8_t *folded, int32_t k_in, int32_t max_rank,
+                                       int32_t n_out, int32_t top_k, int32_t n_experts,
+                                       int32_t row_offset, int32_t row_end) {
+    if (max_rank > 1024 || top_k < 1) return OR_NONE;
+    for (int32_t i = 0; i < n_rows; ++i) {
+        int32_t r = rows[i];
+        const uint16_t *base_row = base_rows + (int64_t)i * n_out;
+        double *ref_row = ref_out + (int64_t)i * n_out;
+        folded[i] = 0;
+        copy_row(base_row, ref_row, n_out);
+        if (r < row_offset || r >= row_end) continue;
+        int32_t owner = -1;
+        for (int32_t e = 0; e < n_experts; ++e) {
+            if (expert_offsets[e] <= r && r < expert_offsets[e + 1]) {
+                owner = e;
+                break;
+            }
+        }
+        if (owner < 0 || !expert_folds(owner, n_experts, a_table, b_table)) continue;
+        if (row_adapter != NULL && row_adapter[src[r] / top_k] < 0) continue;
+        fold_one_row(x_rows + (int64_t)r * k_in, (const uint16_t *)(uintptr_t)a_table[owner],
+                     (const uint16_t *)(uintptr_t)b_table[owner], (double)scale_table[owner],
+                     base_row, ref_row, k_in, max_rank, n_out);
+        folded[i] = 1;
+    }
+    return OR_OK;
+}

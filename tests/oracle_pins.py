@@ -355,6 +355,14 @@ def pin_xrows_forms(o):
                                          w.base, w.k_in, w.max_rank, w.n_out, w.top_k, 0, R)
     assert fold_x.any() and (~fold_x).any()
     assert np.array_equal(fold_x, fold_g) and np.array_equal(ref_x, ref_g)
+    # the row-sampled entry point equals the corresponding rows of a windowed fold
+    ref_w, fold_w = o.grouped_fold_xrows(x_rows, w.expert_offsets, w.src, ra, at, bt, st,
+                                         w.base, w.k_in, w.max_rank, w.n_out, w.top_k, 4, R - 6)
+    rows = np.array([0, 3, 4, R - 7, R - 6, 17, R - 1, 30], np.int32)
+    ref_s, fold_s = o.grouped_fold_xrows_rows(x_rows, w.expert_offsets, w.src, ra, at, bt, st,
+                                              w.base[rows], rows, w.k_in, w.max_rank, w.n_out,
+                                              w.top_k, 4, R - 6)
+    assert np.array_equal(ref_s, ref_w[rows]) and np.array_equal(fold_s, fold_w[rows])
 
 
 ALL_PINS = [

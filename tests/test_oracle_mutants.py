@@ -44,6 +44,8 @@ MUTANTS = {
     "x_rows read by token": ("fold_one_row(x_rows + r * k_in", "fold_one_row(x_rows + (int64_t)(src[r] / top_k) * k_in"),
     "x_rows row map by sorted row": ("row_adapter[src[r] / top_k] < 0) continue;\n            fold_one_row(x_rows",
                                      "row_adapter[r / top_k] < 0) continue;\n            fold_one_row(x_rows"),
+    "sampled x_rows by token": ("fold_one_row(x_rows + (int64_t)r * k_in",
+                                "fold_one_row(x_rows + (int64_t)(src[r] / top_k) * k_in"),
     "padding gets active": ("        } else {\n            out[i] = -1;\n        }",
                             "        } else {\n            out[i] = active;\n        }"),
 }

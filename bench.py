@@ -54,6 +54,8 @@ WORKLOADS = {
                       "experts adapted, rank 64, k_in 2048, n_out 768; 154 active / 64 base / 38 pad",
     "prefill_down": "prefill grouped fold, down-proj: 8 streams U[256,768] tokens x top-8, 128 "
                     "experts, rank 16, k_in 768, n_out 2048, skewed routing, windows of 8192 rows",
+    "prefill_down_xrows": "prefill grouped fold, down-proj, per-row input (x_rows [rows, 768], one "
+                          "row per sorted row): prefill_down's routing, experts and windows",
     "prefill_large": "large prefill grouped fold: 16384 tokens x top-10 (163840 rows), 512 experts, "
                      "rank 32, k_in 512, n_out 2048, skewed routing, windows of 32768 rows",
     "router": "router fold (one-entry route): 16384 tokens, k_in 2048, n_out 512, rank 32",
@@ -99,7 +101,8 @@ def recorded_traffic(kernel_src, workload):
 
 def algorithmic(w, row_map, tables):
     """(rows, folded_rows, bytes, flops) of one step: the bytes the method must
-    move -- x rows of tokens with a folding row, A_e + B_e of each expert hit,
+    move -- x rows of tokens with a folding row (of folding rows, for per-row
+    x), A_e + B_e of each expert hit,
     the base_out read + write of each folding row, and the index arrays."""
     a, b, _ = tables
     E = a.size
@@ -128,7 +131,8 @@ def algorithmic(w, row_map, tables):
     idx_bytes = rows * 4 + (row_map.size * 4 if row_map is not None else 0) + E * 20
     if w.kind == "grouped":
         idx_bytes += (w.n_experts_model + 1) * 4
-    nbytes = tokens * k * 2 + experts * r * (k + n) * 2 + folded * n * 4 + idx_bytes
+    n_x = folded if w.x_rows is not None else tokens  # per-row x: one x row per folding row
+    nbytes = n_x * k * 2 + experts * r * (k + n) * 2 + folded * n * 4 + idx_bytes
     flops = 2 * folded * r * (k + n)
     return rows, folded, int(nbytes), int(flops)
 
@@ -213,6 +217,10 @@ def time_oracle(w, budget_s=10.0):
                                                     w.has_moe_lora)
                 o.gather_fold(w.x, w.indices, ra, at, bt, st, w.base, w.k_in, w.max_rank,
                               w.n_out, w.top_k)
+            elif w.kind == "grouped" and w.x_rows is not None:
+                ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+                o.grouped_fold_xrows(w.x_rows, w.expert_offsets, w.src, ra, at, bt, st, w.base,
+                                     w.k_in, w.max_rank, w.n_out, w.top_k, 0, w.rows)
             elif w.kind == "grouped":
                 ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
                 for s, e in o.grouped_down_windows(w.rows, w.cap):
@@ -227,7 +235,12 @@ def time_oracle(w, budget_s=10.0):
     chunk = 64
     while time.perf_counter() - t0 < budget_s:
         rows = np.sort(rng.choice(w.rows, size=chunk, replace=False)).astype(np.int32)
-        if w.kind == "grouped":
+        if w.kind == "grouped" and w.x_rows is not None:
+            ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+            o.grouped_fold_xrows_rows(w.x_rows, w.expert_offsets, w.src, ra, at, bt, st,
+                                      w.base[rows], rows, w.k_in, w.max_rank, w.n_out, w.top_k,
+                                      0, w.rows)
+        elif w.kind == "grouped":
             ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
             o.grouped_fold_rows(w.x, w.expert_offsets, w.src, ra, at, bt, st, w.base[rows], rows,
                                 w.k_in, w.max_rank, w.n_out, w.top_k, 0, w.rows)
@@ -254,7 +267,8 @@ def n_sets_for(w_bytes):
 # cluster kernel).
 KERNEL_OF = {"decode_down": "mlg_decode.cu", "decode_gate_up": "mlg_gather.cu",
              "tiny_decode": "mlg_gather.cu", "prefill_down": "mlg_grouped.cu",
-             "prefill_large": "mlg_grouped.cu", "router": "mlg_grouped.cu"}
+             "prefill_large": "mlg_grouped.cu", "router": "mlg_grouped.cu",
+             "prefill_down_xrows": "mlg_grouped.cu"}
 
 
 def kernel_source(workload):
@@ -271,10 +285,15 @@ def gpu_measure(name, steps, warmup, device, seed_base=1000, e2e=True):
     gen = synth.NAMED[name]
     w0 = gen()
     p0 = FoldProblem(w0, device=device)
-    rows, folded, nbytes, flops = algorithmic(w0, p0.row_map_host, p0.tables_host)
-    ws_bytes = w0.x.nbytes + w0.base.nbytes + sum(e.A.nbytes + e.B.nbytes for e in w0.experts)
+    ws_bytes = (w0.x.nbytes + w0.base.nbytes + sum(e.A.nbytes + e.B.nbytes for e in w0.experts)
+                + (w0.x_rows.nbytes if w0.x_rows is not None else 0))
     nsets = n_sets_for(ws_bytes)
     probs = [p0] + [FoldProblem(gen(seed=seed_base + i), device=device) for i in range(1, nsets)]
+    # The input sets may differ in size (prefill lengths are drawn per seed):
+    # the per-step figures are the mean over the steps the timed graph runs.
+    alg = np.array([algorithmic(probs[i % nsets].w, probs[i % nsets].row_map_host,
+                                probs[i % nsets].tables_host) for i in range(steps)], np.float64)
+    rows, folded, nbytes, flops = alg.mean(axis=0)
     launches_per_step = 1  # the grouped form folds all windows in one launch
 
     stream = torch.cuda.Stream(device=device)
@@ -314,6 +333,7 @@ def gpu_measure(name, steps, warmup, device, seed_base=1000, e2e=True):
     if mlg.mlg_read_device_errors(clear=True) or errors_before:
         raise RuntimeError("device error bits were set during the benchmark")
     out = {"rows": rows, "folded_rows": folded, "alg_bytes": nbytes, "alg_flops": flops,
+           "rows_set0": w0.rows,
            "ms_total": ms_total, "launches_per_step": launches_per_step, "sets": nsets,
            "set_bytes": ws_bytes, "clocks": clocks.summary(), "kind": w0.kind}
     if e2e:
@@ -331,7 +351,9 @@ def e2e_measure(prob, steps, device):
 
     w = prob.w
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    h_x = pin(w.x.view(np.int16))
+    xrows = w.x_rows is not None
+    h_x = pin((w.x_rows if xrows else w.x).view(np.int16))
+    d_x = prob.x_rows if xrows else prob.x
     h_base = pin(w.base.view(np.int16))
     h_out = torch.empty_like(h_base).pin_memory()
     h_idx = pin(w.indices) if w.kind == "gather" else None
@@ -359,7 +381,7 @@ def e2e_measure(prob, steps, device):
             if m is not None:
                 mlg.mlg_upload_row_adapter(m, prob.row_adapter, stream=s)
                 h2d += m.nbytes
-            prob.x.view(torch.int16).copy_(h_x, non_blocking=True)
+            d_x.view(torch.int16).copy_(h_x, non_blocking=True)
             prob.base.view(torch.int16).copy_(h_base, non_blocking=True)
             h2d += h_x.numel() * 2 + h_base.numel() * 2
             if h_idx is not None:
@@ -474,7 +496,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode_down", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--extra", default="decode_gate_up,prefill_down,prefill_large,router",
+    ap.add_argument("--extra", default="decode_gate_up,prefill_down,prefill_down_xrows,prefill_large,router",
                     help="other workloads measured in the same run (comma list, or 'none')")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=10.0)
@@ -554,17 +576,18 @@ def main():
         "data": "synthetic",
         "config": {"workload": args.workload, "description": WORKLOADS[args.workload],
                    "rows_per_step": main_res["rows"], "folded_rows_per_step": main_res["folded_rows"],
+                   "rows_note": "mean over the timed steps' input sets",
                    "l2": f"inputs rotate over {main_res['sets']} sets of "
                          f"{main_res['set_bytes'] / 2**20:.1f} MiB (> L2 in total)",
                    "timing": "CUDA events around one CUDA-graph replay of the timed steps",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                     "alg_bytes_per_launch": main_res["alg_bytes"] // main_res["launches_per_step"],
+                     "alg_bytes_per_launch": int(main_res["alg_bytes"] / main_res["launches_per_step"]),
                      "traffic": recorded_traffic(kernel_source(args.workload), args.workload)},
         "tflops": main_res["alg_flops"] / (ms_step * 1e-3) / 1e12,
         "cpu_baseline": cpu,
-        "e2e": {"value": job_rows_per_s(main_res["rows"], ws, e2e["s_per_step"] * 1e3),
+        "e2e": {"value": job_rows_per_s(main_res["rows_set0"], ws, e2e["s_per_step"] * 1e3),
                 "unit": "rows/s",
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},

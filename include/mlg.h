@@ -166,6 +166,31 @@ MLG_API mlg_status mlg_grouped_down_all_windows(const mlg_bf16 *x, const int32_t
                                                 int32_t top_k, int32_t n_experts,
                                                 int32_t total_rows, uint32_t cap, void *stream);
 
+/* Per-row x form of moe_lora_grouped_down (moe_lora_grouped module index).
+ * The page leaves open which x row a sorted row reads; in a down projection
+ * the input is the expert's own intermediate row, one per sorted row, so here
+ * sorted row r reads x_rows[r]:
+ *     base_out[r] += scale_e * (x_rows[r] @ A_e^T) @ B_e^T
+ * for r in [row_offset, row_end) held by span e < n_experts.  src serves the
+ * row map only: a row whose token src[r] / top_k has a negative row_adapter
+ * entry, or whose src[r] is negative, keeps its input, as do rows outside the
+ * range or outside every span.  The range is folded in windows of cap rows
+ * (starting at row_offset) in ONE launch; the result does not depend on cap.
+ *
+ *   x_rows         device, [>= row_end, k_in] bf16, indexed by sorted row,
+ *                  16-byte aligned; read only
+ *   expert_offsets, src, row_adapter, tables, base_out
+ *                  as for mlg_grouped_down (src must be non-NULL)
+ *   cap            window length in rows, >= 1
+ * Errors as for mlg_grouped_down, plus CAP_ZERO for cap == 0. */
+MLG_API mlg_status mlg_grouped_down_xrows(const mlg_bf16 *x_rows, const int32_t *expert_offsets,
+                                          const int32_t *src, const int32_t *row_adapter,
+                                          const uint64_t *a_table, const uint64_t *b_table,
+                                          const float *scale_table, mlg_bf16 *base_out,
+                                          int32_t k_in, int32_t max_rank, int32_t n_out,
+                                          int32_t top_k, int32_t n_experts, int32_t row_offset,
+                                          int32_t row_end, uint32_t cap, void *stream);
+
 /* The router fold (MoeExpertRoute, moe_lora_grouped module index): a one-entry
  * route whose expert 0 is the router pair, so every token t folds
  * base_out[t] += scale_0 * (x[t] @ A_0^T) @ B_0^T.  The tables have one entry;

@@ -5,6 +5,9 @@
 // For every expert-sorted row r of the window [row_offset, row_end) held by
 // expert e's span expert_offsets[e] .. expert_offsets[e+1]:
 //     base_out[r] += scale_e * (x[src[r] / top_k] @ A_e^T) @ B_e^T.
+// The per-row x variant reads x_rows[r] instead of x[src[r] / top_k] (the
+// down projection's input is the expert's own intermediate row); src then
+// serves the row map only.
 //
 // GB300 design (not the pages' MLG_M_TILE grid):
 //  * tiles are expert-aligned runs of <= 128 sorted rows (one tcgen05 M), so
@@ -16,11 +19,13 @@
 //    ACC = [H_hi | H_lo] [B_e | B_e]^T (M=128, N=64/128 columns per chunk) into
 //    a double-buffered TMEM accumulator -- h is split into two bf16 halves so
 //    it enters the expand at ~2^-17 relative precision (kept fp32 in effect);
-//  * warp 1 gathers the X rows (via src) and A_e chunks, warp 2 the B_e
-//    chunks, with 16-byte cp.async into 128-byte-swizzled K-major tiles;
-//  * warps 4-7 (one TMEM lane quarter each) scale and split h, then stream
-//    base_out: each warp owns 32 rows of the tile and runs its own ring of
-//    32x64 TMA boxes (prefetch depth D-1), adds the accumulator, rounds once
+//  * warps 1 and 3 gather the X rows (via src, or row r itself for per-row x)
+//    and A_e chunks, warp 2 the B_e chunks, with 16-byte cp.async into
+//    128-byte-swizzled K-major tiles;
+//  * warps 4-11 (two per TMEM lane quarter) scale and split h, then stream
+//    base_out: the pair owns the quarter's 32 rows of the tile, each warp
+//    takes every other 64-column box and runs its own ring of 32x64 TMA
+//    boxes (prefetch depth D-1), adds the accumulator, rounds once
 //    to bf16 (RNE) and TMA-stores boxes it owns whole; rows of a box it owns
 //    only in part are stored row by row, so no row of another tile is written.
 //  Every wait is bounded; a timeout sets an error bit and the CTA drains and
@@ -51,7 +56,7 @@ constexpr uint32_t kTmemH0 = 0, kTmemH1 = 64, kTmemAcc0 = 128, kTmemAcc1 = 256;
 static __device__ uint32_t g_grouped_errors;
 
 struct GroupedParams {
-  const uint8_t *x;              // bf16 [n_tokens, k_in]
+  const uint8_t *x;              // bf16 [n_tokens, k_in], or [rows, k_in] when x_per_row
   const int32_t *offsets;        // [n_experts + 1] or null (router: one span)
   const int32_t *src;            // sorted row -> flat row, or null (identity)
   const int32_t *row_adapter;    // [n_tokens] or null
@@ -70,6 +75,7 @@ struct GroupedParams {
   uint32_t xa_stage, b_stage;    // bytes per stage
   uint32_t off_xa, off_b, off_h, off_base, off_tab, off_my, smem_bytes;
   int32_t my_cap;                // tiles per CTA the tile list holds
+  int32_t x_per_row;             // 1: sorted row r reads x row r (not its token's)
 };
 
 // Byte offset of 16-byte chunk `c` (of 8 per 128-byte row) of row `row` in a
@@ -363,7 +369,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // A_e rows 32-63.  A stage is signalled xa_lag stages late (once the copies
     // of the stages after it are issued), so xa_lag + 1 stages are in flight.
     const int half = warp == 1 ? 0 : 1;
-    const uint64_t keep = l2_evict_last();  // x rows and A_e are re-read by other tiles
+    const uint64_t keep = l2_evict_last();  // A_e (and token x rows) are re-read by other tiles
+    const uint64_t xpol = p.x_per_row ? l2_evict_first() : keep;  // a per-row x row is read once
     uint32_t it = 0;
     int q[6] = {-1, -1, -1, -1, -1, -1};  // issued, not yet signalled stages (q[0] oldest)
     int nq = 0;
@@ -378,7 +385,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int r = mt.r0 + row;
         if (r < mt.r1) {
           const int sr = p.src ? __ldg(p.src + r) : r;
-          tok[u] = sr >= 0 ? sr / p.top_k : -1;
+          tok[u] = sr < 0 ? -1 : (p.x_per_row ? r : sr / p.top_k);
         }
       }
     };
@@ -413,7 +420,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const uint8_t *xr = reinterpret_cast<const uint8_t *>(
               __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(xrow[rl >> 5]), rl & 31));
           const bool v = __shfl_sync(0xffffffffu, xv[rl >> 5], rl & 31);
-          if (v) cp_async_16_hint(xs + sw128(half * 64 + rl, c), xr + (in ? kk * 2 : 0), in ? 16u : 0u, keep);
+          if (v) cp_async_16_hint(xs + sw128(half * 64 + rl, c), xr + (in ? kk * 2 : 0), in ? 16u : 0u, xpol);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -892,6 +899,34 @@ extern "C" mlg_status mlg_grouped_down_all_windows(
   p.row_offset = 0;
   p.row_end = total_rows;
   p.win = cap < static_cast<uint32_t>(total_rows) ? static_cast<int32_t>(cap) : total_rows;
+  return launch_grouped(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mlg_status mlg_grouped_down_xrows(
+    const mlg_bf16 *x_rows, const int32_t *expert_offsets, const int32_t *src,
+    const int32_t *row_adapter, const uint64_t *a_table, const uint64_t *b_table,
+    const float *scale_table, mlg_bf16 *base_out, int32_t k_in, int32_t max_rank, int32_t n_out,
+    int32_t top_k, int32_t n_experts, int32_t row_offset, int32_t row_end, uint32_t cap,
+    void *stream) {
+  using namespace mlg;
+  if (cap == 0) return MLG_ERR_CAP_ZERO;
+  if (top_k < 1 || n_experts < 0 || row_offset < 0 || row_end < row_offset)
+    return MLG_ERR_INVALID_ARG;
+  GroupedParams p = {};
+  const mlg_status st = fill_common(p, x_rows, row_adapter, a_table, b_table, scale_table,
+                                    base_out, k_in, max_rank, n_out);
+  if (st != MLG_OK) return st;
+  if (!expert_offsets || !src) return MLG_ERR_INVALID_ARG;
+  if (row_end == row_offset || n_experts == 0) return MLG_OK;
+  p.offsets = expert_offsets;
+  p.src = src;
+  p.top_k = top_k;
+  p.n_experts = n_experts;
+  p.row_offset = row_offset;
+  p.row_end = row_end;
+  const int32_t len = row_end - row_offset;
+  p.win = cap < static_cast<uint32_t>(len) ? static_cast<int32_t>(cap) : len;
+  p.x_per_row = 1;
   return launch_grouped(p, static_cast<cudaStream_t>(stream));
 }
 

@@ -72,6 +72,7 @@ class FoldProblem:
         mlg.mlg_upload_expert_tables(a, b, s, self.a_table, self.b_table, self.scale_table,
                                      stream=self._stream())
         self.x = _bits_tensor(w.x, self.device)
+        self.x_rows = None if w.x_rows is None else _bits_tensor(w.x_rows, self.device)
         self.guard_rows = guard_rows
         self.base_full = _bits_tensor(
             np.concatenate([np.full((guard_rows, w.n_out), 0x7FC1, np.uint16), w.base,
@@ -101,7 +102,8 @@ class FoldProblem:
 
         The grouped form folds all windows of grouped_down_windows(rows, cap)
         in one launch; per_window=True launches mlg_grouped_down once per
-        window instead (same bits)."""
+        window instead (same bits).  A workload with per-row inputs (x_rows)
+        runs the per-row x form over all rows."""
         w = self.w
         s = stream if stream is not None else self._stream()
         if w.kind == "gather":
@@ -110,7 +112,12 @@ class FoldProblem:
                                 w.max_rank, w.n_out, w.top_k, self.n_experts, stream=s)
         elif w.kind == "grouped":
             ra = self.row_adapter if use_row_map else None
-            if per_window:
+            if self.x_rows is not None:
+                mlg.mlg_grouped_down_xrows(self.x_rows, self.expert_offsets, self.src, ra,
+                                           self.a_table, self.b_table, self.scale_table,
+                                           self.base, w.k_in, w.max_rank, w.n_out, w.top_k,
+                                           self.n_experts, 0, w.rows, w.cap, stream=s)
+            elif per_window:
                 for start, end in self.windows:
                     mlg.mlg_grouped_down(self.x, self.expert_offsets, self.src, ra,
                                          self.a_table, self.b_table, self.scale_table, self.base,

@@ -28,6 +28,9 @@ Shapes of the named workloads:
                        rank 16, k_in 768, n_out 2048, windows of 8192 rows
 * ``decode_gate_up``   256 tokens, top-8, 64 of 128 experts adapted, rank 64,
                        k_in 2048, n_out 768; 154 active, 64 base, 38 padding
+* ``prefill_down_xrows`` ``prefill_down`` with a per-row input: x_rows
+                       [rows, 768] ~ N(0, 1), one row per sorted row (the
+                       expert's intermediate activation in a down projection)
 * ``prefill_large``    16384 tokens, top-10, 512 experts, rank 32, k_in 512,
                        n_out 2048, windows of 32768 rows
 * ``router``           one-entry route over 16384 tokens, k_in 2048,
@@ -93,6 +96,7 @@ class Workload:
     cu_seqlens: Optional[np.ndarray] = None  # int32 [batch + 1]
     stream_slots: Optional[np.ndarray] = None  # int32 [batch]
     cap: int = 0
+    x_rows: Optional[np.ndarray] = None  # bf16 bits [rows, k_in]: per-row input, sorted order
 
     @property
     def rows(self) -> int:
@@ -193,6 +197,14 @@ def prefill_down(seed: int = 2) -> Workload:
     return _prefill("prefill_down", rng, lengths, 8, 128, 768, 2048, 16, 8192)
 
 
+def prefill_down_xrows(seed: int = 2) -> Workload:
+    w = prefill_down(seed)
+    rng = np.random.default_rng(seed + 5000)
+    w.name = "prefill_down_xrows"
+    w.x_rows = _normal_bf16(rng, (w.rows, w.k_in))
+    return w
+
+
 def prefill_large(seed: int = 4) -> Workload:
     rng = np.random.default_rng(seed)
     return _prefill("prefill_large", rng, np.array([16384]), 10, 512, 512, 2048, 32, 32768)
@@ -230,7 +242,7 @@ def custom_gather(seed: int, n_tokens: int, top_k: int, n_experts: int, k_in: in
 def custom_grouped(seed: int, lengths, top_k: int, n_experts: int, k_in: int, n_out: int,
                    max_rank: int, cap: int, adapted_frac: float = 1.0,
                    stream_base: Optional[List[int]] = None,
-                   rank: Optional[int] = None) -> Workload:
+                   rank: Optional[int] = None, per_row_x: bool = False) -> Workload:
     """A packed prefill batch of arbitrary shape (for parity sweeps and edge cases)."""
     rng = np.random.default_rng(seed)
     n_adapt = max(1, int(round(adapted_frac * n_experts)))
@@ -244,6 +256,8 @@ def custom_grouped(seed: int, lengths, top_k: int, n_experts: int, k_in: int, n_
             e.B[:, rank:] = 0
     if stream_base is not None:
         w.stream_slots = np.array([-1 if b else 0 for b in stream_base], np.int32)
+    if per_row_x:
+        w.x_rows = _normal_bf16(rng, (w.rows, k_in))
     return w
 
 
@@ -260,6 +274,7 @@ NAMED = {
     "tiny_decode": tiny_decode,
     "decode_down": decode_down,
     "prefill_down": prefill_down,
+    "prefill_down_xrows": prefill_down_xrows,
     "decode_gate_up": decode_gate_up,
     "prefill_large": prefill_large,
     "router": router,

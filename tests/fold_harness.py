@@ -33,8 +33,13 @@ def oracle_reference(w, o=None, row_offset=None, row_end=None):
         ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
         lo = 0 if row_offset is None else row_offset
         hi = w.rows if row_end is None else row_end
-        ref, folded = o.grouped_fold(w.x, w.expert_offsets, w.src, ra, at, bt, st, w.base,
-                                     w.k_in, w.max_rank, w.n_out, w.top_k, lo, hi)
+        if w.x_rows is not None:
+            ref, folded = o.grouped_fold_xrows(w.x_rows, w.expert_offsets, w.src, ra, at, bt, st,
+                                               w.base, w.k_in, w.max_rank, w.n_out, w.top_k, lo,
+                                               hi)
+        else:
+            ref, folded = o.grouped_fold(w.x, w.expert_offsets, w.src, ra, at, bt, st, w.base,
+                                         w.k_in, w.max_rank, w.n_out, w.top_k, lo, hi)
     else:
         ref, folded = o.router_fold(w.x, None, at, bt, st, w.base, w.k_in, w.max_rank, w.n_out)
     return ref, folded, (he, at.size)

@@ -42,6 +42,8 @@ def integerize(w, seed):
     {1/2, 2}, base integers in [-64, 64] -> every result is a bf16 value."""
     rng = np.random.default_rng(seed)
     w.x = synth.bf16_bits(rng.integers(-1, 2, w.x.shape).astype(np.float32))
+    if w.x_rows is not None:
+        w.x_rows = synth.bf16_bits(rng.integers(-1, 2, w.x_rows.shape).astype(np.float32))
     w.base = synth.bf16_bits(rng.integers(-64, 65, w.base.shape).astype(np.float32))
     for i, e in enumerate(w.experts):
         e.A = synth.bf16_bits(_sparse_pm1(rng, w.max_rank, w.k_in, 2))
@@ -87,6 +89,13 @@ def test_gather_exact(shape, path):
 def test_grouped_exact():
     w = integerize(synth.custom_grouped(31, [120, 70, 90], 4, 10, 192, 320, 32, cap=100,
                                         adapted_frac=0.7, stream_base=[0, 1, 0]), 12)
+    _check_exact(w, lambda prob: prob.run())
+
+
+def test_grouped_xrows_exact():
+    w = integerize(synth.custom_grouped(33, [150, 60, 110], 6, 12, 256, 192, 32, cap=90,
+                                        adapted_frac=0.7, stream_base=[1, 0, 0],
+                                        per_row_x=True), 14)
     _check_exact(w, lambda prob: prob.run())
 
 

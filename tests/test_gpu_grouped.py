@@ -240,3 +240,83 @@ def test_grouped_matches_gather_form():
     ref, folded, _ = fh.oracle_reference(g)
     fh.check_fold(grouped_out, g.base, ref, folded)
     fh.check_fold(gather_out, g.base, ref, folded)
+
+
+# ------------------------------------------------ per-row x form (x_rows[r])
+@pytest.mark.parametrize("shape", GROUPED_SHAPES, ids=lambda s: f"{sum(s[0])}x{s[1]}_{s[3]}_{s[4]}_r{s[5]}")
+def test_xrows_shapes(shape):
+    lengths, K, E, k_in, n_out, r, cap, adapted, sb = shape
+    w = synth.custom_grouped(300 + k_in, lengths, K, E, k_in, n_out, r, cap=cap,
+                             adapted_frac=adapted, stream_base=sb, per_row_x=True)
+    _run_and_check(w)
+
+
+def test_prefill_down_xrows_full():
+    """The benchmark's per-row x workload at full size, every row checked."""
+    _, stats, folded = _run_and_check(synth.prefill_down_xrows())
+    assert folded.all()
+
+
+def test_xrows_token_rows_match_token_form_bits():
+    """x_rows holding each sorted row's token row gives the token form's bits
+    (same tiles, same arithmetic; only the address of each X row differs)."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_grouped(16, [210, 90, 333], 6, 24, 320, 512, 32, cap=400,
+                             adapted_frac=0.75, stream_base=[0, 1, 0])
+    tok = FoldProblem(w)
+    tok.run()
+    torch.cuda.synchronize()
+    w.x_rows = w.x[w.src // w.top_k]
+    per_row = FoldProblem(w)
+    per_row.run()
+    torch.cuda.synchronize()
+    assert np.array_equal(per_row.base_bits(), tok.base_bits())
+    ref, folded, _ = fh.oracle_reference(w)
+    fh.check_fold(per_row.base_bits(), w.base, ref, folded)
+
+
+@pytest.mark.parametrize("lo_hi_cap", [(17, -9, 50), (0, -1, 1 << 20), (128, 0, 128), (3, -200, 7)])
+def test_xrows_row_range_and_windows(lo_hi_cap):
+    """A sub-range [row_offset, row_end) in windows of cap rows: rows outside
+    keep their input (guard rows and all), rows inside match the oracle."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_grouped(18, [150, 260], 4, 12, 192, 256, 16, cap=64, adapted_frac=0.8,
+                             stream_base=[1, 0], per_row_x=True)
+    lo, hi, cap = lo_hi_cap
+    hi = w.rows + hi if hi <= 0 else hi
+    prob = FoldProblem(w, guard_rows=2)
+    mlg.mlg_grouped_down_xrows(prob.x_rows, prob.expert_offsets, prob.src, prob.row_adapter,
+                               prob.a_table, prob.b_table, prob.scale_table, prob.base, w.k_in,
+                               w.max_rank, w.n_out, w.top_k, prob.n_experts, lo, hi, cap)
+    torch.cuda.synchronize()
+    ref, folded, _ = fh.oracle_reference(w, row_offset=lo, row_end=hi)
+    assert not folded[:lo].any() and not folded[hi:].any()
+    fh.check_fold(prob.base_bits(), w.base, ref, folded)
+    assert np.all(prob.guard_bits() == 0x7FC1)
+
+
+def test_xrows_negative_src_and_no_row_map():
+    """Without a row map every row of a span folds; a negative src entry folds
+    nothing (its row keeps its input)."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_grouped(19, [120], 3, 6, 128, 128, 8, cap=1000, per_row_x=True)
+    prob = FoldProblem(w)
+    src = w.src.copy()
+    neg = np.array([0, 5, 77, w.rows - 1])
+    src[neg] = -1
+    mlg.mlg_grouped_down_xrows(prob.x_rows, prob.expert_offsets, torch.from_numpy(src).cuda(),
+                               None, prob.a_table, prob.b_table, prob.scale_table, prob.base,
+                               w.k_in, w.max_rank, w.n_out, w.top_k, prob.n_experts, 0, w.rows,
+                               1000)
+    torch.cuda.synchronize()
+    o = oracle.get()
+    he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
+    at, bt, st = he.tables(o)
+    ref, folded = o.grouped_fold_xrows(w.x_rows, w.expert_offsets, w.src, None, at, bt, st,
+                                       w.base, w.k_in, w.max_rank, w.n_out, w.top_k, 0, w.rows)
+    folded[neg] = False
+    ref[neg] = synth.bf16_to_f32(w.base[neg]).astype(np.float64)
+    fh.check_fold(prob.base_bits(), w.base, ref, folded)

@@ -277,6 +277,26 @@ def test_fold_validation_on_host(L):
     assert all_windows(max_rank=20) == mlg.MLG_ERR_UNSUPPORTED
     assert all_windows(total_rows=0) == mlg.MLG_OK
 
+    def xrows(**kw):
+        args = {**ok, "expert_offsets": p, "src": p, "row_offset": 0, "row_end": 100, "cap": 32,
+                **kw}
+        return L.mlg_grouped_down_xrows(
+            args["x"], args["expert_offsets"], args["src"], args["row_adapter"], args["a_table"],
+            args["b_table"], args["scale_table"], args["base_out"], args["k_in"],
+            args["max_rank"], args["n_out"], args["top_k"], args["n_experts"],
+            args["row_offset"], args["row_end"], args["cap"], 0)
+
+    assert xrows(cap=0) == mlg.MLG_ERR_CAP_ZERO
+    assert xrows(row_offset=7, row_end=6) == mlg.MLG_ERR_INVALID_ARG
+    assert xrows(row_offset=-2) == mlg.MLG_ERR_INVALID_ARG
+    assert xrows(src=None) == mlg.MLG_ERR_INVALID_ARG
+    assert xrows(x=None) == mlg.MLG_ERR_INVALID_ARG
+    assert xrows(x=p + 4) == mlg.MLG_ERR_UNSUPPORTED
+    assert xrows(top_k=0) == mlg.MLG_ERR_INVALID_ARG
+    assert xrows(n_out=12) == mlg.MLG_ERR_UNSUPPORTED
+    assert xrows(row_offset=40, row_end=40) == mlg.MLG_OK
+    assert xrows(n_experts=0) == mlg.MLG_OK
+
     def router(**kw):
         args = {**ok, "n_tokens": 16, **kw}
         return L.mlg_router_fold(args["x"], args["row_adapter"], args["a_table"],

@@ -31,6 +31,9 @@ Shapes of the named workloads:
 * ``prefill_down_xrows`` ``prefill_down`` with a per-row input: x_rows
                        [rows, 768] ~ N(0, 1), one row per sorted row (the
                        expert's intermediate activation in a down projection)
+* ``decode_down_multi`` ``decode_down``'s shape with 4 adapters installed at
+                       once (every expert adapted in each), each request's
+                       slot uniform over the 4; tables of 4 x 128 cells
 * ``prefill_large``    16384 tokens, top-10, 512 experts, rank 32, k_in 512,
                        n_out 2048, windows of 32768 rows
 * ``router``           one-entry route over 16384 tokens, k_in 2048,
@@ -97,6 +100,9 @@ class Workload:
     stream_slots: Optional[np.ndarray] = None  # int32 [batch]
     cap: int = 0
     x_rows: Optional[np.ndarray] = None  # bf16 bits [rows, k_in]: per-row input, sorted order
+    # multi-adapter form: tables of n_adapters * n_experts_model cells, slot-major
+    # (expert_id of an Expert is its cell, slot * n_experts_model + expert)
+    n_adapters: int = 0
 
     @property
     def rows(self) -> int:
@@ -239,6 +245,40 @@ def custom_gather(seed: int, n_tokens: int, top_k: int, n_experts: int, k_in: in
                     indices=idx, adapter_slots=slots, padded_n=n_tokens, active=0)
 
 
+def custom_gather_multi(seed: int, n_tokens: int, top_k: int, n_experts: int, k_in: int,
+                        n_out: int, max_rank: int, n_adapters: int, adapted_frac: float = 1.0,
+                        base_frac: float = 0.0, pad: int = 0, bad_ids: int = 0) -> Workload:
+    """A decode batch over several adapters at once: request slots are drawn
+    over [0, n_adapters) (base requests -1), each adapter adapts its own
+    subset of experts, and the expert pairs are keyed by cell
+    slot * n_experts + expert."""
+    rng = np.random.default_rng(seed)
+    idx = top_k_routing(rng, n_tokens, n_experts, top_k).reshape(-1)
+    for _ in range(bad_ids):
+        idx[int(rng.integers(0, idx.size))] = int(rng.choice([n_experts + 3, -1, 1 << 30]))
+    n_adapt = max(1, int(round(adapted_frac * n_experts)))
+    cells = []
+    for s in range(n_adapters):
+        adapted = np.sort(rng.choice(n_experts, size=n_adapt, replace=False))
+        cells += [s * n_experts + int(e) for e in adapted]
+    real = max(0, n_tokens - pad)
+    slots = rng.integers(0, n_adapters, real).astype(np.int32)
+    slots[rng.random(real) < base_frac] = -1
+    x = _normal_bf16(rng, (n_tokens, k_in))
+    base = _normal_bf16(rng, (n_tokens * top_k, n_out))
+    experts = _experts(rng, cells, k_in, max_rank, n_out)
+    return Workload(f"gather_multi{n_adapters}_{n_tokens}x{top_k}_{k_in}_{n_out}_r{max_rank}",
+                    "gather", k_in, max_rank, n_out, top_k, n_tokens, x, base, experts, n_experts,
+                    indices=idx, adapter_slots=slots, padded_n=n_tokens, active=0,
+                    n_adapters=n_adapters)
+
+
+def decode_down_multi(seed: int = 6) -> Workload:
+    w = custom_gather_multi(seed, 64, 8, 128, 768, 2048, 16, 4)
+    w.name = "decode_down_multi"
+    return w
+
+
 def custom_grouped(seed: int, lengths, top_k: int, n_experts: int, k_in: int, n_out: int,
                    max_rank: int, cap: int, adapted_frac: float = 1.0,
                    stream_base: Optional[List[int]] = None,
@@ -276,6 +316,7 @@ NAMED = {
     "prefill_down": prefill_down,
     "prefill_down_xrows": prefill_down_xrows,
     "decode_gate_up": decode_gate_up,
+    "decode_down_multi": decode_down_multi,
     "prefill_large": prefill_large,
     "router": router,
 }

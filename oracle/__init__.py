@@ -74,6 +74,10 @@ class Oracle:
         L.oracle_ensure_decode_route_servable.restype = _i32
         L.oracle_build_moe_row_adapter_decode.argtypes = [_p, _i64, _i64, _i32, _i32, _p]
         L.oracle_build_moe_row_adapter_decode.restype = None
+        L.oracle_build_moe_row_adapter_decode_multi.argtypes = [_p, _i64, _i64, _i32, _i32, _p]
+        L.oracle_build_moe_row_adapter_decode_multi.restype = _i32
+        L.oracle_gather_fold_multi.argtypes = [_p] * 9 + [_i32] * 7
+        L.oracle_gather_fold_multi.restype = _i32
         L.oracle_build_moe_row_adapter_host.argtypes = [_p, _i64, _p, _i64, _p, _i64, _p]
         L.oracle_build_moe_row_adapter_host.restype = _i32
         L.oracle_pack_expert_tables.argtypes = [_p, _p, _p, _p, _i64, _p, _p, _p, _i64, _p]
@@ -113,6 +117,15 @@ class Oracle:
         self.lib.oracle_build_moe_row_adapter_decode(
             _ptr(slots), slots.size, padded_n, active, int(bool(has_moe_lora)), _ptr(out))
         return out
+
+    def build_moe_row_adapter_decode_multi(self, adapter_slots, padded_n: int, n_adapters: int,
+                                           has_moe_lora: bool):
+        """(status, map): the multi-adapter decode map, or REFUSE with nothing written."""
+        slots = np.ascontiguousarray(adapter_slots, dtype=np.int32)
+        out = np.full(padded_n, 0x5A5A5A5A, dtype=np.int32)
+        st = self.lib.oracle_build_moe_row_adapter_decode_multi(
+            _ptr(slots), slots.size, padded_n, n_adapters, int(bool(has_moe_lora)), _ptr(out))
+        return st, out
 
     def build_moe_row_adapter_host(self, cu_seqlens, adapter_slots) -> Optional[np.ndarray]:
         cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
@@ -203,6 +216,24 @@ class Oracle:
                                           _ptr(bt), _ptr(st_), _ptr(base), _ptr(ref),
                                           _ptr(folded), total, k_in, max_rank, n_out, top_k,
                                           at.size, row_offset, row_end)
+        assert st == OK, st
+        return ref, folded.astype(bool)
+
+    def gather_fold_multi(self, x, indices, row_adapter, a_table, b_table, scale_table, base,
+                          k_in, max_rank, n_out, top_k, n_experts, n_adapters):
+        """Multi-adapter gather fold over slot-major tables of n_adapters * n_experts cells."""
+        x, base = self._u16(x), self._u16(base)
+        idx = np.ascontiguousarray(indices, np.int32)
+        ra = np.ascontiguousarray(row_adapter, np.int32)
+        at, bt = np.ascontiguousarray(a_table, np.uint64), np.ascontiguousarray(b_table, np.uint64)
+        st_ = np.ascontiguousarray(scale_table, np.float32)
+        assert at.size == bt.size == st_.size == n_experts * n_adapters
+        n = idx.size
+        ref = np.empty((n, n_out), np.float64)
+        folded = np.empty(n, np.uint8)
+        st = self.lib.oracle_gather_fold_multi(_ptr(x), _ptr(idx), _ptr(ra), _ptr(at), _ptr(bt),
+                                               _ptr(st_), _ptr(base), _ptr(ref), _ptr(folded), n,
+                                               k_in, max_rank, n_out, top_k, n_experts, n_adapters)
         assert st == OK, st
         return ref, folded.astype(bool)
 
@@ -331,6 +362,13 @@ class HostExperts:
             self.b_addr.append(B.ctypes.data)
             self.scale.append(float(s))
 
-    def tables(self, oracle: Optional[Oracle] = None):
+    def tables(self, oracle: Optional[Oracle] = None, length: Optional[int] = None):
+        """Packed tables; with `length`, padded with empty cells to that many."""
         o = oracle or get()
-        return o.pack_expert_tables(self.ids, self.a_addr, self.b_addr, self.scale)
+        at, bt, st = o.pack_expert_tables(self.ids, self.a_addr, self.b_addr, self.scale)
+        if length is not None and length > at.size:
+            pad = length - at.size
+            at = np.concatenate([at, np.zeros(pad, at.dtype)])
+            bt = np.concatenate([bt, np.zeros(pad, bt.dtype)])
+            st = np.concatenate([st, np.zeros(pad, st.dtype)])
+        return at, bt, st

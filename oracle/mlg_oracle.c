@@ -86,6 +86,31 @@ void oracle_build_moe_row_adapter_decode(const int32_t *adapter_slots, int64_t n
     }
 }
 
+/* Multi-adapter decode map.  [P1] resolve_moe_lora_route refuses any slot
+ * other than the active one because only the active adapter's pairs are
+ * installed (ensure_decode_route_servable's message: one adapter per batch).
+ * With one table set installed per slot 0 .. n_adapters - 1, the entry of a
+ * request is its own slot when that slot has a set, and -1 for base requests
+ * (slot < 0) and padding entries.  A slot at or past n_adapters has no set:
+ * the whole batch is refused (OR_REFUSE) with nothing written, the same
+ * refusal moved to the slots without tables.  With no MoE LoRA loaded
+ * (has_moe_lora == 0) nothing folds: every entry is -1. */
+int32_t oracle_build_moe_row_adapter_decode_multi(const int32_t *adapter_slots, int64_t n_slots,
+                                                  int64_t padded_n, int32_t n_adapters,
+                                                  int32_t has_moe_lora, int32_t *out) {
+    if (has_moe_lora) {
+        for (int64_t i = 0; i < n_slots && i < padded_n; ++i) {
+            if (adapter_slots[i] >= n_adapters) return OR_REFUSE;
+        }
+    }
+    for (int64_t i = 0; i < padded_n; ++i) {
+        int32_t entry = -1;
+        if (has_moe_lora && i < n_slots && adapter_slots[i] >= 0) entry = adapter_slots[i];
+        out[i] = entry;
+    }
+    return OR_OK;
+}
+
 /* [P1] build_moe_row_adapter_host: the [total_tokens] prefill map.  `cu` is the
  * [batch + 1] prefix sum of stream lengths; stream b's slot is written
  * unchanged over rows cu[b] .. cu[b+1].  None (OR_NONE, nothing written) when
@@ -233,6 +258,39 @@ int32_t oracle_gather_fold(const uint16_t *x, const int32_t *indices, const int3
         const uint16_t *B = (const uint16_t *)(uintptr_t)b_table[e];
         fold_one_row(x + (int64_t)t * k_in, A, B, (double)scale_table[e], base_row, ref_row, k_in,
                      max_rank, n_out);
+        folded[row] = 1;
+    }
+    return OR_OK;
+}
+
+/* Multi-adapter gather fold.  The tables hold one set of n_experts cells per
+ * adapter slot, slot-major: cell s * n_experts + e is adapter s's pair for
+ * expert e.  The row map entry of a row's token names the set:
+ * s = row_adapter[row / top_k]; a row folds nothing when s < 0, when
+ * s >= n_adapters, when e = indices[row] is outside [0, n_experts), or when
+ * its cell is zero; otherwise it folds as the [P2] moe_lora_gather_bgmv row
+ * does, through its cell. */
+int32_t oracle_gather_fold_multi(const uint16_t *x, const int32_t *indices,
+                                 const int32_t *row_adapter, const uint64_t *a_table,
+                                 const uint64_t *b_table, const float *scale_table,
+                                 const uint16_t *base_in, double *ref_out, uint8_t *folded,
+                                 int32_t n_slots, int32_t k_in, int32_t max_rank, int32_t n_out,
+                                 int32_t top_k, int32_t n_experts, int32_t n_adapters) {
+    if (max_rank > 1024 || top_k < 1 || n_adapters < 1) return OR_NONE;
+    for (int32_t row = 0; row < n_slots; ++row) {
+        const uint16_t *base_row = base_in + (int64_t)row * n_out;
+        double *ref_row = ref_out + (int64_t)row * n_out;
+        int32_t t = row / top_k;
+        int32_t s = row_adapter[t];
+        int32_t e = indices[row];
+        folded[row] = 0;
+        copy_row(base_row, ref_row, n_out);
+        if (s < 0 || s >= n_adapters || e < 0 || e >= n_experts) continue;
+        int64_t cell = (int64_t)s * n_experts + e;
+        if (!expert_folds(cell, n_adapters * n_experts, a_table, b_table)) continue;
+        fold_one_row(x + (int64_t)t * k_in, (const uint16_t *)(uintptr_t)a_table[cell],
+                     (const uint16_t *)(uintptr_t)b_table[cell], (double)scale_table[cell],
+                     base_row, ref_row, k_in, max_rank, n_out);
         folded[row] = 1;
     }
     return OR_OK;

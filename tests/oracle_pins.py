@@ -365,6 +365,55 @@ def pin_xrows_forms(o):
     assert np.array_equal(ref_s, ref_w[rows]) and np.array_equal(fold_s, fold_w[rows])
 
 
+def pin_multi_adapter(o):
+    """The multi-adapter fold: with one adapter it is the gather fold; in
+    general it is, row for row, the gather fold of the row's own adapter's
+    table slice (each row folds through exactly one set); and its decode map
+    keeps installed slots, blanks base requests and padding, refuses a slot
+    with no set, and folds nothing without MoE LoRA."""
+    E, S = 9, 3
+    w = synth.custom_gather_multi(21, n_tokens=13, top_k=3, n_experts=E, k_in=40, n_out=24,
+                                  max_rank=8, n_adapters=S, adapted_frac=0.7, base_frac=0.2,
+                                  bad_ids=2)
+    he = HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
+    at, bt, st = he.tables(o, length=S * E)
+    status, ra = o.build_moe_row_adapter_decode_multi(w.adapter_slots, w.padded_n, S, True)
+    assert status == 0 and np.array_equal(ra, np.where(w.adapter_slots >= 0, w.adapter_slots, -1))
+    ref_m, fold_m = o.gather_fold_multi(w.x, w.indices, ra, at, bt, st, w.base, w.k_in,
+                                        w.max_rank, w.n_out, w.top_k, E, S)
+    assert fold_m.any() and (~fold_m).any()
+    tok = np.arange(w.rows) // w.top_k
+    acc = _f(w.base)
+    seen = np.zeros(w.rows, bool)
+    for s in range(S):
+        sl = slice(s * E, (s + 1) * E)
+        ra_s = np.where(ra == s, 0, -1).astype(np.int32)
+        ref_s, fold_s = o.gather_fold(w.x, w.indices, ra_s, at[sl], bt[sl], st[sl], w.base,
+                                      w.k_in, w.max_rank, w.n_out, w.top_k)
+        mine = ra[tok] == s
+        assert not (fold_s & ~mine).any()
+        acc[mine] = ref_s[mine]
+        seen |= fold_s
+    assert np.array_equal(seen, fold_m) and np.array_equal(acc, ref_m)
+    # one adapter: the gather fold itself
+    ra1 = np.where(ra >= 0, 0, -1).astype(np.int32)
+    ref_1, fold_1 = o.gather_fold_multi(w.x, w.indices, ra1, at[:E], bt[:E], st[:E], w.base,
+                                        w.k_in, w.max_rank, w.n_out, w.top_k, E, 1)
+    ref_g, fold_g = o.gather_fold(w.x, w.indices, ra1, at[:E], bt[:E], st[:E], w.base, w.k_in,
+                                  w.max_rank, w.n_out, w.top_k)
+    assert np.array_equal(ref_1, ref_g) and np.array_equal(fold_1, fold_g)
+    # decode map cases
+    st_, m = o.build_moe_row_adapter_decode_multi([2, -1, 0, 1, -7], 6, 3, True)
+    assert st_ == 0 and m.tolist() == [2, -1, 0, 1, -1, -1]
+    st_, m = o.build_moe_row_adapter_decode_multi([0, 3, -1], 4, 3, True)
+    assert st_ == -4 and np.all(m == 0x5A5A5A5A)  # refused, nothing written
+    st_, m = o.build_moe_row_adapter_decode_multi([0, 3, 1], 4, 3, False)
+    assert st_ == 0 and m.tolist() == [-1, -1, -1, -1]
+    slots = np.array([0, -1, 0, 0, -1], np.int32)
+    st_, m = o.build_moe_row_adapter_decode_multi(slots, 7, 1, True)
+    assert st_ == 0 and np.array_equal(m, o.build_moe_row_adapter_decode(slots, 7, 0, True))
+
+
 ALL_PINS = [
     pin_route_truth_table,
     pin_decode_maps,
@@ -383,4 +432,5 @@ ALL_PINS = [
     pin_router_is_one_entry_route,
     pin_sampled_rows_match_full,
     pin_xrows_forms,
+    pin_multi_adapter,
 ]

@@ -46,6 +46,13 @@ MUTANTS = {
                                      "row_adapter[r / top_k] < 0) continue;\n            fold_one_row(x_rows"),
     "sampled x_rows by token": ("fold_one_row(x_rows + (int64_t)r * k_in",
                                 "fold_one_row(x_rows + (int64_t)(src[r] / top_k) * k_in"),
+    "multi cell expert-major": ("int64_t cell = (int64_t)s * n_experts + e;",
+                                "int64_t cell = (int64_t)e * n_adapters + s;"),
+    "multi map writes slot 0": ("adapter_slots[i] >= 0) entry = adapter_slots[i];",
+                                "adapter_slots[i] >= 0) entry = 0;"),
+    "multi refusal dropped": ("if (adapter_slots[i] >= n_adapters) return OR_REFUSE;", ";"),
+    "multi base requests kept": ("if (has_moe_lora && i < n_slots && adapter_slots[i] >= 0)",
+                                 "if (has_moe_lora && i < n_slots)"),
     "padding gets active": ("        } else {\n            out[i] = -1;\n        }",
                             "        } else {\n            out[i] = active;\n        }"),
 }

@@ -52,6 +52,9 @@ WORKLOADS = {
                    "all adapted, rank 16, k_in 768, n_out 2048, bf16",
     "decode_gate_up": "decode gather BGMV, gate/up: 256 tokens x top-8 (2048 rows), 64 of 128 "
                       "experts adapted, rank 64, k_in 2048, n_out 768; 154 active / 64 base / 38 pad",
+    "decode_down_multi": "multi-adapter decode gather BGMV, down-proj: decode_down's shape with 4 "
+                         "adapters installed at once (4 x 128 cells, all adapted), request slots "
+                         "uniform over the 4",
     "prefill_down": "prefill grouped fold, down-proj: 8 streams U[256,768] tokens x top-8, 128 "
                     "experts, rank 16, k_in 768, n_out 2048, skewed routing, windows of 8192 rows",
     "prefill_down_xrows": "prefill grouped fold, down-proj, per-row input (x_rows [rows, 768], one "
@@ -110,6 +113,10 @@ def algorithmic(w, row_map, tables):
         rows = w.indices.size
         tok = np.arange(rows) // w.top_k
         e = w.indices.astype(np.int64)
+        if w.n_adapters:  # the row's cell in the slot-major multi-adapter tables
+            s = row_map[tok].astype(np.int64)
+            ok_id = (s >= 0) & (s < w.n_adapters) & (e >= 0) & (e < w.n_experts_model)
+            e = np.where(ok_id, s * w.n_experts_model + e, -1)
     elif w.kind == "grouped":
         rows = w.rows
         e = np.repeat(np.arange(w.n_experts_model), np.diff(w.expert_offsets))
@@ -203,7 +210,7 @@ def time_oracle(w, budget_s=10.0):
 
     o = oracle.get()
     he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
-    at, bt, st = he.tables(o)
+    at, bt, st = he.tables(o, length=(w.n_adapters * w.n_experts_model) if w.n_adapters else None)
     flops_row = 2 * w.max_rank * (w.k_in + w.n_out)
     full_cost = w.rows * flops_row
     rng = np.random.default_rng(0)
@@ -212,7 +219,12 @@ def time_oracle(w, budget_s=10.0):
     passes = 0
     if full_cost <= 2e9:
         while time.perf_counter() - t0 < budget_s or passes == 0:
-            if w.kind == "gather":
+            if w.kind == "gather" and w.n_adapters:
+                _, ra = o.build_moe_row_adapter_decode_multi(w.adapter_slots, w.padded_n,
+                                                             w.n_adapters, w.has_moe_lora)
+                o.gather_fold_multi(w.x, w.indices, ra, at, bt, st, w.base, w.k_in, w.max_rank,
+                                    w.n_out, w.top_k, w.n_experts_model, w.n_adapters)
+            elif w.kind == "gather":
                 ra = o.build_moe_row_adapter_decode(w.adapter_slots, w.padded_n, w.active,
                                                     w.has_moe_lora)
                 o.gather_fold(w.x, w.indices, ra, at, bt, st, w.base, w.k_in, w.max_rank,
@@ -268,7 +280,7 @@ def n_sets_for(w_bytes):
 KERNEL_OF = {"decode_down": "mlg_decode.cu", "decode_gate_up": "mlg_gather.cu",
              "tiny_decode": "mlg_gather.cu", "prefill_down": "mlg_grouped.cu",
              "prefill_large": "mlg_grouped.cu", "router": "mlg_grouped.cu",
-             "prefill_down_xrows": "mlg_grouped.cu"}
+             "prefill_down_xrows": "mlg_grouped.cu", "decode_down_multi": "mlg_gather.cu"}
 
 
 def kernel_source(workload):
@@ -348,6 +360,7 @@ def e2e_measure(prob, steps, device):
     import torch
 
     import lora_moe_expert_gb300 as mlg
+    from lora_moe_expert_gb300.device import pad_tables
 
     w = prob.w
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
@@ -366,7 +379,10 @@ def e2e_measure(prob, steps, device):
         nonlocal h2d, d2h
         h2d = d2h = 0
         with torch.cuda.stream(s):
-            if w.kind == "gather":
+            if w.kind == "gather" and w.n_adapters:
+                m = mlg.mlg_build_moe_row_adapter_decode_multi(w.adapter_slots, w.padded_n,
+                                                               w.n_adapters, w.has_moe_lora)
+            elif w.kind == "gather":
                 m = mlg.mlg_build_moe_row_adapter_decode(w.adapter_slots, w.padded_n, w.active,
                                                          w.has_moe_lora)
             elif w.kind == "grouped":
@@ -375,6 +391,8 @@ def e2e_measure(prob, steps, device):
                 m = None
             a, b, sc = mlg.mlg_pack_expert_tables(prob.pool.ids, prob.pool.a_addr,
                                                   prob.pool.b_addr, prob.pool.scale)
+            if w.n_adapters:
+                a, b, sc = pad_tables(a, b, sc, w.n_adapters * w.n_experts_model)
             mlg.mlg_upload_expert_tables(a, b, sc, prob.a_table, prob.b_table, prob.scale_table,
                                          stream=s)
             h2d += a.nbytes + b.nbytes + sc.nbytes

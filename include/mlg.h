@@ -124,6 +124,33 @@ MLG_API mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices, co
                            int32_t k_in, int32_t max_rank, int32_t n_out, int32_t top_k,
                            int32_t n_experts, void *stream);
 
+/* Multi-adapter gather fold.  The single-active rule of resolve_moe_lora_route
+ * and ensure_decode_route_servable (moe_row_adapter.rs) refuses a batch that
+ * mixes adapters because only the active adapter's pairs are installed.  Here
+ * one table set per adapter slot is installed at once, slot-major: cell
+ * s * n_experts + e holds adapter s's pair for expert e.  A row's token names
+ * its set through the row map, s = row_adapter[row / top_k], and the row folds
+ *     base_out[row] += scale[c] * (x[row / top_k] @ A_c^T) @ B_c^T,
+ *     c = s * n_experts + indices[row],
+ * unless s < 0, s >= n_adapters, indices[row] is outside [0, n_experts) or
+ * cell c is zero (those rows keep their input).
+ *
+ *   tables       device, [n_adapters * n_experts] each, slot-major; every
+ *                set packed by mlg_pack_expert_tables with cap n_experts
+ *                (holes are zero cells)
+ *   row_adapter  device, [ceil(n_slots / top_k)] int32 slot per token
+ *                (mlg_build_moe_row_adapter_decode_multi), required
+ *   n_adapters   >= 1; n_adapters * n_experts <= 2^30
+ *   others       as for mlg_gather_bgmv
+ * Errors as for mlg_gather_bgmv, plus INVALID_ARG for n_adapters < 1 and
+ * UNSUPPORTED for more than 2^30 cells. */
+MLG_API mlg_status mlg_gather_bgmv_multi(const mlg_bf16 *x, const int32_t *indices,
+                                         const int32_t *row_adapter, const uint64_t *a_table,
+                                         const uint64_t *b_table, const float *scale_table,
+                                         mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
+                                         int32_t max_rank, int32_t n_out, int32_t top_k,
+                                         int32_t n_experts, int32_t n_adapters, void *stream);
+
 /* moe_lora_grouped_down (moe_lora_grouped module index): the prefill-side fold
  * over expert-sorted rows r in the window [row_offset, row_end).  e is the
  * expert whose span expert_offsets[e] <= r < expert_offsets[e + 1] holds r
@@ -227,6 +254,18 @@ MLG_API mlg_status mlg_ensure_decode_route_servable(int32_t route);
 MLG_API mlg_status mlg_build_moe_row_adapter_decode(const int32_t *adapter_slots, size_t n_slots,
                                             size_t padded_n, int32_t active,
                                             int32_t has_moe_lora, int32_t *out);
+
+/* Decode map of the multi-adapter fold (see mlg_gather_bgmv_multi): entry i
+ * is adapter_slots[i] when 0 <= slot < n_adapters, -1 for a base request
+ * (slot < 0) and for padding (i >= n_slots), and -1 everywhere when
+ * has_moe_lora is 0.  A slot >= n_adapters has no table set: the call
+ * returns MLG_ERR_REFUSE and writes nothing (the single-active refusal, moved
+ * to the slots without tables).  Errors: INVALID_ARG for out == NULL with
+ * padded_n > 0, adapter_slots == NULL with n_slots > 0, or n_adapters < 1. */
+MLG_API mlg_status mlg_build_moe_row_adapter_decode_multi(const int32_t *adapter_slots,
+                                                          size_t n_slots, size_t padded_n,
+                                                          int32_t n_adapters,
+                                                          int32_t has_moe_lora, int32_t *out);
 
 /* build_moe_row_adapter_host (moe_row_adapter.rs): the [total_tokens] prefill
  * row map.  cu_seqlens holds n_cu = batch + 1 prefix sums; stream b's slot is

@@ -64,6 +64,8 @@ _SIGNATURES = {
     "mlg_ensure_decode_route_servable": ([_i32], _i32),
     "mlg_build_moe_row_adapter_decode": ([_p, _sz, _sz, _i32, _i32, _p], _i32),
     "mlg_build_moe_row_adapter_host": ([_p, _sz, _p, _sz, _p, _sz, _p], _i32),
+    "mlg_build_moe_row_adapter_decode_multi": ([_p, _sz, _sz, _i32, _i32, _p], _i32),
+    "mlg_gather_bgmv_multi": ([_p] * 7 + [_i32] * 7 + [_p], _i32),
     "mlg_pack_expert_tables": ([_p, _sz, _p, _p, _p, _sz, _p], _i32),
     "mlg_upload_expert_tables": ([_p, _p, _p, _u32, _p, _p, _p, _p], _i32),
     "mlg_upload_row_adapter": ([_p, _sz, _p, _p], _i32),
@@ -138,6 +140,16 @@ def mlg_gather_bgmv(x, indices, row_adapter, a_table, b_table, scale_table, base
            "mlg_gather_bgmv")
 
 
+def mlg_gather_bgmv_multi(x, indices, row_adapter, a_table, b_table, scale_table, base_out,
+                          n_slots, k_in, max_rank, n_out, top_k, n_experts, n_adapters,
+                          stream=None) -> None:
+    _check(lib().mlg_gather_bgmv_multi(_addr(x), _addr(indices), _addr(row_adapter),
+                                       _addr(a_table), _addr(b_table), _addr(scale_table),
+                                       _addr(base_out), n_slots, k_in, max_rank, n_out, top_k,
+                                       n_experts, n_adapters, _stream(stream)),
+           "mlg_gather_bgmv_multi")
+
+
 def mlg_grouped_down(x, expert_offsets, src, row_adapter, a_table, b_table, scale_table,
                      base_out, k_in, max_rank, n_out, top_k, n_experts, row_offset, row_end,
                      stream=None) -> None:
@@ -190,6 +202,17 @@ def mlg_build_moe_row_adapter_decode(adapter_slots, padded_n: int, active: int,
     _check(lib().mlg_build_moe_row_adapter_decode(_hp(slots), slots.size, padded_n, active,
                                                   int(bool(has_moe_lora)), _hp(out)),
            "mlg_build_moe_row_adapter_decode")
+    return out
+
+
+def mlg_build_moe_row_adapter_decode_multi(adapter_slots, padded_n: int, n_adapters: int,
+                                           has_moe_lora: bool) -> np.ndarray:
+    slots = _host(adapter_slots, np.int32)
+    out = np.empty(padded_n, np.int32)
+    _check(lib().mlg_build_moe_row_adapter_decode_multi(_hp(slots), slots.size, padded_n,
+                                                        n_adapters, int(bool(has_moe_lora)),
+                                                        _hp(out)),
+           "mlg_build_moe_row_adapter_decode_multi")
     return out
 
 

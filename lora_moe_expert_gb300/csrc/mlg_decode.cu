@@ -64,7 +64,8 @@ struct DecodeParams {
   const uint64_t *b_table;
   const float *scale_table;
   uint16_t *base_out;
-  int32_t n_slots, k_in, n_out, top_k, n_experts;
+  int32_t n_slots, k_in, n_out, top_k, n_experts;  // n_experts: table cells
+  int32_t e_model, n_adapters;  // multi-adapter tables (n_adapters > 0): cell = slot * e_model + id
   int32_t spec_mode;  // 0: speculative row scan, 1: none, 2: scan a different expert (tests)
   uint32_t stride_a;  // bytes per A_e / x row in shared memory
   uint32_t off_a, off_x, off_b, off_p, off_h, zero_bytes, smem_bytes;
@@ -103,6 +104,10 @@ __device__ __forceinline__ void scan_load(const DecodeParams &p, int base, int (
       idx[i] = ld_cg_s32(p.indices + row);
       ra[i] = ld_cg_s32(p.row_adapter + row / p.top_k);
     }
+    if (p.n_adapters > 0)  // the row map names the table set: fold through its cell
+      idx[i] = (ra[i] >= 0 && ra[i] < p.n_adapters && idx[i] >= 0 && idx[i] < p.e_model)
+                   ? ra[i] * p.e_model + idx[i]
+                   : -1;
   }
 }
 
@@ -714,10 +719,10 @@ int gather_path_override() { return g_path_override; }
 // Whether the resident-pair kernel takes this problem (shapes already
 // validated): rank 16 or 32, n_out <= 2048, the pair, 8 x rows and the
 // buffers within half an SM, and at most one expert per SM.
-bool decode_fold_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t n_experts) {
+bool decode_fold_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t n_cells) {
   if (max_rank != 16 && max_rank != 32) return false;
   if (n_out > kMaxBlocks * kWarps * 64) return false;
-  if (n_experts > decode_grid()) return false;
+  if (n_cells > decode_grid()) return false;
   DecodeParams p = {};
   p.k_in = k_in;
   p.n_out = n_out;
@@ -729,7 +734,8 @@ cudaError_t decode_fold_launch(const uint16_t *x, const int32_t *indices,
                                const uint64_t *b_table, const float *scale_table,
                                uint16_t *base_out, int32_t n_slots, int32_t k_in,
                                int32_t max_rank, int32_t n_out, int32_t top_k,
-                               int32_t n_experts, cudaStream_t stream) {
+                               int32_t n_cells, int32_t e_model, int32_t n_adapters,
+                               cudaStream_t stream) {
   DecodeParams p = {};
   p.x = x;
   p.indices = indices;
@@ -742,7 +748,9 @@ cudaError_t decode_fold_launch(const uint16_t *x, const int32_t *indices,
   p.k_in = k_in;
   p.n_out = n_out;
   p.top_k = top_k;
-  p.n_experts = n_experts;
+  p.n_experts = n_cells;
+  p.e_model = e_model;
+  p.n_adapters = n_adapters;
   p.spec_mode = g_spec_mode;
   layout(p, max_rank);
   const int grid = decode_grid();  // owners, then helpers for experts with many rows

@@ -58,7 +58,8 @@ struct GatherParams {
   const uint64_t *b_table;
   const float *scale_table;
   uint16_t *base_out;
-  int32_t n_slots, k_in, rank, n_out, top_k, n_experts;
+  int32_t n_slots, k_in, rank, n_out, top_k, n_experts;  // n_experts: table cells
+  int32_t e_model, n_adapters;  // multi-adapter tables (n_adapters > 0): cell = slot * e_model + id
   int32_t ns2;            // n slices per cluster rank (independent CTAs, full shrink each)
   int32_t ks, ns;         // k columns per cluster rank, n columns per CTA
   int32_t rg;             // rows per pass (16 or 32)
@@ -87,6 +88,10 @@ __device__ __forceinline__ void scan_load(const GatherParams &p, int base, int (
       idx[i] = __ldg(p.indices + row);
       ra[i] = __ldg(p.row_adapter + row / p.top_k);
     }
+    if (p.n_adapters > 0)  // the row map names the table set: fold through its cell
+      idx[i] = (ra[i] >= 0 && ra[i] < p.n_adapters && idx[i] >= 0 && idx[i] < p.e_model)
+                   ? ra[i] * p.e_model + idx[i]
+                   : -1;
   }
 }
 
@@ -697,16 +702,16 @@ void gather_set_nsplit_override(int ns2) { g_nsplit_override = ns2; }
 
 }  // namespace mlg
 
-extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
-                                      const int32_t *row_adapter, const uint64_t *a_table,
-                                      const uint64_t *b_table, const float *scale_table,
-                                      mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
-                                      int32_t max_rank, int32_t n_out, int32_t top_k,
-                                      int32_t n_experts, void *stream) {
-  using namespace mlg;
-  if (n_slots < 0 || n_experts < 0 || top_k < 1) return MLG_ERR_INVALID_ARG;
-  const mlg_status shape = check_shapes(k_in, max_rank, n_out);
-  if (shape != MLG_OK) return shape;
+namespace mlg {
+namespace {
+
+// Both gather entry points: n_experts is the table length (cells); e_model /
+// n_adapters describe multi-adapter tables (n_adapters == 0: single set).
+mlg_status gather_dispatch(const mlg_bf16 *x, const int32_t *indices, const int32_t *row_adapter,
+                           const uint64_t *a_table, const uint64_t *b_table,
+                           const float *scale_table, mlg_bf16 *base_out, int32_t n_slots,
+                           int32_t k_in, int32_t max_rank, int32_t n_out, int32_t top_k,
+                           int32_t n_experts, int32_t e_model, int32_t n_adapters, void *stream) {
   if (n_slots == 0 || n_experts == 0) return MLG_OK;
   if (!x || !indices || !row_adapter || !a_table || !b_table || !scale_table || !base_out)
     return MLG_ERR_INVALID_ARG;
@@ -719,7 +724,8 @@ extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
   if (path != 2 && resident)
     return cuda_status(decode_fold_launch(x, indices, row_adapter, a_table, b_table, scale_table,
                                           base_out, n_slots, k_in, max_rank, n_out, top_k,
-                                          n_experts, static_cast<cudaStream_t>(stream)));
+                                          n_experts, e_model, n_adapters,
+                                          static_cast<cudaStream_t>(stream)));
 
   GatherParams p = {};
   p.x = x;
@@ -735,6 +741,8 @@ extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
   p.n_out = n_out;
   p.top_k = top_k;
   p.n_experts = n_experts;
+  p.e_model = e_model;
+  p.n_adapters = n_adapters;
   const int rp = static_cast<int>(round_up(max_rank, 16));
   // Rows per pass: decode batches spread ~n_slots / n_experts rows per expert.
   p.rg = (n_slots <= 16 * n_experts) ? 16 : 32;
@@ -770,4 +778,38 @@ extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
     default: err = launch<64>(p, cs, clusters, s); break;
   }
   return cuda_status(err);
+}
+
+}  // namespace
+}  // namespace mlg
+
+extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
+                                      const int32_t *row_adapter, const uint64_t *a_table,
+                                      const uint64_t *b_table, const float *scale_table,
+                                      mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
+                                      int32_t max_rank, int32_t n_out, int32_t top_k,
+                                      int32_t n_experts, void *stream) {
+  using namespace mlg;
+  if (n_slots < 0 || n_experts < 0 || top_k < 1) return MLG_ERR_INVALID_ARG;
+  const mlg_status shape = check_shapes(k_in, max_rank, n_out);
+  if (shape != MLG_OK) return shape;
+  return gather_dispatch(x, indices, row_adapter, a_table, b_table, scale_table, base_out,
+                         n_slots, k_in, max_rank, n_out, top_k, n_experts, n_experts, 0, stream);
+}
+
+extern "C" mlg_status mlg_gather_bgmv_multi(const mlg_bf16 *x, const int32_t *indices,
+                                            const int32_t *row_adapter, const uint64_t *a_table,
+                                            const uint64_t *b_table, const float *scale_table,
+                                            mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
+                                            int32_t max_rank, int32_t n_out, int32_t top_k,
+                                            int32_t n_experts, int32_t n_adapters, void *stream) {
+  using namespace mlg;
+  if (n_slots < 0 || n_experts < 0 || n_adapters < 1 || top_k < 1) return MLG_ERR_INVALID_ARG;
+  const int64_t cells = static_cast<int64_t>(n_experts) * n_adapters;
+  if (cells > (1 << 30)) return MLG_ERR_UNSUPPORTED;
+  const mlg_status shape = check_shapes(k_in, max_rank, n_out);
+  if (shape != MLG_OK) return shape;
+  return gather_dispatch(x, indices, row_adapter, a_table, b_table, scale_table, base_out,
+                         n_slots, k_in, max_rank, n_out, top_k, static_cast<int32_t>(cells),
+                         n_experts, n_adapters, stream);
 }

@@ -60,6 +60,23 @@ mlg_status mlg_build_moe_row_adapter_decode(const int32_t *adapter_slots, size_t
   return MLG_OK;
 }
 
+mlg_status mlg_build_moe_row_adapter_decode_multi(const int32_t *adapter_slots, size_t n_slots,
+                                                  size_t padded_n, int32_t n_adapters,
+                                                  int32_t has_moe_lora, int32_t *out) {
+  if (padded_n > 0 && out == nullptr) return MLG_ERR_INVALID_ARG;
+  if (n_slots > 0 && adapter_slots == nullptr) return MLG_ERR_INVALID_ARG;
+  if (n_adapters < 1) return MLG_ERR_INVALID_ARG;
+  const size_t real = n_slots < padded_n ? n_slots : padded_n;
+  if (has_moe_lora) {  // a slot without a table set refuses the batch, nothing written
+    for (size_t i = 0; i < real; ++i)
+      if (adapter_slots[i] >= n_adapters) return MLG_ERR_REFUSE;
+  }
+  for (size_t i = 0; i < real; ++i)
+    out[i] = (has_moe_lora && adapter_slots[i] >= 0) ? adapter_slots[i] : -1;
+  for (size_t i = real; i < padded_n; ++i) out[i] = -1;  // padding rows never fold
+  return MLG_OK;
+}
+
 mlg_status mlg_build_moe_row_adapter_host(const int32_t *cu_seqlens, size_t n_cu,
                                           const int32_t *adapter_slots, size_t n_slots,
                                           int32_t *out, size_t cap, size_t *total_out) {

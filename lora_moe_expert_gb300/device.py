@@ -30,6 +30,15 @@ def _bits_tensor(a: np.ndarray, device) -> torch.Tensor:
         torch.bfloat16)
 
 
+def pad_tables(a, b, s, length: int):
+    """Extend packed tables with zero cells to `length` entries."""
+    pad = length - a.size
+    if pad < 0:
+        raise ValueError(f"tables of {a.size} cells exceed {length}")
+    return (np.concatenate([a, np.zeros(pad, a.dtype)]), np.concatenate([b, np.zeros(pad, b.dtype)]),
+            np.concatenate([s, np.zeros(pad, s.dtype)]))
+
+
 class ExpertPool:
     """All expert pairs of a workload in one allocation, each 256-byte aligned."""
 
@@ -64,6 +73,8 @@ class FoldProblem:
         self.pool = pool or ExpertPool(w.experts, self.device)
         a, b, s = mlg.mlg_pack_expert_tables(self.pool.ids, self.pool.a_addr, self.pool.b_addr,
                                              self.pool.scale)
+        if w.n_adapters:  # slot-major sets of n_experts_model cells; trailing holes are zero
+            a, b, s = pad_tables(a, b, s, w.n_adapters * w.n_experts_model)
         self.n_experts = int(a.size)
         self.a_table = torch.empty(self.n_experts, dtype=torch.int64, device=self.device)
         self.b_table = torch.empty(self.n_experts, dtype=torch.int64, device=self.device)
@@ -82,8 +93,12 @@ class FoldProblem:
         self.row_adapter = None
         if w.kind == "gather":
             self.indices = _dev(w.indices.astype(np.int32), self.device)
-            self.row_map_host = mlg.mlg_build_moe_row_adapter_decode(
-                w.adapter_slots, w.padded_n, w.active, w.has_moe_lora)
+            if w.n_adapters:
+                self.row_map_host = mlg.mlg_build_moe_row_adapter_decode_multi(
+                    w.adapter_slots, w.padded_n, w.n_adapters, w.has_moe_lora)
+            else:
+                self.row_map_host = mlg.mlg_build_moe_row_adapter_decode(
+                    w.adapter_slots, w.padded_n, w.active, w.has_moe_lora)
         elif w.kind == "grouped":
             self.expert_offsets = _dev(w.expert_offsets.astype(np.int32), self.device)
             self.src = _dev(w.src.astype(np.int32), self.device)
@@ -106,7 +121,12 @@ class FoldProblem:
         runs the per-row x form over all rows."""
         w = self.w
         s = stream if stream is not None else self._stream()
-        if w.kind == "gather":
+        if w.kind == "gather" and w.n_adapters:
+            mlg.mlg_gather_bgmv_multi(self.x, self.indices, self.row_adapter, self.a_table,
+                                      self.b_table, self.scale_table, self.base, w.rows, w.k_in,
+                                      w.max_rank, w.n_out, w.top_k, w.n_experts_model,
+                                      w.n_adapters, stream=s)
+        elif w.kind == "gather":
             mlg.mlg_gather_bgmv(self.x, self.indices, self.row_adapter, self.a_table,
                                 self.b_table, self.scale_table, self.base, w.rows, w.k_in,
                                 w.max_rank, w.n_out, w.top_k, self.n_experts, stream=s)

@@ -23,6 +23,15 @@ def oracle_reference(w, o=None, row_offset=None, row_end=None):
     """(ref fp64, folded bool, keepalive) for the whole workload."""
     o = o or oracle.get()
     he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
+    if w.n_adapters:
+        at, bt, st = he.tables(o, length=w.n_adapters * w.n_experts_model)
+        status, ra = o.build_moe_row_adapter_decode_multi(w.adapter_slots, w.padded_n,
+                                                          w.n_adapters, w.has_moe_lora)
+        assert status == 0, status
+        ref, folded = o.gather_fold_multi(w.x, w.indices, ra, at, bt, st, w.base, w.k_in,
+                                          w.max_rank, w.n_out, w.top_k, w.n_experts_model,
+                                          w.n_adapters)
+        return ref, folded, (he, at.size)
     at, bt, st = he.tables(o)
     if w.kind == "gather":
         ra = o.build_moe_row_adapter_decode(w.adapter_slots, w.padded_n, w.active,

@@ -86,6 +86,17 @@ def test_gather_exact(shape, path):
         mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
 
 
+@pytest.mark.parametrize("path", [0, 1, 2])
+def test_gather_multi_exact(path):
+    w = integerize(synth.custom_gather_multi(45, 40, 4, 32, 256, 264, 16, 4, adapted_frac=0.8,
+                                             base_frac=0.2, bad_ids=2), 15)
+    try:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, path)
+        _check_exact(w, lambda prob: prob.run())
+    finally:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+
+
 def test_grouped_exact():
     w = integerize(synth.custom_grouped(31, [120, 70, 90], 4, 10, 192, 320, 32, cap=100,
                                         adapted_frac=0.7, stream_base=[0, 1, 0]), 12)

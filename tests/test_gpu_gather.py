@@ -254,3 +254,53 @@ def test_resident_kernel_rejects_other_shapes():
     finally:
         mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
     assert np.array_equal(prob.base_bits(), w.base)
+
+
+# ------------------------------------------------ multi-adapter tables
+MULTI_SHAPES = [
+    # (tokens, top_k, experts, k_in, n_out, rank, adapters, adapted, base_frac, bad_ids)
+    (24, 4, 32, 256, 512, 16, 4, 0.8, 0.2, 2),
+    (40, 4, 20, 192, 264, 32, 3, 0.7, 0.1, 1),
+    (96, 6, 64, 1024, 512, 64, 3, 0.6, 0.15, 2),
+    (32, 2, 8, 128, 96, 8, 5, 1.0, 0.0, 0),
+    (7, 3, 16, 64, 64, 16, 2, 0.5, 0.3, 1),
+]
+
+
+@pytest.mark.parametrize("path", [0, 1, 2])
+@pytest.mark.parametrize("shape", MULTI_SHAPES, ids=lambda s: "x".join(map(str, s[:7])))
+def test_gather_multi(shape, path):
+    T, K, E, k_in, n_out, r, S, adapted, bf, bad = shape
+    w = synth.custom_gather_multi(500 + T, T, K, E, k_in, n_out, r, S, adapted_frac=adapted,
+                                  base_frac=bf, bad_ids=bad)
+    if path == 1 and (r not in (16, 32) or S * E > 152):
+        pytest.skip("the resident-pair kernel takes rank 16 / 32 and one cell per SM")
+    try:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, path)
+        _, stats, folded = _run_and_check(w)
+    finally:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+    assert 0 < folded.sum()
+
+
+def test_decode_down_multi_full():
+    w = synth.decode_down_multi()
+    _, stats, folded = _run_and_check(w)
+    assert folded.all()
+
+
+def test_multi_one_adapter_matches_single_bits():
+    """One installed set: the multi-adapter call gives the single-set call's bits."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_gather(77, 48, 4, 24, 256, 320, 16, adapted_frac=0.8, base_frac=0.2,
+                            bad_ids=2)
+    single = FoldProblem(w)
+    single.run()
+    torch.cuda.synchronize()
+    multi = FoldProblem(w)
+    mlg.mlg_gather_bgmv_multi(multi.x, multi.indices, multi.row_adapter, multi.a_table,
+                              multi.b_table, multi.scale_table, multi.base, w.rows, w.k_in,
+                              w.max_rank, w.n_out, w.top_k, multi.n_experts, 1)
+    torch.cuda.synchronize()
+    assert np.array_equal(multi.base_bits(), single.base_bits())

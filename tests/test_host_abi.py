@@ -103,6 +103,38 @@ def test_decode_map_brute_force(L, o):
                         assert np.array_equal(got, exp), (slots, padded, active, has)
 
 
+def test_decode_map_multi_brute_force(L, o):
+    vals = [-2, -1, 0, 1, 2, 3]
+    for n in range(0, 4):
+        for slots in itertools.product(vals, repeat=n):
+            for padded in range(0, 5):
+                for n_adapters in (1, 2, 3):
+                    for has in (False, True):
+                        st, exp = o.build_moe_row_adapter_decode_multi(list(slots), padded,
+                                                                       n_adapters, has)
+                        if st == 0:
+                            got = mlg.mlg_build_moe_row_adapter_decode_multi(
+                                list(slots), padded, n_adapters, has)
+                            assert np.array_equal(got, exp), (slots, padded, n_adapters, has)
+                        else:
+                            with pytest.raises(mlg.MlgError) as ei:
+                                mlg.mlg_build_moe_row_adapter_decode_multi(list(slots), padded,
+                                                                           n_adapters, has)
+                            assert ei.value.status == st == mlg.MLG_ERR_REFUSE
+    with pytest.raises(mlg.MlgError) as ei:
+        mlg.mlg_build_moe_row_adapter_decode_multi([0], 1, 0, True)
+    assert ei.value.status == mlg.MLG_ERR_INVALID_ARG
+
+
+def test_decode_map_multi_refusal_writes_nothing(L):
+    import ctypes
+    slots = np.array([0, 5, 1], np.int32)
+    out = np.full(4, 77, np.int32)
+    st = L.mlg_build_moe_row_adapter_decode_multi(slots.ctypes.data_as(ctypes.c_void_p), 3, 4, 2,
+                                                  1, out.ctypes.data_as(ctypes.c_void_p))
+    assert st == mlg.MLG_ERR_REFUSE and np.all(out == 77)
+
+
 def test_host_map_fixtures(L):
     for cu, slots, exp in golden_io.host_map_cases():
         if exp is None:
@@ -246,6 +278,24 @@ def test_fold_validation_on_host(L):
     assert gather(base_out=p + 2) == mlg.MLG_ERR_UNSUPPORTED
     assert gather(n_slots=0) == mlg.MLG_OK  # no-op, nothing launched
     assert gather(n_experts=0) == mlg.MLG_OK
+
+    def multi(**kw):
+        args = {**ok, "n_adapters": 3, **kw}
+        return L.mlg_gather_bgmv_multi(args["x"], args["indices"], args["row_adapter"],
+                                       args["a_table"], args["b_table"], args["scale_table"],
+                                       args["base_out"], args["n_slots"], args["k_in"],
+                                       args["max_rank"], args["n_out"], args["top_k"],
+                                       args["n_experts"], args["n_adapters"], 0)
+
+    assert multi(n_adapters=0) == mlg.MLG_ERR_INVALID_ARG
+    assert multi(n_adapters=-1) == mlg.MLG_ERR_INVALID_ARG
+    assert multi(n_experts=1 << 20, n_adapters=1 << 11) == mlg.MLG_ERR_UNSUPPORTED
+    assert multi(top_k=0) == mlg.MLG_ERR_INVALID_ARG
+    assert multi(row_adapter=None) == mlg.MLG_ERR_INVALID_ARG
+    assert multi(k_in=12) == mlg.MLG_ERR_UNSUPPORTED
+    assert multi(x=p + 8) == mlg.MLG_ERR_UNSUPPORTED
+    assert multi(n_slots=0) == mlg.MLG_OK
+    assert multi(n_experts=0) == mlg.MLG_OK
 
     def grouped(**kw):
         args = {**ok, "expert_offsets": p, "src": p, "row_offset": 0, "row_end": 100, **kw}

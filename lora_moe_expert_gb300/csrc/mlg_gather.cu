@@ -60,6 +60,7 @@ struct GatherParams {
   uint16_t *base_out;
   int32_t n_slots, k_in, rank, n_out, top_k, n_experts;  // n_experts: table cells
   int32_t e_model, n_adapters;  // multi-adapter tables (n_adapters > 0): cell = slot * e_model + id
+  int32_t hit_compact;          // units: only cells with a folding row (routing read first)
   int32_t ns2;            // n slices per cluster rank (independent CTAs, full shrink each)
   int32_t ks, ns;         // k columns per cluster rank, n columns per CTA
   int32_t rg;             // rows per pass (16 or 32)
@@ -249,8 +250,21 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
 
   // Units are (expert, n slice) pairs over the experts whose cells fold
   // (tables are never written by the preceding kernel: read before the wait),
-  // so no cluster spends a round on an expert that folds nothing.
+  // so no cluster spends a round on an expert that folds nothing.  With
+  // hit_compact (sparse tables: many cells, few rows each) the routing is
+  // read first and only cells with a folding row become units, so no pair is
+  // loaded that no row of this batch needs.
   const bool compact = p.n_experts <= kMaxCompact;
+  int *s_hist = reinterpret_cast<int *>(smem + p.off_p);  // counts; free until a shrink
+  const int no_idx[kScanPer] = {};
+  const bool hits = compact && p.hit_compact;
+  if (hits) {
+    griddep_wait();
+    waited = true;
+    for (int i = tid; i < p.n_experts; i += kThreads) s_hist[i] = 0;
+    __syncthreads();
+    scan_rows(p, -1, 0, 0, no_idx, no_idx, false, s_rows, s_cnt, s_hist);
+  }
   int n_fold = p.n_experts;
   if (compact) {
     n_fold = 0;
@@ -260,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
       if (ex < p.n_experts) {
         const uint64_t a = __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + ex);
         const uint64_t bb = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ex);
-        f = a != 0 && bb != 0 && ((a | bb) & 15u) == 0;
+        f = a != 0 && bb != 0 && ((a | bb) & 15u) == 0 && (!hits || s_hist[ex] > 0);
       }
       const unsigned m = __ballot_sync(0xffffffffu, f);
       if (lane == 0) s_cnt[0][warp] = __popc(m);
@@ -283,8 +297,6 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
   // sides decide from the same per-expert row counts, read after the wait.
   const int ncl = static_cast<int>(ncluster_x());
   const int n_helpers = (compact && p.ns2 == 1 && n_units < ncl) ? ncl - n_units : 0;
-  int *s_hist = reinterpret_cast<int *>(smem + p.off_p);  // counts; free until a shrink
-  const int no_idx[kScanPer] = {};
   for (int unit = static_cast<int>(cluster_id_x()); unit < n_units + n_helpers; unit += ncl) {
     const bool help = unit >= n_units;
     int e = help ? -1 : (compact ? s_ex[unit / p.ns2] : unit / p.ns2);
@@ -310,6 +322,30 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
     const float scale = __ldg(p.scale_table + e);
     if (a_addr == 0 || b_addr == 0 || ((a_addr | b_addr) & 15u) != 0)
       continue;  // the expert folds nothing (uniform in the cluster)
+    if (warp == 1 && lane == 0 && !help && unit + ncl < n_units) {
+      // This CTA's slices of the next unit's pair, into L2 while this one runs.
+      const int u2 = unit + ncl;
+      const int e2 = compact ? s_ex[u2 / p.ns2] : u2 / p.ns2;
+      const uint64_t a2 = __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + e2);
+      const uint64_t b2 = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + e2);
+      const int n2 = ((u2 % p.ns2) * static_cast<int>(cs) + static_cast<int>(q)) * p.ns;
+      const int nsv2 = max(0, min(p.ns, p.n_out - n2));
+      if (a2 != 0 && b2 != 0 && ((a2 | b2) & 15u) == 0) {
+        const uint8_t *A2 = reinterpret_cast<const uint8_t *>(a2);
+        if (ksv > 0) {
+          if (ksv == p.k_in) {  // whole rows: one contiguous run
+            for (uint32_t o = 0; o < static_cast<uint32_t>(r * p.k_in * 2); o += 8192)
+              prefetch_l2(A2 + o, min(8192u, static_cast<uint32_t>(r * p.k_in * 2) - o));
+          } else {
+            for (int j = 0; j < r; ++j)
+              prefetch_l2(A2 + (static_cast<size_t>(j) * p.k_in + k0) * 2, ksv * 2u);
+          }
+        }
+        const uint8_t *B2 = reinterpret_cast<const uint8_t *>(b2) + static_cast<size_t>(n2) * r * 2;
+        const uint32_t bb = static_cast<uint32_t>(nsv2 * r * 2);
+        for (uint32_t o = 0; o < bb; o += 8192) prefetch_l2(B2 + o, min(8192u, bb - o));
+      }
+    }
     fence_proxy_async_smem();  // earlier generic accesses before new async writes
     __syncthreads();
     if (warp == 0 && !bad) {  // A_e k slice: one bulk copy per rank row
@@ -743,6 +779,9 @@ mlg_status gather_dispatch(const mlg_bf16 *x, const int32_t *indices, const int3
   p.n_experts = n_experts;
   p.e_model = e_model;
   p.n_adapters = n_adapters;
+  // Multi-adapter tables are sparse in a batch (a cell is one adapter's
+  // expert): read the routing first and give units only to cells it hits.
+  p.hit_compact = n_adapters > 0 ? 1 : 0;
   const int rp = static_cast<int>(round_up(max_rank, 16));
   // Rows per pass: decode batches spread ~n_slots / n_experts rows per expert.
   p.rg = (n_slots <= 16 * n_experts) ? 16 : 32;

@@ -53,6 +53,7 @@ constexpr int kScanChunk = kScanPer * kThreads;
 constexpr int kSpecRows = 32;    // rows of the speculative scan kept for L2 prefetch
 constexpr int kMaxCtas = 160;    // owner + helper CTAs (and table entries) at most
 constexpr int kSplitRows = 6;    // an expert with more folding rows than this gets a helper
+constexpr int kMaxUnits = 8;     // cells one CTA takes in the multi-adapter form
 
 static __device__ uint32_t g_decode_errors;
 
@@ -305,7 +306,12 @@ __device__ __forceinline__ void assign_helper(const int *s_hist, int n_experts, 
   if (lane == 0) *s_out = v;
 }
 
-template <int RP>  // max_rank: 16 or 32
+// MULTI = false: one CTA per table entry, its pair requested before the grid
+// dependency wait (plus helper CTAs for heavy experts).  MULTI = true (the
+// multi-adapter tables, where a batch hits few of many cells): the routing
+// is read first, and the cells it hits are dealt round-robin to the CTAs,
+// each folding its cells one after another.
+template <int RP, bool MULTI>  // max_rank: 16 or 32
 __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[2];  // 0: the pair, 1: x rows
@@ -314,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
   __shared__ int s_cnt[kScanPer][kWarps];
   __shared__ int s_hist[kMaxCtas];   // folding rows per expert
   __shared__ int s_role;
+  __shared__ int s_units[kMaxUnits];  // MULTI: this CTA's cells
 
   constexpr int MT = RP / 16;   // rank m-tiles of the shrink
   constexpr int WPL = RP / 8;   // rank words (bf16 pairs) per lane in the expand
@@ -353,9 +360,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
 
   // Owner CTA e folds expert e; helper CTA h (blockIdx >= n_experts) folds the
   // second half of the rows of the h-th heavy expert, whose owner folds the first.
-  const bool helper = static_cast<int>(blockIdx.x) >= p.n_experts;
+  const bool helper = !MULTI && static_cast<int>(blockIdx.x) >= p.n_experts;
   const int who = helper ? static_cast<int>(blockIdx.x) - p.n_experts : static_cast<int>(blockIdx.x);
-  const int n_helpers = static_cast<int>(gridDim.x) - p.n_experts;
+  const int n_helpers = MULTI ? 0 : static_cast<int>(gridDim.x) - p.n_experts;
   const bool spec = p.spec_mode != 1;
   int e = helper ? -1 : who;
   int total = 0;
@@ -384,264 +391,331 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
   };
   auto spec_target = [&](int ex) { return p.spec_mode == 2 ? (ex + 1) % p.n_experts : ex; };
 
-  // ---- before the wait: the pair, and a speculative row list (L2 loads only)
-  if (spec) {
-    total = scan_expert_rows(p, helper ? -1 : spec_target(e), 0, kSpecRows, s_spec, s_cnt, no_idx,
-                             no_idx, false, s_hist);
-    if (helper) {
-      // (spec_mode 2: a different heavy expert, so that the check after the wait fails)
-      assign_helper(s_hist, p.n_experts, n_helpers + 1, true, p.spec_mode == 2 ? who + 1 : who,
-                    &s_role);
-      __syncthreads();
-      e = s_role;
-      if (e >= 0)
-        total = scan_expert_rows(p, spec_target(e), 0, kSpecRows, s_spec, s_cnt, no_idx, no_idx,
-                                 false, nullptr);
-    }
-  }
-  int spec_role = 0;  // owner: 1 if the speculative counts give it a helper
-  if (spec && !helper) {
-    assign_helper(s_hist, p.n_experts, n_helpers, false, who, &s_role);
-    __syncthreads();
-    spec_role = s_role;
-  }
-  if (e >= 0) pair = request_pair(e);
-  // Rows of a split expert: the owner folds ranks [0, half), the helper
-  // [half, total), half = ceil(total / 2); passes of up to 8 rows each.
-  const bool spec_split = helper || spec_role == 1;
-  const int spec_g0 = helper ? (total + 1) / 2 : 0;
-  const int spec_end = (spec_split && !helper) ? (total + 1) / 2 : total;
-  int n_spec = (spec && pair && spec_g0 < kSpecRows - kRows)
-                   ? max(0, min(kRows, spec_end - spec_g0)) : 0;
-  if (warp == 1 && lane < n_spec) {
-    const int row = s_spec[spec_g0 + lane];
-    prefetch_l2(p.x + static_cast<size_t>(row / p.top_k) * p.k_in, row_bytes_x);
-    prefetch_l2(p.base_out + static_cast<size_t>(row) * p.n_out, static_cast<uint32_t>(p.n_out) * 2u);
-  }
-  for (int i = tid; i < kMaxCtas; i += kThreads) s_hist[i] = 0;
-  // The pair lands while the preceding kernel runs; B_e into its bank-spread
-  // row slots.
-  bool have_pair = false;
-  if (pair) {  // one thread polls, pausing; the others sleep in the barrier
-    const bool t = tid == 0 && !mbar_wait_bounded_sleep(bar_w, ph_w, 128);
-    ph_w ^= 1u;
-    have_pair = true;
-    if (__syncthreads_or(t)) {
-      if (tid == 0) record_error(kErrWaitTimeout);
-      bad = true;
-    } else {
-      permute_b<RP>(smem + p.off_b, p.n_out);
-    }
-  }
-  __syncthreads();
-  griddep_wait();  // routing, x and base_out may be written by the preceding kernel
-
-  // ---- after the wait: the speculative first pass's x and base_out rows, the
-  // fresh scan's loads and its base_out loads are all in flight together.
+  // State of the passes over one expert's rows (set by each form below).
   uint4 base_v[kMaxBlocks][2];
   int my_row[2] = {-1, -1};
-  if (n_spec > 0) request_x(p, warp, lane, n_spec, row_bytes_x, bad, s_spec + spec_g0, sX, bar_x);
-  int idx0[kScanPer], ra0[kScanPer];
-  scan_load(p, 0, idx0, ra0);
-  if (n_spec > 0) request_base(p, warp, g, c, n_spec, s_spec + spec_g0, base_v, my_row);
-  int fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, idx0, ra0, true, s_hist);
-  assign_helper(s_hist, p.n_experts, n_helpers, helper, who, &s_role);
-  __syncthreads();
-  const int role = s_role;  // helper: its expert; owner: 1 if it has a helper
-  bool timed_out = false;
-  if (helper && role != e) {  // the speculation picked another expert (or none)
-    if (n_spec > 0) {
-      timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
+  bool have_pair = false;
+  bool issued = false;  // the next pass's x copies and base_out loads are in flight
+  int list0 = 0;        // rank of s_rows[0] in the row list
+  int g_begin = 0, g_end = 0;
+
+  // Fold rows [g_begin, g_end) of expert e's row list, kRows per pass.
+  auto run_passes = [&]() {
+    bool timed_out = false;
+    for (int g0 = g_begin; g0 < g_end && !bad; g0 += kRows) {
+      if (g0 + kRows > list0 + kSpecRows) {  // this pass's rows are past the list
+        scan_expert_rows(p, e, g0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false, nullptr);
+        list0 = g0;
+      }
+      const int *rows = s_rows + (g0 - list0);
+      const int n_g = min(kRows, g_end - g0);
+      if (!issued) {
+        request_x(p, warp, lane, n_g, row_bytes_x, bad, rows, sX, bar_x);
+        request_base(p, warp, g, c, n_g, rows, base_v, my_row);
+      }
+      issued = false;
+      timed_out = false;
+      if (!have_pair) {  // the pair lands; B_e into its bank-spread row slots
+        timed_out = tid == 0 && !mbar_wait_bounded(bar_w, ph_w);
+        ph_w ^= 1u;
+        have_pair = true;
+        if (__syncthreads_or(timed_out)) {
+          if (tid == 0) record_error(kErrWaitTimeout);
+          bad = true;
+          break;
+        }
+        permute_b<RP>(smem + p.off_b, p.n_out);
+      }
+      // One thread polls; the barrier passes what it observed to the others.
+      timed_out = tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
       ph_x ^= 1u;
+      if (__syncthreads_or(timed_out)) {  // (also orders the permuted B_e before its reads)
+        if (tid == 0) record_error(kErrWaitTimeout);
+        bad = true;
+        break;
+      }
+
+      // ---- shrink: h[row][j] = sum_k x[row][k] A_e[j][k], k split over warps
+      // Lane column c feeds physical k = 8c .. 8c+7 of every 32-wide k block
+      // to both operands, so the contraction covers every k once.
+      float acc[MT][4];
+  #pragma unroll
+      for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+      for (int kb = warp; kb < kblocks; kb += kWarps) {
+        const uint32_t kbyte = (kb * 32 + 8 * c) * 2;
+        const uint4 sx = *reinterpret_cast<const uint4 *>(sX + g * p.stride_a + kbyte);
+  #pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint4 pa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g) * p.stride_a + kbyte);
+          const uint4 qa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g + 8) * p.stride_a + kbyte);
+          mma_bf16_16816(acc[mt], pa.x, qa.x, pa.y, qa.y, sx.x, sx.y);
+          mma_bf16_16816(acc[mt], pa.z, qa.z, pa.w, qa.w, sx.z, sx.w);
+        }
+      }
+      // acc[mt] = (j mt*16+g, row 2c), (j, row 2c+1), (j+8, row 2c), (j+8, row 2c+1)
+      float *part = sP + warp * (kRows * PS);
+  #pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int j = mt * 16 + g, row = 2 * c;
+        part[row * PS + j] = acc[mt][0];
+        part[(row + 1) * PS + j] = acc[mt][1];
+        part[row * PS + j + 8] = acc[mt][2];
+        part[(row + 1) * PS + j + 8] = acc[mt][3];
+      }
+      __syncthreads();
+      // The next pass of this CTA (its rows already in s_rows): its x rows are
+      // requested now that sX is free, its base_out rows as the quads of this
+      // pass retire, so neither round trip is exposed.
+      const int g1 = g0 + kRows;
+      const bool pre = g1 < g_end && g1 + kRows <= list0 + kSpecRows;  // CTA-uniform
+      const int *rows1 = s_rows + (g1 - list0);
+      const int n_g1 = pre ? min(kRows, g_end - g1) : 0;
+      int my_row1[2];
+      my_row1[0] = 2 * c < n_g1 ? rows1[2 * c] : -1;
+      my_row1[1] = 2 * c + 1 < n_g1 ? rows1[2 * c + 1] : -1;
+      if (pre) request_x(p, warp, lane, n_g1, row_bytes_x, bad, rows1, sX, bar_x);
+      // Sum the warps' partials in warp order; split h into bf16 hi + lo.
+      if (tid < kRows * RP / 2) {
+        const int row = (2 * tid) / RP, j = (2 * tid) % RP;
+        float h0 = 0.f, h1 = 0.f;
+  #pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          h0 += sP[w * (kRows * PS) + row * PS + j];
+          h1 += sP[w * (kRows * PS) + row * PS + j + 1];
+        }
+        float a0, b0, a1, b1;
+        split_hi_lo(h0, a0, b0);
+        split_hi_lo(h1, a1, b1);
+        *reinterpret_cast<uint32_t *>(sHhi + (row * RP + j) * 2) = pack_bf16x2(a0, a1);
+        *reinterpret_cast<uint32_t *>(sHlo + (row * RP + j) * 2) = pack_bf16x2(b0, b1);
+      }
+      __syncthreads();
+
+      // ---- expand + epilogue (see expand_block).  Lane c takes rank words
+      // c*WPL .. c*WPL+WPL-1 of h and of B_e: k-step st uses word c*WPL + 2st
+      // (logical k 2c, 2c+1) and the next (logical 2c+8, 2c+9).
+      {
+        uint32_t hh[WPL], hl[WPL];
+        load_words<WPL>(hh, sHhi + (g * RP + c * WPL * 2) * 2);
+        load_words<WPL>(hl, sHlo + (g * RP + c * WPL * 2) * 2);
+        // base_v[0] is always the current block: the registers rotate down and
+        // the next pass's loads enter at the top.
+  #pragma unroll
+        for (int i = 0; i < kMaxBlocks; ++i) {
+          const int blk = warp + i * kWarps;
+          uint4 nv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+          if (blk * 64 < p.n_out) {  // warp-uniform
+            float d[4][4];
+            expand_block<RP>(d, sB, hh, hl, blk, p.n_out);
+            const int col = blk * 64 + 8 * g;
+            const bool col_ok = col < p.n_out;
+  #pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              if (my_row[r] >= 0 && col_ok) {
+                const uint4 b = base_v[0][r];
+                uint4 o;
+                o.x = fold_pair(b.x, d[0][r], d[0][r + 2], scale);
+                o.y = fold_pair(b.y, d[1][r], d[1][r + 2], scale);
+                o.z = fold_pair(b.z, d[2][r], d[2][r + 2], scale);
+                o.w = fold_pair(b.w, d[3][r], d[3][r + 2], scale);
+                st_v4(p.base_out + static_cast<size_t>(my_row[r]) * p.n_out + col, o);
+              }
+              if (pre && my_row1[r] >= 0 && col_ok)
+                nv[r] = ld_cg_v4(p.base_out + static_cast<size_t>(my_row1[r]) * p.n_out + col);
+            }
+          }
+  #pragma unroll
+          for (int k = 0; k + 1 < kMaxBlocks; ++k) {
+            base_v[k][0] = base_v[k + 1][0];
+            base_v[k][1] = base_v[k + 1][1];
+          }
+          base_v[kMaxBlocks - 1][0] = nv[0];
+          base_v[kMaxBlocks - 1][1] = nv[1];
+        }
+      }
+      __syncthreads();  // sP / sH are rewritten by the next pass
+      if (pre) {
+        my_row[0] = my_row1[0];
+        my_row[1] = my_row1[1];
+        issued = true;
+      }
     }
+  };
+  auto drain = [&]() {
+    // Let every copy still in flight land before leaving (a pair requested but
+    // never waited for when no pass ran; after a timeout, whatever was issued).
     if (pair && !have_pair) {
-      timed_out = (!bad && tid == 0 && !mbar_wait_bounded(bar_w, ph_w)) || timed_out;
+      const bool t = tid == 0 && !mbar_wait_bounded(bar_w, ph_w);
+      if (t && tid == 0) record_error(kErrWaitTimeout);
+    }
+    if (issued) {
+      const bool t = tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
+      if (t && tid == 0) record_error(kErrWaitTimeout);
+    }
+  };
+
+  if constexpr (!MULTI) {
+    // ---- before the wait: the pair, and a speculative row list (L2 loads only)
+    if (spec) {
+      total = scan_expert_rows(p, helper ? -1 : spec_target(e), 0, kSpecRows, s_spec, s_cnt, no_idx,
+                               no_idx, false, s_hist);
+      if (helper) {
+        // (spec_mode 2: a different heavy expert, so that the check after the wait fails)
+        assign_helper(s_hist, p.n_experts, n_helpers + 1, true, p.spec_mode == 2 ? who + 1 : who,
+                      &s_role);
+        __syncthreads();
+        e = s_role;
+        if (e >= 0)
+          total = scan_expert_rows(p, spec_target(e), 0, kSpecRows, s_spec, s_cnt, no_idx, no_idx,
+                                   false, nullptr);
+      }
+    }
+    int spec_role = 0;  // owner: 1 if the speculative counts give it a helper
+    if (spec && !helper) {
+      assign_helper(s_hist, p.n_experts, n_helpers, false, who, &s_role);
+      __syncthreads();
+      spec_role = s_role;
+    }
+    if (e >= 0) pair = request_pair(e);
+    // Rows of a split expert: the owner folds ranks [0, half), the helper
+    // [half, total), half = ceil(total / 2); passes of up to 8 rows each.
+    const bool spec_split = helper || spec_role == 1;
+    const int spec_g0 = helper ? (total + 1) / 2 : 0;
+    const int spec_end = (spec_split && !helper) ? (total + 1) / 2 : total;
+    int n_spec = (spec && pair && spec_g0 < kSpecRows - kRows)
+                     ? max(0, min(kRows, spec_end - spec_g0)) : 0;
+    if (warp == 1 && lane < n_spec) {
+      const int row = s_spec[spec_g0 + lane];
+      prefetch_l2(p.x + static_cast<size_t>(row / p.top_k) * p.k_in, row_bytes_x);
+      prefetch_l2(p.base_out + static_cast<size_t>(row) * p.n_out, static_cast<uint32_t>(p.n_out) * 2u);
+    }
+    for (int i = tid; i < kMaxCtas; i += kThreads) s_hist[i] = 0;
+    // The pair lands while the preceding kernel runs; B_e into its bank-spread
+    // row slots.
+    if (pair) {  // one thread polls, pausing; the others sleep in the barrier
+      const bool t = tid == 0 && !mbar_wait_bounded_sleep(bar_w, ph_w, 128);
       ph_w ^= 1u;
+      have_pair = true;
+      if (__syncthreads_or(t)) {
+        if (tid == 0) record_error(kErrWaitTimeout);
+        bad = true;
+      } else {
+        permute_b<RP>(smem + p.off_b, p.n_out);
+      }
     }
-    have_pair = false;
-    if (__syncthreads_or(timed_out)) {
-      if (!bad && tid == 0) record_error(kErrWaitTimeout);
-      bad = true;
-    }
-    n_spec = 0;
-    my_row[0] = my_row[1] = -1;
-    e = role;
-    pair = false;
-    if (e >= 0 && !bad) {
-      fence_proxy_async_smem();  // the old pair's buffers were read by no one; order anyway
-      pair = request_pair(e);
-      if (pair) fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false, nullptr);
-    }
-  } else if (n_spec > 0) {
-    // The speculative rows stand if the fresh scan agrees.
-    // (equal totals and roles give the same first pass [spec_g0, spec_g0 + n_spec))
-    bool differ = tid == 0 && (fresh != total || (!helper && role != spec_role));
-    if (tid < n_spec && s_rows[spec_g0 + tid] != s_spec[spec_g0 + tid]) differ = true;
-    if (__syncthreads_or(differ)) {  // let the copies of the stale rows land first
-      timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
-      ph_x ^= 1u;
+    __syncthreads();
+    griddep_wait();  // routing, x and base_out may be written by the preceding kernel
+
+    // ---- after the wait: the speculative first pass's x and base_out rows, the
+    // fresh scan's loads and its base_out loads are all in flight together.
+    if (n_spec > 0) request_x(p, warp, lane, n_spec, row_bytes_x, bad, s_spec + spec_g0, sX, bar_x);
+    int idx0[kScanPer], ra0[kScanPer];
+    scan_load(p, 0, idx0, ra0);
+    if (n_spec > 0) request_base(p, warp, g, c, n_spec, s_spec + spec_g0, base_v, my_row);
+    int fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, idx0, ra0, true, s_hist);
+    assign_helper(s_hist, p.n_experts, n_helpers, helper, who, &s_role);
+    __syncthreads();
+    const int role = s_role;  // helper: its expert; owner: 1 if it has a helper
+    bool timed_out = false;
+    if (helper && role != e) {  // the speculation picked another expert (or none)
+      if (n_spec > 0) {
+        timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
+        ph_x ^= 1u;
+      }
+      if (pair && !have_pair) {
+        timed_out = (!bad && tid == 0 && !mbar_wait_bounded(bar_w, ph_w)) || timed_out;
+        ph_w ^= 1u;
+      }
+      have_pair = false;
       if (__syncthreads_or(timed_out)) {
         if (!bad && tid == 0) record_error(kErrWaitTimeout);
         bad = true;
       }
       n_spec = 0;
       my_row[0] = my_row[1] = -1;
-    }
-  }
-  total = pair ? fresh : 0;
-  const bool split = helper || role == 1;
-  const int g_begin = helper ? (total + 1) / 2 : 0;
-  const int g_end = (split && !helper) ? (total + 1) / 2 : total;
-  bool issued = n_spec > 0;  // the first pass's x copies and base_out loads are in flight
-  int list0 = 0;             // rank of s_rows[0] in the row list
-
-  for (int g0 = g_begin; g0 < g_end && !bad; g0 += kRows) {
-    if (g0 + kRows > list0 + kSpecRows) {  // this pass's rows are past the list
-      scan_expert_rows(p, e, g0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false, nullptr);
-      list0 = g0;
-    }
-    const int *rows = s_rows + (g0 - list0);
-    const int n_g = min(kRows, g_end - g0);
-    if (!issued) {
-      request_x(p, warp, lane, n_g, row_bytes_x, bad, rows, sX, bar_x);
-      request_base(p, warp, g, c, n_g, rows, base_v, my_row);
-    }
-    issued = false;
-    timed_out = false;
-    if (!have_pair) {  // the pair lands; B_e into its bank-spread row slots
-      timed_out = tid == 0 && !mbar_wait_bounded(bar_w, ph_w);
-      ph_w ^= 1u;
-      have_pair = true;
-      if (__syncthreads_or(timed_out)) {
-        if (tid == 0) record_error(kErrWaitTimeout);
-        bad = true;
-        break;
+      e = role;
+      pair = false;
+      if (e >= 0 && !bad) {
+        fence_proxy_async_smem();  // the old pair's buffers were read by no one; order anyway
+        pair = request_pair(e);
+        if (pair) fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false, nullptr);
       }
-      permute_b<RP>(smem + p.off_b, p.n_out);
-    }
-    // One thread polls; the barrier passes what it observed to the others.
-    timed_out = tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
-    ph_x ^= 1u;
-    if (__syncthreads_or(timed_out)) {  // (also orders the permuted B_e before its reads)
-      if (tid == 0) record_error(kErrWaitTimeout);
-      bad = true;
-      break;
-    }
-
-    // ---- shrink: h[row][j] = sum_k x[row][k] A_e[j][k], k split over warps
-    // Lane column c feeds physical k = 8c .. 8c+7 of every 32-wide k block
-    // to both operands, so the contraction covers every k once.
-    float acc[MT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-    for (int kb = warp; kb < kblocks; kb += kWarps) {
-      const uint32_t kbyte = (kb * 32 + 8 * c) * 2;
-      const uint4 sx = *reinterpret_cast<const uint4 *>(sX + g * p.stride_a + kbyte);
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const uint4 pa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g) * p.stride_a + kbyte);
-        const uint4 qa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g + 8) * p.stride_a + kbyte);
-        mma_bf16_16816(acc[mt], pa.x, qa.x, pa.y, qa.y, sx.x, sx.y);
-        mma_bf16_16816(acc[mt], pa.z, qa.z, pa.w, qa.w, sx.z, sx.w);
+    } else if (n_spec > 0) {
+      // The speculative rows stand if the fresh scan agrees.
+      // (equal totals and roles give the same first pass [spec_g0, spec_g0 + n_spec))
+      bool differ = tid == 0 && (fresh != total || (!helper && role != spec_role));
+      if (tid < n_spec && s_rows[spec_g0 + tid] != s_spec[spec_g0 + tid]) differ = true;
+      if (__syncthreads_or(differ)) {  // let the copies of the stale rows land first
+        timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
+        ph_x ^= 1u;
+        if (__syncthreads_or(timed_out)) {
+          if (!bad && tid == 0) record_error(kErrWaitTimeout);
+          bad = true;
+        }
+        n_spec = 0;
+        my_row[0] = my_row[1] = -1;
       }
     }
-    // acc[mt] = (j mt*16+g, row 2c), (j, row 2c+1), (j+8, row 2c), (j+8, row 2c+1)
-    float *part = sP + warp * (kRows * PS);
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      const int j = mt * 16 + g, row = 2 * c;
-      part[row * PS + j] = acc[mt][0];
-      part[(row + 1) * PS + j] = acc[mt][1];
-      part[row * PS + j + 8] = acc[mt][2];
-      part[(row + 1) * PS + j + 8] = acc[mt][3];
-    }
+    total = pair ? fresh : 0;
+    const bool split = helper || role == 1;
+    g_begin = helper ? (total + 1) / 2 : 0;
+    g_end = (split && !helper) ? (total + 1) / 2 : total;
+    issued = n_spec > 0;  // the first pass's x copies and base_out loads are in flight
+    list0 = 0;
+    run_passes();
+    drain();
+  } else {
+    griddep_wait();  // the routing may be written by the preceding kernel
+    // Units: the foldable cells with a folding row in this batch, in cell
+    // order; the one of rank k goes to CTA k mod gridDim.x.  The counts live
+    // in the shrink partials' space, free until the first shrink.
+    int *hist = reinterpret_cast<int *>(smem + p.off_p);
+    for (int i = tid; i < p.n_experts; i += kThreads) hist[i] = 0;
     __syncthreads();
-    // The next pass of this CTA (its rows already in s_rows): its x rows are
-    // requested now that sX is free, its base_out rows as the quads of this
-    // pass retire, so neither round trip is exposed.
-    const int g1 = g0 + kRows;
-    const bool pre = g1 < g_end && g1 + kRows <= list0 + kSpecRows;  // CTA-uniform
-    const int *rows1 = s_rows + (g1 - list0);
-    const int n_g1 = pre ? min(kRows, g_end - g1) : 0;
-    int my_row1[2];
-    my_row1[0] = 2 * c < n_g1 ? rows1[2 * c] : -1;
-    my_row1[1] = 2 * c + 1 < n_g1 ? rows1[2 * c + 1] : -1;
-    if (pre) request_x(p, warp, lane, n_g1, row_bytes_x, bad, rows1, sX, bar_x);
-    // Sum the warps' partials in warp order; split h into bf16 hi + lo.
-    if (tid < kRows * RP / 2) {
-      const int row = (2 * tid) / RP, j = (2 * tid) % RP;
-      float h0 = 0.f, h1 = 0.f;
+    scan_expert_rows(p, -1, 0, 0, s_rows, s_cnt, no_idx, no_idx, false, hist);
+    int n_hit = 0;
+    for (int b = 0; b < p.n_experts; b += kThreads) {
+      const int ex = b + tid;
+      bool f = false;
+      if (ex < p.n_experts && hist[ex] > 0) {
+        const uint64_t a = __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + ex);
+        const uint64_t bb = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ex);
+        f = a != 0 && bb != 0 && ((a | bb) & 15u) == 0;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, f);
+      if (lane == 0) s_cnt[0][warp] = __popc(m);
+      __syncthreads();
+      int before = n_hit;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        h0 += sP[w * (kRows * PS) + row * PS + j];
-        h1 += sP[w * (kRows * PS) + row * PS + j + 1];
+        before += (w < warp) ? s_cnt[0][w] : 0;
+        n_hit += s_cnt[0][w];
       }
-      float a0, b0, a1, b1;
-      split_hi_lo(h0, a0, b0);
-      split_hi_lo(h1, a1, b1);
-      *reinterpret_cast<uint32_t *>(sHhi + (row * RP + j) * 2) = pack_bf16x2(a0, a1);
-      *reinterpret_cast<uint32_t *>(sHlo + (row * RP + j) * 2) = pack_bf16x2(b0, b1);
+      const int rank = before + __popc(m & ((1u << lane) - 1u));
+      const int slot = rank / static_cast<int>(gridDim.x);
+      if (f && rank % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x) && slot < kMaxUnits)
+        s_units[slot] = ex;
+      __syncthreads();
     }
-    __syncthreads();
-
-    // ---- expand + epilogue (see expand_block).  Lane c takes rank words
-    // c*WPL .. c*WPL+WPL-1 of h and of B_e: k-step st uses word c*WPL + 2st
-    // (logical k 2c, 2c+1) and the next (logical 2c+8, 2c+9).
-    {
-      uint32_t hh[WPL], hl[WPL];
-      load_words<WPL>(hh, sHhi + (g * RP + c * WPL * 2) * 2);
-      load_words<WPL>(hl, sHlo + (g * RP + c * WPL * 2) * 2);
-      // base_v[0] is always the current block: the registers rotate down and
-      // the next pass's loads enter at the top.
-#pragma unroll
-      for (int i = 0; i < kMaxBlocks; ++i) {
-        const int blk = warp + i * kWarps;
-        uint4 nv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-        if (blk * 64 < p.n_out) {  // warp-uniform
-          float d[4][4];
-          expand_block<RP>(d, sB, hh, hl, blk, p.n_out);
-          const int col = blk * 64 + 8 * g;
-          const bool col_ok = col < p.n_out;
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            if (my_row[r] >= 0 && col_ok) {
-              const uint4 b = base_v[0][r];
-              uint4 o;
-              o.x = fold_pair(b.x, d[0][r], d[0][r + 2], scale);
-              o.y = fold_pair(b.y, d[1][r], d[1][r + 2], scale);
-              o.z = fold_pair(b.z, d[2][r], d[2][r + 2], scale);
-              o.w = fold_pair(b.w, d[3][r], d[3][r + 2], scale);
-              st_v4(p.base_out + static_cast<size_t>(my_row[r]) * p.n_out + col, o);
-            }
-            if (pre && my_row1[r] >= 0 && col_ok)
-              nv[r] = ld_cg_v4(p.base_out + static_cast<size_t>(my_row1[r]) * p.n_out + col);
-          }
-        }
-#pragma unroll
-        for (int k = 0; k + 1 < kMaxBlocks; ++k) {
-          base_v[k][0] = base_v[k + 1][0];
-          base_v[k][1] = base_v[k + 1][1];
-        }
-        base_v[kMaxBlocks - 1][0] = nv[0];
-        base_v[kMaxBlocks - 1][1] = nv[1];
-      }
+    const int me = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+    const int n_mine = n_hit > me ? min(kMaxUnits, (n_hit - 1 - me) / G + 1) : 0;
+    for (int u = 0; u < n_mine && !bad; ++u) {
+      e = s_units[u];
+      fence_proxy_async_smem();  // the last unit's buffers were read: order before new copies
+      __syncthreads();
+      pair = request_pair(e);
+      have_pair = false;
+      total = pair ? scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false,
+                                      nullptr)
+                   : 0;
+      g_begin = 0;
+      g_end = total;
+      issued = false;
+      list0 = 0;
+      my_row[0] = my_row[1] = -1;
+      run_passes();
+      drain();
     }
-    __syncthreads();  // sP / sH are rewritten by the next pass
-    if (pre) {
-      my_row[0] = my_row1[0];
-      my_row[1] = my_row1[1];
-      issued = true;
-    }
-  }
-  // Let every copy still in flight land before exit (a pair requested but
-  // never waited for when no pass ran; after a timeout, whatever was issued).
-  if (pair && !have_pair) {
-    const bool t = tid == 0 && !mbar_wait_bounded(bar_w, ph_w);
-    if (t && tid == 0) record_error(kErrWaitTimeout);
-  }
-  if (issued) {
-    const bool t = tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
-    if (t && tid == 0) record_error(kErrWaitTimeout);
   }
 }
 
@@ -675,14 +749,14 @@ uint32_t layout(DecodeParams &p, int rp) {
   return p.smem_bytes;
 }
 
-template <int RP>
+template <int RP, bool MULTI>
 cudaError_t launch(const DecodeParams &p, int grid, cudaStream_t stream) {
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
   int dev = 0;
   cudaGetDevice(&dev);
   std::call_once(once[dev & 63], [d = dev & 63] {
-    attr_err[d] = cudaFuncSetAttribute(decode_fold_kernel<RP>,
+    attr_err[d] = cudaFuncSetAttribute(decode_fold_kernel<RP, MULTI>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemTwoPerSm));
   });
@@ -697,7 +771,7 @@ cudaError_t launch(const DecodeParams &p, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_fold_kernel<RP>, p);
+  return cudaLaunchKernelEx(&cfg, decode_fold_kernel<RP, MULTI>, p);
 }
 
 }  // namespace
@@ -729,6 +803,20 @@ bool decode_fold_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t
   return layout(p, max_rank) <= kSmemTwoPerSm;
 }
 
+// The multi-cell form: the same pair limits, two CTAs on every SM, at most
+// kMaxUnits cells per CTA, and the per-cell counts within the shrink
+// partials' space.
+bool decode_multi_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t n_cells) {
+  if (max_rank != 16 && max_rank != 32) return false;
+  if (n_out > kMaxBlocks * kWarps * 64) return false;
+  if (n_cells > kMaxUnits * 2 * sm_count()) return false;
+  if (static_cast<int64_t>(n_cells) * 4 > kWarps * kRows * (max_rank + 4) * 4) return false;
+  DecodeParams p = {};
+  p.k_in = k_in;
+  p.n_out = n_out;
+  return layout(p, max_rank) <= kSmemTwoPerSm;
+}
+
 cudaError_t decode_fold_launch(const uint16_t *x, const int32_t *indices,
                                const int32_t *row_adapter, const uint64_t *a_table,
                                const uint64_t *b_table, const float *scale_table,
@@ -753,8 +841,12 @@ cudaError_t decode_fold_launch(const uint16_t *x, const int32_t *indices,
   p.n_adapters = n_adapters;
   p.spec_mode = g_spec_mode;
   layout(p, max_rank);
+  if (n_adapters > 0) {  // cells dealt to two CTAs per SM
+    const int grid = 2 * sm_count();
+    return max_rank == 16 ? launch<16, true>(p, grid, stream) : launch<32, true>(p, grid, stream);
+  }
   const int grid = decode_grid();  // owners, then helpers for experts with many rows
-  return max_rank == 16 ? launch<16>(p, grid, stream) : launch<32>(p, grid, stream);
+  return max_rank == 16 ? launch<16, false>(p, grid, stream) : launch<32, false>(p, grid, stream);
 }
 
 }  // namespace mlg

@@ -755,7 +755,8 @@ mlg_status gather_dispatch(const mlg_bf16 *x, const int32_t *indices, const int3
 
   // Expert pairs that fit half an SM go to the resident-pair kernel.
   const int path = gather_path_override();
-  const bool resident = decode_fold_eligible(k_in, max_rank, n_out, n_experts);
+  const bool resident = n_adapters > 0 ? decode_multi_eligible(k_in, max_rank, n_out, n_experts)
+                                       : decode_fold_eligible(k_in, max_rank, n_out, n_experts);
   if (path == 1 && !resident) return MLG_ERR_UNSUPPORTED;
   if (path != 2 && resident)
     return cuda_status(decode_fold_launch(x, indices, row_adapter, a_table, b_table, scale_table,

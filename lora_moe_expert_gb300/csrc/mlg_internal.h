@@ -38,9 +38,11 @@ int sm_count();  // multiprocessors of the current device (cached per device)
 // n_cells is the table length; with n_adapters > 0 the tables hold
 // n_adapters sets of e_model cells, slot-major, and a row's cell is
 // row_adapter[token] * e_model + indices[row] (n_adapters == 0: the cell is
-// indices[row] and the row map only gates).
+// indices[row] and the row map only gates).  A launch with n_adapters > 0
+// takes the multi-cell form (decode_multi_eligible).
 int gather_path_override();  // 0 auto, 1 resident-pair kernel, 2 cluster kernel
 bool decode_fold_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t n_cells);
+bool decode_multi_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t n_cells);
 cudaError_t decode_fold_launch(const uint16_t *x, const int32_t *indices,
                                const int32_t *row_adapter, const uint64_t *a_table,
                                const uint64_t *b_table, const float *scale_table,

@@ -273,8 +273,8 @@ def test_gather_multi(shape, path):
     T, K, E, k_in, n_out, r, S, adapted, bf, bad = shape
     w = synth.custom_gather_multi(500 + T, T, K, E, k_in, n_out, r, S, adapted_frac=adapted,
                                   base_frac=bf, bad_ids=bad)
-    if path == 1 and (r not in (16, 32) or S * E > 152):
-        pytest.skip("the resident-pair kernel takes rank 16 / 32 and one cell per SM")
+    if path == 1 and r not in (16, 32):
+        pytest.skip("the resident-pair kernel takes rank 16 or 32")
     try:
         mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, path)
         _, stats, folded = _run_and_check(w)

@@ -439,12 +439,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       // Lane column c feeds physical k = 8c .. 8c+7 of every 32-wide k block
       // to both operands, so the contraction covers every k once.
       float acc[MT][4];
-  #pragma unroll
+#pragma unroll
       for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
       for (int kb = warp; kb < kblocks; kb += kWarps) {
         const uint32_t kbyte = (kb * 32 + 8 * c) * 2;
         const uint4 sx = *reinterpret_cast<const uint4 *>(sX + g * p.stride_a + kbyte);
-  #pragma unroll
+#pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const uint4 pa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g) * p.stride_a + kbyte);
           const uint4 qa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g + 8) * p.stride_a + kbyte);
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       }
       // acc[mt] = (j mt*16+g, row 2c), (j, row 2c+1), (j+8, row 2c), (j+8, row 2c+1)
       float *part = sP + warp * (kRows * PS);
-  #pragma unroll
+#pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const int j = mt * 16 + g, row = 2 * c;
         part[row * PS + j] = acc[mt][0];
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       if (tid < kRows * RP / 2) {
         const int row = (2 * tid) / RP, j = (2 * tid) % RP;
         float h0 = 0.f, h1 = 0.f;
-  #pragma unroll
+#pragma unroll
         for (int w = 0; w < kWarps; ++w) {
           h0 += sP[w * (kRows * PS) + row * PS + j];
           h1 += sP[w * (kRows * PS) + row * PS + j + 1];
@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
         load_words<WPL>(hl, sHlo + (g * RP + c * WPL * 2) * 2);
         // base_v[0] is always the current block: the registers rotate down and
         // the next pass's loads enter at the top.
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < kMaxBlocks; ++i) {
           const int blk = warp + i * kWarps;
           uint4 nv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
             expand_block<RP>(d, sB, hh, hl, blk, p.n_out);
             const int col = blk * 64 + 8 * g;
             const bool col_ok = col < p.n_out;
-  #pragma unroll
+#pragma unroll
             for (int r = 0; r < 2; ++r) {
               if (my_row[r] >= 0 && col_ok) {
                 const uint4 b = base_v[0][r];
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
                 nv[r] = ld_cg_v4(p.base_out + static_cast<size_t>(my_row1[r]) * p.n_out + col);
             }
           }
-  #pragma unroll
+#pragma unroll
           for (int k = 0; k + 1 < kMaxBlocks; ++k) {
             base_v[k][0] = base_v[k + 1][0];
             base_v[k][1] = base_v[k + 1][1];

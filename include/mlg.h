@@ -360,7 +360,9 @@ MLG_API mlg_status mlg_read_device_errors(uint32_t *flags_out, int32_t clear);
  *                             the preceding kernel completes and checked after it, 1 = scanned
  *                             after it only, 2 = the early scan reads another expert's rows so
  *                             that every check fails and the rows are requested again (a test
- *                             of that path; results are the same in all three modes)
+ *                             of that path; results are the same in all three modes).  In the
+ *                             multi-adapter form the same modes pick the first cell whose pair
+ *                             loads before the wait (2: another CTA's cell)
  * Errors: INVALID_ARG for an unknown knob or a value out of range. */
 #define MLG_TUNE_GATHER_CLUSTER 1
 #define MLG_TUNE_GROUPED_CTAS 2

@@ -54,6 +54,7 @@ constexpr int kSpecRows = 32;    // rows of the speculative scan kept for L2 pre
 constexpr int kMaxCtas = 160;    // owner + helper CTAs (and table entries) at most
 constexpr int kSplitRows = 6;    // an expert with more folding rows than this gets a helper
 constexpr int kMaxUnits = 8;     // cells one CTA takes in the multi-adapter form
+constexpr int kMaxCells = 1280;  // table cells of the multi-adapter form at most
 
 static __device__ uint32_t g_decode_errors;
 
@@ -308,9 +309,11 @@ __device__ __forceinline__ void assign_helper(const int *s_hist, int n_experts, 
 
 // MULTI = false: one CTA per table entry, its pair requested before the grid
 // dependency wait (plus helper CTAs for heavy experts).  MULTI = true (the
-// multi-adapter tables, where a batch hits few of many cells): the routing
-// is read first, and the cells it hits are dealt round-robin to the CTAs,
-// each folding its cells one after another.
+// multi-adapter tables, where a batch hits few of many cells): the cells the
+// routing hits are dealt round-robin to the CTAs, each folding its cells one
+// after another; the first cell is picked from a speculative (L2-only) read
+// of the routing before the wait, so its pair loads while the preceding
+// kernel runs, and is kept only if the fresh routing deals the same cell.
 template <int RP, bool MULTI>  // max_rank: 16 or 32
 __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -321,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
   __shared__ int s_hist[kMaxCtas];   // folding rows per expert
   __shared__ int s_role;
   __shared__ int s_units[kMaxUnits];  // MULTI: this CTA's cells
+  __shared__ uint32_t s_fold[MULTI ? kMaxCells / 32 : 1];  // MULTI: foldable cells, one bit each
 
   constexpr int MT = RP / 16;   // rank m-tiles of the shrink
   constexpr int WPL = RP / 8;   // rank words (bf16 pairs) per lane in the expand
@@ -665,46 +669,91 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     run_passes();
     drain();
   } else {
-    griddep_wait();  // the routing may be written by the preceding kernel
-    // Units: the foldable cells with a folding row in this batch, in cell
-    // order; the one of rank k goes to CTA k mod gridDim.x.  The counts live
-    // in the shrink partials' space, free until the first shrink.
-    int *hist = reinterpret_cast<int *>(smem + p.off_p);
-    for (int i = tid; i < p.n_experts; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    scan_expert_rows(p, -1, 0, 0, s_rows, s_cnt, no_idx, no_idx, false, hist);
-    int n_hit = 0;
+    // ---- before the wait: which cells fold (the tables are never written by
+    // the preceding kernel), a speculative unit list from an L2-only routing
+    // scan, and the pair of this CTA's first speculative cell.
+    int *hist = reinterpret_cast<int *>(smem + p.off_p);  // free until the first shrink
     for (int b = 0; b < p.n_experts; b += kThreads) {
       const int ex = b + tid;
       bool f = false;
-      if (ex < p.n_experts && hist[ex] > 0) {
+      if (ex < p.n_experts) {
         const uint64_t a = __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + ex);
         const uint64_t bb = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ex);
         f = a != 0 && bb != 0 && ((a | bb) & 15u) == 0;
       }
       const unsigned m = __ballot_sync(0xffffffffu, f);
-      if (lane == 0) s_cnt[0][warp] = __popc(m);
-      __syncthreads();
-      int before = n_hit;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        before += (w < warp) ? s_cnt[0][w] : 0;
-        n_hit += s_cnt[0][w];
-      }
-      const int rank = before + __popc(m & ((1u << lane) - 1u));
-      const int slot = rank / static_cast<int>(gridDim.x);
-      if (f && rank % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x) && slot < kMaxUnits)
-        s_units[slot] = ex;
-      __syncthreads();
+      if (lane == 0) s_fold[(b >> 5) + warp] = m;
     }
-    const int me = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
-    const int n_mine = n_hit > me ? min(kMaxUnits, (n_hit - 1 - me) / G + 1) : 0;
+    // Units: the foldable cells with a folding row, in cell order; the one of
+    // rank k goes to CTA k mod gridDim.x.  Returns this CTA's count.
+    const int G = static_cast<int>(gridDim.x);
+    auto deal_units = [&](int me) -> int {
+      for (int i = tid; i < p.n_experts; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      scan_expert_rows(p, -1, 0, 0, s_rows, s_cnt, no_idx, no_idx, false, hist);
+      int n_hit = 0;
+      for (int b = 0; b < p.n_experts; b += kThreads) {
+        const int ex = b + tid;
+        const bool f = ex < p.n_experts && hist[ex] > 0 && ((s_fold[ex >> 5] >> (ex & 31)) & 1u);
+        const unsigned m = __ballot_sync(0xffffffffu, f);
+        if (lane == 0) s_cnt[0][warp] = __popc(m);
+        __syncthreads();
+        int before = n_hit;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          before += (w < warp) ? s_cnt[0][w] : 0;
+          n_hit += s_cnt[0][w];
+        }
+        const int rank = before + __popc(m & ((1u << lane) - 1u));
+        if (f && rank % G == me && rank / G < kMaxUnits) s_units[rank / G] = ex;
+        __syncthreads();
+      }
+      return n_hit > me ? min(kMaxUnits, (n_hit - 1 - me) / G + 1) : 0;
+    };
+    // (spec_mode 1: no speculation; 2: another CTA's first cell, so that the
+    // check after the wait fails)
+    const int me = static_cast<int>(blockIdx.x);
+    int n_mine = spec ? deal_units(p.spec_mode == 2 ? (me + 1) % G : me) : 0;
+    const int e_spec = n_mine > 0 ? s_units[0] : -1;
+    bool spec_pair = false;
+    if (e_spec >= 0) {
+      spec_pair = request_pair(e_spec);
+      const int ns = scan_expert_rows(p, e_spec, 0, kSpecRows, s_spec, s_cnt, no_idx, no_idx,
+                                      false, nullptr);
+      if (warp == 1 && lane < min(ns, kRows)) {
+        const int row = s_spec[lane];
+        prefetch_l2(p.x + static_cast<size_t>(row / p.top_k) * p.k_in, row_bytes_x);
+        prefetch_l2(p.base_out + static_cast<size_t>(row) * p.n_out,
+                    static_cast<uint32_t>(p.n_out) * 2u);
+      }
+      if (spec_pair) {  // one thread polls, pausing; the others sleep in the barrier
+        const bool t = tid == 0 && !mbar_wait_bounded_sleep(bar_w, ph_w, 128);
+        ph_w ^= 1u;
+        if (__syncthreads_or(t)) {
+          if (tid == 0) record_error(kErrWaitTimeout);
+          bad = true;
+        } else {
+          permute_b<RP>(smem + p.off_b, p.n_out);
+        }
+      }
+    }
+    __syncthreads();
+    griddep_wait();  // the routing, x and base_out may be written by the preceding kernel
+
+    // ---- after the wait: the fresh unit list; the first cell's pair is kept
+    // when the speculation picked it.
+    n_mine = deal_units(me);
     for (int u = 0; u < n_mine && !bad; ++u) {
       e = s_units[u];
-      fence_proxy_async_smem();  // the last unit's buffers were read: order before new copies
-      __syncthreads();
-      pair = request_pair(e);
-      have_pair = false;
+      if (u == 0 && spec_pair && e == e_spec) {
+        pair = true;  // landed and permuted before the wait; scale set by its request
+        have_pair = true;
+      } else {
+        fence_proxy_async_smem();  // the last unit's buffers were read: order before new copies
+        __syncthreads();
+        pair = request_pair(e);
+        have_pair = false;
+      }
       total = pair ? scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false,
                                       nullptr)
                    : 0;
@@ -809,7 +858,7 @@ bool decode_fold_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t
 bool decode_multi_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t n_cells) {
   if (max_rank != 16 && max_rank != 32) return false;
   if (n_out > kMaxBlocks * kWarps * 64) return false;
-  if (n_cells > kMaxUnits * 2 * sm_count()) return false;
+  if (n_cells > kMaxUnits * 2 * sm_count() || n_cells > kMaxCells) return false;
   if (static_cast<int64_t>(n_cells) * 4 > kWarps * kRows * (max_rank + 4) * 4) return false;
   DecodeParams p = {};
   p.k_in = k_in;

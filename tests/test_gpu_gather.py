@@ -194,14 +194,20 @@ def test_resident_and_cluster_kernels(shape, path):
         mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
 
 
+@pytest.mark.parametrize("multi", [False, True], ids=["single", "multi"])
 @pytest.mark.parametrize("mode", [1, 2])
-def test_speculation_modes_give_the_same_bits(mode):
-    """Row lists scanned before the preceding kernel completes are checked
-    after it: with no early scan (1) or an early scan that always disagrees
-    (2, every row requested again) the bits are those of the default mode."""
+def test_speculation_modes_give_the_same_bits(mode, multi):
+    """Row lists (multi-adapter form: first cells) picked before the preceding
+    kernel completes are checked after it: with no early scan (1) or an early
+    scan that always disagrees (2, everything requested again) the bits are
+    those of the default mode."""
     from lora_moe_expert_gb300.device import FoldProblem
 
-    w = synth.custom_gather(21, 48, 8, 64, 768, 1024, 16, adapted_frac=0.9, base_frac=0.2)
+    if multi:
+        w = synth.custom_gather_multi(24, 48, 8, 64, 768, 1024, 16, 3, adapted_frac=0.9,
+                                      base_frac=0.2)
+    else:
+        w = synth.custom_gather(21, 48, 8, 64, 768, 1024, 16, adapted_frac=0.9, base_frac=0.2)
     outs = []
     try:
         for m in (0, mode):
@@ -217,14 +223,18 @@ def test_speculation_modes_give_the_same_bits(mode):
     fh.check_fold(outs[1], w.base, ref, folded)
 
 
-def test_routing_written_by_the_preceding_kernel():
+@pytest.mark.parametrize("multi", [False, True], ids=["single", "multi"])
+def test_routing_written_by_the_preceding_kernel(multi):
     """The routing is rewritten on the stream right before the fold (by a
     kernel the fold may overlap): the fold uses the new routing."""
     import copy
 
     from lora_moe_expert_gb300.device import FoldProblem
 
-    w = synth.custom_gather(22, 64, 8, 128, 768, 2048, 16)
+    if multi:
+        w = synth.custom_gather_multi(25, 64, 8, 128, 768, 2048, 16, 4)
+    else:
+        w = synth.custom_gather(22, 64, 8, 128, 768, 2048, 16)
     w2 = copy.deepcopy(w)
     w2.indices = np.roll(w.indices, 8 * 5).copy()  # another token order
     prob = FoldProblem(w)

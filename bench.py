@@ -514,7 +514,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode_down", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--extra", default="decode_gate_up,prefill_down,prefill_down_xrows,prefill_large,router",
+    ap.add_argument("--extra", default="decode_gate_up,decode_down_multi,prefill_down,prefill_down_xrows,"
+                                       "prefill_large,router",
                     help="other workloads measured in the same run (comma list, or 'none')")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=10.0)

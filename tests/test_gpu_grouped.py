@@ -320,3 +320,33 @@ def test_xrows_negative_src_and_no_row_map():
     folded[neg] = False
     ref[neg] = synth.bf16_to_f32(w.base[neg]).astype(np.float64)
     fh.check_fold(prob.base_bits(), w.base, ref, folded)
+
+
+def test_multi_adapter_prefill_through_cell_sort():
+    """The prefill form of the multi-adapter fold needs no kernel of its own:
+    rows sorted by cell (slot * n_experts + expert) and the grouped fold over
+    the n_adapters * n_experts spans of slot-major tables give the oracle's
+    multi-adapter fold, row for row."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    E, S = 12, 3
+    w = synth.custom_gather_multi(61, 150, 4, E, 256, 320, 32, S, adapted_frac=0.75,
+                                  base_frac=0.2, bad_ids=3)
+    prob = FoldProblem(w)  # x, slot-major tables (S * E cells), per-token slots as the row map
+    slots = w.adapter_slots.astype(np.int64)
+    tok = np.arange(w.rows) // w.top_k
+    idx = w.indices.astype(np.int64)
+    ok = (slots[tok] >= 0) & (idx >= 0) & (idx < E)
+    key = np.where(ok, slots[tok] * E + idx, S * E)  # rows of no cell sort past the table
+    offsets, src = synth.sort_rows_by_expert(key, S * E + 1)
+    sorted_base = torch.from_numpy(w.base[src].view(np.int16)).cuda().view(torch.bfloat16)
+    row_map = torch.from_numpy(w.adapter_slots.astype(np.int32)).cuda()
+    mlg.mlg_grouped_down(prob.x, torch.from_numpy(offsets).cuda(), torch.from_numpy(src).cuda(),
+                         row_map, prob.a_table, prob.b_table, prob.scale_table, sorted_base,
+                         w.k_in, w.max_rank, w.n_out, w.top_k, prob.n_experts, 0, w.rows)
+    torch.cuda.synchronize()
+    got = np.empty_like(w.base)
+    got[src] = sorted_base.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref, folded, _ = fh.oracle_reference(w)
+    assert 0 < folded.sum() < folded.size
+    fh.check_fold(got, w.base, ref, folded)

@@ -402,6 +402,57 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
   bool issued = false;  // the next pass's x copies and base_out loads are in flight
   int list0 = 0;        // rank of s_rows[0] in the row list
   int g_begin = 0, g_end = 0;
+  bool h_ready = false;  // the first pass's h is already split into sHhi / sHlo
+
+  // ---- shrink: h[row][j] = sum_k x[row][k] A_e[j][k] over the pass's x rows
+  // in sX, k split over warps, into the warps' partials.  Lane column c feeds
+  // physical k = 8c .. 8c+7 of every 32-wide k block to both operands, so the
+  // contraction covers every k once.
+  auto shrink_pass = [&]() {
+    float acc[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    for (int kb = warp; kb < kblocks; kb += kWarps) {
+      const uint32_t kbyte = (kb * 32 + 8 * c) * 2;
+      const uint4 sx = *reinterpret_cast<const uint4 *>(sX + g * p.stride_a + kbyte);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const uint4 pa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g) * p.stride_a + kbyte);
+        const uint4 qa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g + 8) * p.stride_a + kbyte);
+        mma_bf16_16816(acc[mt], pa.x, qa.x, pa.y, qa.y, sx.x, sx.y);
+        mma_bf16_16816(acc[mt], pa.z, qa.z, pa.w, qa.w, sx.z, sx.w);
+      }
+    }
+    // acc[mt] = (j mt*16+g, row 2c), (j, row 2c+1), (j+8, row 2c), (j+8, row 2c+1)
+    float *part = sP + warp * (kRows * PS);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int j = mt * 16 + g, row = 2 * c;
+      part[row * PS + j] = acc[mt][0];
+      part[(row + 1) * PS + j] = acc[mt][1];
+      part[row * PS + j + 8] = acc[mt][2];
+      part[(row + 1) * PS + j + 8] = acc[mt][3];
+    }
+    __syncthreads();
+  };
+  // Sum the warps' partials in warp order; split h into bf16 hi + lo.
+  auto split_h = [&]() {
+    if (tid < kRows * RP / 2) {
+      const int row = (2 * tid) / RP, j = (2 * tid) % RP;
+      float h0 = 0.f, h1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        h0 += sP[w * (kRows * PS) + row * PS + j];
+        h1 += sP[w * (kRows * PS) + row * PS + j + 1];
+      }
+      float a0, b0, a1, b1;
+      split_hi_lo(h0, a0, b0);
+      split_hi_lo(h1, a1, b1);
+      *reinterpret_cast<uint32_t *>(sHhi + (row * RP + j) * 2) = pack_bf16x2(a0, a1);
+      *reinterpret_cast<uint32_t *>(sHlo + (row * RP + j) * 2) = pack_bf16x2(b0, b1);
+    }
+    __syncthreads();
+  };
 
   // Fold rows [g_begin, g_end) of expert e's row list, kRows per pass.
   auto run_passes = [&]() {
@@ -430,43 +481,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
         }
         permute_b<RP>(smem + p.off_b, p.n_out);
       }
-      // One thread polls; the barrier passes what it observed to the others.
-      timed_out = tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
-      ph_x ^= 1u;
-      if (__syncthreads_or(timed_out)) {  // (also orders the permuted B_e before its reads)
-        if (tid == 0) record_error(kErrWaitTimeout);
-        bad = true;
-        break;
-      }
-
-      // ---- shrink: h[row][j] = sum_k x[row][k] A_e[j][k], k split over warps
-      // Lane column c feeds physical k = 8c .. 8c+7 of every 32-wide k block
-      // to both operands, so the contraction covers every k once.
-      float acc[MT][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-      for (int kb = warp; kb < kblocks; kb += kWarps) {
-        const uint32_t kbyte = (kb * 32 + 8 * c) * 2;
-        const uint4 sx = *reinterpret_cast<const uint4 *>(sX + g * p.stride_a + kbyte);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const uint4 pa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g) * p.stride_a + kbyte);
-          const uint4 qa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g + 8) * p.stride_a + kbyte);
-          mma_bf16_16816(acc[mt], pa.x, qa.x, pa.y, qa.y, sx.x, sx.y);
-          mma_bf16_16816(acc[mt], pa.z, qa.z, pa.w, qa.w, sx.z, sx.w);
+      if (!h_ready) {
+        // One thread polls; the barrier passes what it observed to the others.
+        timed_out = tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
+        ph_x ^= 1u;
+        if (__syncthreads_or(timed_out)) {  // (also orders the permuted B_e before its reads)
+          if (tid == 0) record_error(kErrWaitTimeout);
+          bad = true;
+          break;
         }
+        shrink_pass();
       }
-      // acc[mt] = (j mt*16+g, row 2c), (j, row 2c+1), (j+8, row 2c), (j+8, row 2c+1)
-      float *part = sP + warp * (kRows * PS);
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const int j = mt * 16 + g, row = 2 * c;
-        part[row * PS + j] = acc[mt][0];
-        part[(row + 1) * PS + j] = acc[mt][1];
-        part[row * PS + j + 8] = acc[mt][2];
-        part[(row + 1) * PS + j + 8] = acc[mt][3];
-      }
-      __syncthreads();
       // The next pass of this CTA (its rows already in s_rows): its x rows are
       // requested now that sX is free, its base_out rows as the quads of this
       // pass retire, so neither round trip is exposed.
@@ -478,22 +503,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       my_row1[0] = 2 * c < n_g1 ? rows1[2 * c] : -1;
       my_row1[1] = 2 * c + 1 < n_g1 ? rows1[2 * c + 1] : -1;
       if (pre) request_x(p, warp, lane, n_g1, row_bytes_x, bad, rows1, sX, bar_x);
-      // Sum the warps' partials in warp order; split h into bf16 hi + lo.
-      if (tid < kRows * RP / 2) {
-        const int row = (2 * tid) / RP, j = (2 * tid) % RP;
-        float h0 = 0.f, h1 = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          h0 += sP[w * (kRows * PS) + row * PS + j];
-          h1 += sP[w * (kRows * PS) + row * PS + j + 1];
-        }
-        float a0, b0, a1, b1;
-        split_hi_lo(h0, a0, b0);
-        split_hi_lo(h1, a1, b1);
-        *reinterpret_cast<uint32_t *>(sHhi + (row * RP + j) * 2) = pack_bf16x2(a0, a1);
-        *reinterpret_cast<uint32_t *>(sHlo + (row * RP + j) * 2) = pack_bf16x2(b0, b1);
-      }
-      __syncthreads();
+      if (!h_ready) split_h();
+      h_ready = false;
 
       // ---- expand + epilogue (see expand_block).  Lane c takes rank words
       // c*WPL .. c*WPL+WPL-1 of h and of B_e: k-step st uses word c*WPL + 2st
@@ -560,9 +571,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
 
   if constexpr (!MULTI) {
     // ---- before the wait: the pair, and a speculative row list (L2 loads only)
+    // When the routing is one scan chunk, the values read here are kept, so
+    // that after the wait an unchanged routing confirms everything derived
+    // from them without a second scan.
+    int idx_s[kScanPer] = {}, ra_s[kScanPer] = {};
+    const bool snap = spec && p.n_slots <= kScanChunk;
+    if (snap) scan_load(p, 0, idx_s, ra_s);
     if (spec) {
-      total = scan_expert_rows(p, helper ? -1 : spec_target(e), 0, kSpecRows, s_spec, s_cnt, no_idx,
-                               no_idx, false, s_hist);
+      total = scan_expert_rows(p, helper ? -1 : spec_target(e), 0, kSpecRows, s_spec, s_cnt, idx_s,
+                               ra_s, snap, s_hist);
       if (helper) {
         // (spec_mode 2: a different heavy expert, so that the check after the wait fails)
         assign_helper(s_hist, p.n_experts, n_helpers + 1, true, p.spec_mode == 2 ? who + 1 : who,
@@ -570,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
         __syncthreads();
         e = s_role;
         if (e >= 0)
-          total = scan_expert_rows(p, spec_target(e), 0, kSpecRows, s_spec, s_cnt, no_idx, no_idx,
-                                   false, nullptr);
+          total = scan_expert_rows(p, spec_target(e), 0, kSpecRows, s_spec, s_cnt, idx_s, ra_s,
+                                   snap, nullptr);
       }
     }
     int spec_role = 0;  // owner: 1 if the speculative counts give it a helper
@@ -616,48 +633,84 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     int idx0[kScanPer], ra0[kScanPer];
     scan_load(p, 0, idx0, ra0);
     if (n_spec > 0) request_base(p, warp, g, c, n_spec, s_spec + spec_g0, base_v, my_row);
-    int fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, idx0, ra0, true, s_hist);
-    assign_helper(s_hist, p.n_experts, n_helpers, helper, who, &s_role);
-    __syncthreads();
-    const int role = s_role;  // helper: its expert; owner: 1 if it has a helper
-    bool timed_out = false;
-    if (helper && role != e) {  // the speculation picked another expert (or none)
-      if (n_spec > 0) {
-        timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
-        ph_x ^= 1u;
-      }
-      if (pair && !have_pair) {
-        timed_out = (!bad && tid == 0 && !mbar_wait_bounded(bar_w, ph_w)) || timed_out;
-        ph_w ^= 1u;
-      }
-      have_pair = false;
-      if (__syncthreads_or(timed_out)) {
-        if (!bad && tid == 0) record_error(kErrWaitTimeout);
+    // The speculative first pass's h, while the fresh routing loads are in
+    // flight: its x rows land and are shrunk before the scan is read, and the
+    // h is kept only if the scan confirms the rows (h_ready below).
+    bool x_landed = false;
+    if (n_spec > 0 && have_pair && !bad) {
+      const bool t = tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
+      ph_x ^= 1u;
+      x_landed = true;
+      if (__syncthreads_or(t)) {
+        if (tid == 0) record_error(kErrWaitTimeout);
         bad = true;
+      } else {
+        shrink_pass();
+        split_h();
       }
-      n_spec = 0;
-      my_row[0] = my_row[1] = -1;
-      e = role;
-      pair = false;
-      if (e >= 0 && !bad) {
-        fence_proxy_async_smem();  // the old pair's buffers were read by no one; order anyway
-        pair = request_pair(e);
-        if (pair) fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false, nullptr);
-      }
-    } else if (n_spec > 0) {
-      // The speculative rows stand if the fresh scan agrees.
-      // (equal totals and roles give the same first pass [spec_g0, spec_g0 + n_spec))
-      bool differ = tid == 0 && (fresh != total || (!helper && role != spec_role));
-      if (tid < n_spec && s_rows[spec_g0 + tid] != s_spec[spec_g0 + tid]) differ = true;
-      if (__syncthreads_or(differ)) {  // let the copies of the stale rows land first
-        timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
-        ph_x ^= 1u;
+    }
+    // The speculation stands as a whole when the routing it read (one chunk,
+    // its own expert) is unchanged: its rows, counts and roles are then the
+    // fresh ones.  Otherwise scan again and check the first pass's rows.
+    int fresh = total;
+    int role = helper ? e : spec_role;  // helper: its expert; owner: 1 if it has a helper
+    bool timed_out = false;
+    bool same = snap && p.spec_mode == 0;
+    if (same) {
+#pragma unroll
+      for (int i = 0; i < kScanPer; ++i) same = same && idx0[i] == idx_s[i] && ra0[i] == ra_s[i];
+      same = !__syncthreads_or(!same);
+    }
+    if (same) {
+      if (tid < kSpecRows) s_rows[tid] = s_spec[tid];
+      __syncthreads();
+    } else {
+      fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, idx0, ra0, true, s_hist);
+      assign_helper(s_hist, p.n_experts, n_helpers, helper, who, &s_role);
+      __syncthreads();
+      role = s_role;
+      if (helper && role != e) {  // the speculation picked another expert (or none)
+        if (n_spec > 0 && !x_landed) {
+          timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
+          ph_x ^= 1u;
+        }
+        if (pair && !have_pair) {
+          timed_out = (!bad && tid == 0 && !mbar_wait_bounded(bar_w, ph_w)) || timed_out;
+          ph_w ^= 1u;
+        }
+        have_pair = false;
         if (__syncthreads_or(timed_out)) {
           if (!bad && tid == 0) record_error(kErrWaitTimeout);
           bad = true;
         }
         n_spec = 0;
         my_row[0] = my_row[1] = -1;
+        e = role;
+        pair = false;
+        if (e >= 0 && !bad) {
+          fence_proxy_async_smem();  // the old pair's buffers were read by no one; order anyway
+          pair = request_pair(e);
+          if (pair)
+            fresh = scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false,
+                                     nullptr);
+        }
+      } else if (n_spec > 0) {
+        // The speculative rows stand if the fresh scan agrees.
+        // (equal totals and roles give the same first pass [spec_g0, spec_g0 + n_spec))
+        bool differ = tid == 0 && (fresh != total || (!helper && role != spec_role));
+        if (tid < n_spec && s_rows[spec_g0 + tid] != s_spec[spec_g0 + tid]) differ = true;
+        if (__syncthreads_or(differ)) {  // let the copies of the stale rows land first
+          if (!x_landed) {
+            timed_out = !bad && tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
+            ph_x ^= 1u;
+          }
+          if (__syncthreads_or(timed_out)) {
+            if (!bad && tid == 0) record_error(kErrWaitTimeout);
+            bad = true;
+          }
+          n_spec = 0;
+          my_row[0] = my_row[1] = -1;
+        }
       }
     }
     total = pair ? fresh : 0;
@@ -665,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     g_begin = helper ? (total + 1) / 2 : 0;
     g_end = (split && !helper) ? (total + 1) / 2 : total;
     issued = n_spec > 0;  // the first pass's x copies and base_out loads are in flight
+    h_ready = issued && x_landed && !bad;  // ... and its x already shrunk into h
     list0 = 0;
     run_passes();
     drain();

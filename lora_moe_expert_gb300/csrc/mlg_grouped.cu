@@ -33,6 +33,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "mlg_internal.h"
@@ -76,6 +77,8 @@ struct GroupedParams {
   uint32_t off_xa, off_b, off_h, off_base, off_tab, off_my, smem_bytes;
   int32_t my_cap;                // tiles per CTA the tile list holds
   int32_t x_per_row;             // 1: sorted row r reads x row r (not its token's)
+  int32_t tile_m;                // rows per tile (<= kTileM; the MMA M stays kTileM)
+  int32_t x_tma;                 // 1: a tile's x rows are rows r0.. of x (router, per-row x)
 };
 
 // Byte offset of 16-byte chunk `c` (of 8 per 128-byte row) of row `row` in a
@@ -123,17 +126,16 @@ __device__ __forceinline__ int span_hi(const GroupedParams &p, int e) {
   return min(hi, p.row_end);
 }
 
-// Tiles of one expert span [lo, hi): runs of <= 128 rows that also never
+// Tiles of one expert span [lo, hi): runs of <= tile_m rows that also never
 // cross a window boundary (boundaries at row_offset + i * win).
 __device__ __forceinline__ int span_tiles(const GroupedParams &p, int lo, int hi) {
   if (hi <= lo) return 0;
-  const int ro = p.row_offset, W = p.win;
+  const int ro = p.row_offset, W = p.win, T = p.tile_m;
   const int w0 = (lo - ro) / W, w1 = (hi - 1 - ro) / W;
-  if (w0 == w1) return (hi - lo + kTileM - 1) / kTileM;
+  if (w0 == w1) return (hi - lo + T - 1) / T;
   const int first = ro + (w0 + 1) * W - lo;
   const int last = hi - (ro + w1 * W);
-  return (first + kTileM - 1) / kTileM + (w1 - w0 - 1) * ((W + kTileM - 1) / kTileM) +
-         (last + kTileM - 1) / kTileM;
+  return (first + T - 1) / T + (w1 - w0 - 1) * ((W + T - 1) / T) + (last + T - 1) / T;
 }
 
 // Tile t: the expert owning it (tile_start is an exclusive prefix over
@@ -147,23 +149,23 @@ __device__ TileInfo tile_info(const GroupedParams &p, const int *tile_start, int
   TileInfo ti;
   ti.e = lo;
   const int slo = span_lo(p, lo), shi = span_hi(p, lo);
-  const int ro = p.row_offset, W = p.win;
+  const int ro = p.row_offset, W = p.win, T = p.tile_m;
   int u = t - tile_start[lo];
   // walk the window pieces of the span (O(1) per piece type)
   const int w0 = (slo - ro) / W;
   int a = slo;
   int b = min(shi, ro + (w0 + 1) * W);
-  int n = (b - a + kTileM - 1) / kTileM;
+  int n = (b - a + T - 1) / T;
   if (u >= n) {
     u -= n;
-    const int per = (W + kTileM - 1) / kTileM;  // tiles of one whole window
+    const int per = (W + T - 1) / T;  // tiles of one whole window
     const int w = w0 + 1 + u / per;
     u %= per;
     a = ro + w * W;
     b = min(shi, a + W);
   }
-  ti.r0 = a + u * kTileM;
-  ti.r1 = min(ti.r0 + kTileM, b);
+  ti.r0 = a + u * T;
+  ti.r1 = min(ti.r0 + T, b);
   return ti;
 }
 
@@ -190,9 +192,13 @@ __device__ __forceinline__ uint4 add8_bf16(const uint4 b, const float *v) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-template <int RP>  // rank rounded up to a multiple of 16
+// RP: rank rounded up to a multiple of 16.  XTMA: a tile's x rows are rows
+// r0.. of x (router, per-row x) and come in as TMA boxes; else they are
+// gathered row by row through src.
+template <int RP, bool XTMA>
 __global__ void __launch_bounds__(kGThreads, 1)
-    grouped_fold_kernel(const __grid_constant__ CUtensorMap tmap_base, const GroupedParams p) {
+    grouped_fold_kernel(const __grid_constant__ CUtensorMap tmap_base,
+                        const __grid_constant__ CUtensorMap tmap_x, const GroupedParams p) {
   constexpr int KEXP = (2 * RP + 63) / 64 * 64;  // expand K: [hi | lo | zero pad]
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ Ctl ctl;
@@ -273,7 +279,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
   const int n_tiles_all = tile_start[n_e];
   int my_count = 0;
   if (static_cast<int>(blockIdx.x) < n_tiles_all)
-    my_count = min(p.my_cap, (n_tiles_all - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1);
+    my_count = min(p.my_cap, (n_tiles_all - 1 - static_cast<int>(blockIdx.x)) /
+                                     static_cast<int>(gridDim.x) + 1);
   if (tid < my_count) {
     const TileInfo ti = tile_info(p, tile_start, n_e, blockIdx.x + tid * gridDim.x);
     my_tiles[tid].e = ti.e;
@@ -370,7 +377,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // of the stages after it are issued), so xa_lag + 1 stages are in flight.
     const int half = warp == 1 ? 0 : 1;
     const uint64_t keep = l2_evict_last();  // A_e (and token x rows) are re-read by other tiles
-    const uint64_t xpol = p.x_per_row ? l2_evict_first() : keep;  // a per-row x row is read once
+    // a per-row x row (and a router row) is read once
+    const uint64_t xpol = (p.x_per_row || XTMA) ? l2_evict_first() : keep;
     uint32_t it = 0;
     int q[6] = {-1, -1, -1, -1, -1, -1};  // issued, not yet signalled stages (q[0] oldest)
     int nq = 0;
@@ -389,8 +397,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
       }
     };
-    int tok_next[2];
-    tokens(0, tok_next);
+    int tok_next[2] = {-1, -1};
+    if constexpr (!XTMA) tokens(0, tok_next);
     for (int t = 0; t < n_tiles; ++t) {
       const MyTile ti = my_tiles[t];
       const uint8_t *A = reinterpret_cast<const uint8_t *>(
@@ -402,7 +410,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         xv[u] = tok_next[u] >= 0;
         xrow[u] = p.x + static_cast<size_t>(tok_next[u] >= 0 ? tok_next[u] : 0) * p.k_in * 2;
       }
-      tokens(t + 1, tok_next);
+      if constexpr (!XTMA) tokens(t + 1, tok_next);
       for (int kc = 0; kc < p.kc_count; ++kc, ++it) {
         const int st = it % p.nxa;
         if (!wait_bar(ctl, ctl.xa_empty[st], ((it / p.nxa) & 1) ^ 1)) goto prod_a_done;
@@ -414,13 +422,26 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int c = lane & 7;
         const int kk = k0 + 8 * c;
         const bool in = kk < p.k_in;
+        if constexpr (XTMA) {
+          // This warp's 64 rows of the chunk in one box (rows past the tensor
+          // and columns past k_in read as zero); its bytes complete on the
+          // stage's barrier beside the lanes' arrivals for the A_e copies.
+          if (lane == 0) {
+            const uint32_t full = smem_addr(&ctl.xa_full[st]);
+            mbar_expect_tx(full, 64 * 128);
+            tma_load_2d_hint(xs + half * 64 * 128, &tmap_x, k0, ti.r0 + half * 64, full, xpol);
+          }
+        } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int rl = 4 * i + (lane >> 3);  // row of this warp's 64
-          const uint8_t *xr = reinterpret_cast<const uint8_t *>(
-              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(xrow[rl >> 5]), rl & 31));
-          const bool v = __shfl_sync(0xffffffffu, xv[rl >> 5], rl & 31);
-          if (v) cp_async_16_hint(xs + sw128(half * 64 + rl, c), xr + (in ? kk * 2 : 0), in ? 16u : 0u, xpol);
+          for (int i = 0; i < 16; ++i) {
+            const int rl = 4 * i + (lane >> 3);  // row of this warp's 64
+            const uint8_t *xr = reinterpret_cast<const uint8_t *>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(xrow[rl >> 5]), rl & 31));
+            const bool v = __shfl_sync(0xffffffffu, xv[rl >> 5], rl & 31);
+            if (v)
+              cp_async_16_hint(xs + sw128(half * 64 + rl, c), xr + (in ? kk * 2 : 0), in ? 16u : 0u,
+                               xpol);
+          }
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -775,22 +796,37 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return MLG_ERR_CUDA;
+  CUtensorMap tmap_x = tmap;  // unused unless x_tma
+  if (p.x_tma) {  // x rows [row_end, k_in], 64 x 64 boxes in the X tile's 128-byte swizzle
+    const cuuint64_t xdims[2] = {static_cast<cuuint64_t>(p.k_in),
+                                 static_cast<cuuint64_t>(p.row_end)};
+    const cuuint64_t xstrides[1] = {static_cast<cuuint64_t>(p.k_in) * 2};
+    const cuuint32_t xbox[2] = {64, 64};
+    if (enc(&tmap_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t *>(p.x), xdims,
+            xstrides, xbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLG_ERR_CUDA;
+  }
 
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
   int dev = 0;
   cudaGetDevice(&dev);
   std::call_once(once[dev & 63], [d = dev & 63] {
-    cudaError_t e = cudaSuccess;
     const int lim = static_cast<int>(kGSmemLimit);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grouped_fold_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grouped_fold_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grouped_fold_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grouped_fold_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    const void *fns[] = {
+        reinterpret_cast<const void *>(grouped_fold_kernel<16, false>),
+        reinterpret_cast<const void *>(grouped_fold_kernel<32, false>),
+        reinterpret_cast<const void *>(grouped_fold_kernel<48, false>),
+        reinterpret_cast<const void *>(grouped_fold_kernel<64, false>),
+        reinterpret_cast<const void *>(grouped_fold_kernel<16, true>),
+        reinterpret_cast<const void *>(grouped_fold_kernel<32, true>),
+        reinterpret_cast<const void *>(grouped_fold_kernel<48, true>),
+        reinterpret_cast<const void *>(grouped_fold_kernel<64, true>)};
+    cudaError_t e = cudaSuccess;
+    for (const void *fn : fns)
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, attr, lim);
     attr_err[d] = e;
   });
   if (attr_err[dev & 63] != cudaSuccess) return cuda_status(attr_err[dev & 63]);
@@ -800,19 +836,29 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
   const int64_t rows = p.row_end - p.row_offset;
   const int64_t n_win = (rows + p.win - 1) / p.win;
   const int64_t full = rows / p.win, rest = rows % p.win;
-  const int64_t max_tiles = full * ((p.win + kTileM - 1) / kTileM) + (rest + kTileM - 1) / kTileM +
-                            n_e + n_win;
+  const int64_t T = p.tile_m;
+  const int64_t max_tiles = full * ((p.win + T - 1) / T) + (rest + T - 1) / T + n_e + n_win;
   int grid = sm_count();
   if (g_grouped_ctas > 0) grid = g_grouped_ctas;
   const int64_t need = (max_tiles + kMyTilesMax - 1) / kMyTilesMax;
   if (grid < need) grid = static_cast<int>(need);
   if (grid > max_tiles) grid = static_cast<int>(max_tiles);
   p.my_cap = kMyTilesMax;
-  switch (p.r_pad) {
-    case 16: grouped_fold_kernel<16><<<grid, kGThreads, total, stream>>>(tmap, p); break;
-    case 32: grouped_fold_kernel<32><<<grid, kGThreads, total, stream>>>(tmap, p); break;
-    case 48: grouped_fold_kernel<48><<<grid, kGThreads, total, stream>>>(tmap, p); break;
-    default: grouped_fold_kernel<64><<<grid, kGThreads, total, stream>>>(tmap, p); break;
+  const dim3 g(grid), b(kGThreads);
+  if (p.x_tma) {
+    switch (p.r_pad) {
+      case 16: grouped_fold_kernel<16, true><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
+      case 32: grouped_fold_kernel<32, true><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
+      case 48: grouped_fold_kernel<48, true><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
+      default: grouped_fold_kernel<64, true><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
+    }
+  } else {
+    switch (p.r_pad) {
+      case 16: grouped_fold_kernel<16, false><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
+      case 32: grouped_fold_kernel<32, false><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
+      case 48: grouped_fold_kernel<48, false><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
+      default: grouped_fold_kernel<64, false><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
+    }
   }
   return cuda_status(cudaGetLastError());
 }
@@ -833,6 +879,7 @@ mlg_status fill_common(GroupedParams &p, const mlg_bf16 *x, const int32_t *row_a
   p.k_in = k_in;
   p.rank = max_rank;
   p.n_out = n_out;
+  p.tile_m = kTileM;
   return MLG_OK;
 }
 
@@ -927,6 +974,7 @@ extern "C" mlg_status mlg_grouped_down_xrows(
   const int32_t len = row_end - row_offset;
   p.win = cap < static_cast<uint32_t>(len) ? static_cast<int32_t>(cap) : len;
   p.x_per_row = 1;
+  p.x_tma = 1;
   return launch_grouped(p, static_cast<cudaStream_t>(stream));
 }
 
@@ -949,5 +997,11 @@ extern "C" mlg_status mlg_router_fold(const mlg_bf16 *x, const int32_t *row_adap
   p.row_offset = 0;
   p.row_end = n_tokens;
   p.win = n_tokens;
+  // One span: tiles just tall enough that every SM gets at most one (whole
+  // 16-row steps), so no SM idles while others fold a second tile.
+  const int64_t per_sm = (static_cast<int64_t>(n_tokens) + sm_count() - 1) / sm_count();
+  p.tile_m = static_cast<int32_t>(
+      std::min<int64_t>(kTileM, std::max<int64_t>(16, (per_sm + 15) / 16 * 16)));
+  p.x_tma = 1;
   return launch_grouped(p, static_cast<cudaStream_t>(stream));
 }

@@ -473,6 +473,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
     cp_async_wait_group<0>();
     fence_proxy_async_smem();
     for (int i = 0; i < nq; ++i) mbar_arrive(smem_addr(&ctl.xa_full[q[i]]));
+    if constexpr (XTMA) {  // this warp's boxes of the unsignalled stages: let them land
+      if (lane == 0)
+        for (int j = 0; j < nq; ++j) {
+          const uint32_t k = it - nq + j;
+          mbar_wait_bounded(smem_addr(&ctl.xa_full[k % p.nxa]), (k / p.nxa) & 1);
+        }
+    }
   } else if (warp == 2) {
     // ================================================================ B_e producer
     // One B_e tile [n_ch rows x rank] per accumulator chunk, signalled `lag`

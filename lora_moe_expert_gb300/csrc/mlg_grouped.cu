@@ -237,6 +237,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
   // copies of B_e's rank columns.
   for (uint32_t i = tid * 16; i < p.off_h; i += kGThreads * 16)
     *reinterpret_cast<uint4 *>(smem + i) = make_uint4(0, 0, 0, 0);
+  __syncthreads();  // barriers initialised (and visible) before anyone waits on them
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  // Everything above runs while the preceding kernel finishes (programmatic
+  // dependent launch); the routing, x, the row map and base_out may be written
+  // by it, so every thread waits before its first read of them.  The next
+  // fold may start its own setup now.
+  griddep_launch_dependents();
+  griddep_wait();
   // Tile table: tiles of expert e = ceil(rows of e in the window / 128), 0 if
   // the expert folds nothing; exclusive prefix over experts.  One expert per
   // thread per pass, its four loads issued together.
@@ -287,11 +298,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
     my_tiles[tid].r0 = ti.r0;
     my_tiles[tid].r1 = ti.r1;
     my_tiles[tid].scale = __ldg(p.scale_table + ti.e);
-  }
-  __syncthreads();
-  if (warp == 0) {
-    tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -851,22 +857,26 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
   if (grid < need) grid = static_cast<int>(need);
   if (grid > max_tiles) grid = static_cast<int>(max_tiles);
   p.my_cap = kMyTilesMax;
-  const dim3 g(grid), b(kGThreads);
-  if (p.x_tma) {
-    switch (p.r_pad) {
-      case 16: grouped_fold_kernel<16, true><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
-      case 32: grouped_fold_kernel<32, true><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
-      case 48: grouped_fold_kernel<48, true><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
-      default: grouped_fold_kernel<64, true><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
-    }
-  } else {
-    switch (p.r_pad) {
-      case 16: grouped_fold_kernel<16, false><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
-      case 32: grouped_fold_kernel<32, false><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
-      case 48: grouped_fold_kernel<48, false><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
-      default: grouped_fold_kernel<64, false><<<g, b, total, stream>>>(tmap, tmap_x, p); break;
-    }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kGThreads, 1, 1);
+  cfg.dynamicSmemBytes = total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  using KernelFn = void (*)(CUtensorMap, CUtensorMap, GroupedParams);
+  KernelFn fn;
+  switch (p.r_pad) {
+    case 16: fn = p.x_tma ? grouped_fold_kernel<16, true> : grouped_fold_kernel<16, false>; break;
+    case 32: fn = p.x_tma ? grouped_fold_kernel<32, true> : grouped_fold_kernel<32, false>; break;
+    case 48: fn = p.x_tma ? grouped_fold_kernel<48, true> : grouped_fold_kernel<48, false>; break;
+    default: fn = p.x_tma ? grouped_fold_kernel<64, true> : grouped_fold_kernel<64, false>; break;
   }
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, fn, tmap, tmap_x, p);
+  if (err != cudaSuccess) return cuda_status(err);
   return cuda_status(cudaGetLastError());
 }
 

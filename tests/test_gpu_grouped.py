@@ -350,3 +350,37 @@ def test_multi_adapter_prefill_through_cell_sort():
     ref, folded, _ = fh.oracle_reference(w)
     assert 0 < folded.sum() < folded.size
     fh.check_fold(got, w.base, ref, folded)
+
+
+@pytest.mark.parametrize("per_row_x", [False, True], ids=["token_x", "row_x"])
+def test_inputs_written_by_the_preceding_kernel(per_row_x):
+    """x and the expert spans are rewritten on the stream right before the
+    fold (by kernels the fold may overlap): the fold uses the new values."""
+    import copy
+
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_grouped(71, [300, 180, 250], 6, 24, 256, 512, 32, cap=400,
+                             adapted_frac=0.8, per_row_x=per_row_x)
+    w2 = copy.deepcopy(w)
+    rng = np.random.default_rng(5)
+    if per_row_x:
+        w2.x_rows = synth.bf16_bits(rng.standard_normal(w.x_rows.shape).astype(np.float32))
+    else:
+        w2.x = synth.bf16_bits(rng.standard_normal(w.x.shape).astype(np.float32))
+    prob = FoldProblem(w)
+    xt = prob.x_rows if per_row_x else prob.x
+    x_new = torch.from_numpy((w2.x_rows if per_row_x else w2.x).view(np.int16)).cuda()
+    off_new = prob.expert_offsets.clone()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        prob.reset()
+        xt.view(torch.int16).zero_()
+        xt.view(torch.int16).add_(x_new)
+        prob.expert_offsets.zero_()
+        prob.expert_offsets.add_(off_new)
+        prob.run(stream=s)
+    torch.cuda.synchronize()
+    ref, folded, _ = fh.oracle_reference(w2)
+    fh.check_fold(prob.base_bits(), w2.base, ref, folded)

@@ -16,9 +16,13 @@
 //  * the rows of the expert are found before the wait by a speculative scan of
 //    the routing (L2 loads only; the values may still change), and their x
 //    and base_out lines are prefetched into L2.  After the wait the x rows and
-//    base_out rows of that row list are requested at once, and the routing is
-//    scanned again; only if the fresh scan disagrees are they requested again.
-//    The round trip on the routing thus overlaps the one on x and base_out;
+//    base_out rows of that row list are requested at once with the fresh
+//    routing loads; the first pass's x is shrunk while those are in flight.
+//    A routing of one scan chunk is compared value for value with what the
+//    speculation read (kept in registers): unchanged, the speculative rows,
+//    counts and roles stand; else the routing is scanned again and rows that
+//    differ are requested again.  The round trip on the routing thus overlaps
+//    the one on x and the shrink;
 //  * shrink h = x A_e^T with mma.sync m16n8k16 (M = rank, N = 8 rows, k split
 //    over the warps, partial sums added in a fixed order), h split into bf16
 //    hi + lo halves (h enters the expand at ~2^-17 relative precision);
@@ -34,6 +38,8 @@
 //    second, both deciding the split from the same per-expert row counts
 //    (the rows a CTA stores bound its time: one SM writes ~32 B per cycle).
 // Rows are folded 8 at a time; an expert with more rows runs several passes.
+// Multi-adapter tables (one set of cells per adapter slot) take a second form
+// of the kernel, described at decode_fold_kernel.
 #include <cuda_bf16.h>
 
 #include <mutex>

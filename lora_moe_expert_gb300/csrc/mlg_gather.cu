@@ -29,7 +29,11 @@
 //    relative precision (h stays fp32 in effect) and the expand cost does not
 //    depend on how many rows an expert has;
 //  * epilogue: out = RNE_bf16(base + scale * (h B^T)) in shared memory, then
-//    bulk-stored; rows that do not fold are never loaded or stored.
+//    bulk-stored; rows that do not fold are never loaded or stored;
+//  * multi-adapter tables (one set of cells per adapter slot, the row map
+//    naming the set) fold through the row's cell; for them the units are the
+//    cells the routing hits (read first), and a CTA prefetches its next
+//    unit's slices into L2 while it folds the current one.
 #include <cuda_bf16.h>
 
 #include <mutex>

@@ -13,15 +13,18 @@
 //  * tiles are expert-aligned runs of <= 128 sorted rows (one tcgen05 M), so
 //    a tile never mixes experts and every output row has one owner; the tile
 //    list is built on the device from expert_offsets and the tables (no host
-//    copy), and persistent CTAs (one per SM) walk it round-robin;
+//    copy), and persistent CTAs (one per SM) walk it round-robin.  The setup
+//    that reads none of the fold's inputs runs before griddepcontrol.wait, so
+//    it overlaps the preceding kernel (programmatic dependent launch);
 //  * warp 0 issues the tensor-core work: shrink H = X A_e^T (M=128, N=rank,
 //    K=k_in in 64-wide chunks) into tensor memory, then expand
 //    ACC = [H_hi | H_lo] [B_e | B_e]^T (M=128, N=64/128 columns per chunk) into
 //    a double-buffered TMEM accumulator -- h is split into two bf16 halves so
 //    it enters the expand at ~2^-17 relative precision (kept fp32 in effect);
-//  * warps 1 and 3 gather the X rows (via src, or row r itself for per-row x)
-//    and A_e chunks, warp 2 the B_e chunks, with 16-byte cp.async into
-//    128-byte-swizzled K-major tiles;
+//  * warps 1 and 3 gather the X rows via src and A_e chunks, warp 2 the B_e
+//    chunks, with 16-byte cp.async into 128-byte-swizzled K-major tiles; when
+//    a tile's x rows are rows r0.. of x (router, per-row x) they come in as
+//    64 x 64 TMA boxes instead;
 //  * warps 4-11 (two per TMEM lane quarter) scale and split h, then stream
 //    base_out: the pair owns the quarter's 32 rows of the tile, each warp
 //    takes every other 64-column box and runs its own ring of 32x64 TMA

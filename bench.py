@@ -45,6 +45,7 @@ METRIC = "MoE LoRA fold rows/s and achieved HBM GB/s (% of GB300 roofline), 1 GP
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 SOAK_S = 0.8  # seconds of untimed replays under the clock sampler before the timed region
+REF_TOTAL_S = 120.0  # wall-clock bound of the reference arm's timed steps
 
 # workload name -> (generator, description)
 WORKLOADS = {
@@ -466,10 +467,13 @@ def run_reference(args):
     steps_rows = []
     for _ in range(args.warmup):
         time_oracle(w, budget_s=0.0)
+    # Each step is a bounded sample: the whole timed run stays within about
+    # REF_TOTAL_S whatever --steps is (at most --ref-budget seconds a step).
+    budget = min(args.ref_budget, REF_TOTAL_S / max(args.steps, 1))
     t0 = time.perf_counter()
     samples = []
     for _ in range(args.steps):
-        rps, desc = time_oracle(w, budget_s=args.ref_budget)
+        rps, desc = time_oracle(w, budget_s=budget)
         steps_rows.append(rps)
         samples.append(desc)
     total = time.perf_counter() - t0

@@ -314,3 +314,23 @@ def test_multi_one_adapter_matches_single_bits():
                               w.max_rank, w.n_out, w.top_k, multi.n_experts, 1)
     torch.cuda.synchronize()
     assert np.array_equal(multi.base_bits(), single.base_bits())
+
+
+def test_multi_large_tables_fall_back_to_the_cluster_kernel():
+    """More cells than the multi-cell form takes (6 adapters x 300 experts):
+    the cluster kernel folds them (no compaction past 512 cells), and forcing
+    the resident-pair kernel is refused without touching base_out."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.custom_gather_multi(81, 24, 4, 300, 128, 256, 16, 6, adapted_frac=0.3,
+                                  base_frac=0.2, bad_ids=2)
+    _run_and_check(w)
+    prob = FoldProblem(w)
+    try:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 1)
+        with pytest.raises(mlg.MlgError) as ei:
+            prob.run()
+        assert ei.value.status == mlg.MLG_ERR_UNSUPPORTED
+    finally:
+        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+    assert np.array_equal(prob.base_bits(), w.base)

@@ -15,6 +15,13 @@
  * ensure_decode_route_servable, build_moe_row_adapter_host,
  * build_moe_row_adapter_decode).
  *
+ * Two widened forms sit beside the pages' calls: a per-row x grouped fold
+ * (mlg_grouped_down_xrows: sorted row r reads x_rows[r], the input a down
+ * projection has) and a multi-adapter decode fold (mlg_gather_bgmv_multi,
+ * with mlg_build_moe_row_adapter_decode_multi: one table set per adapter
+ * slot, each token's row-map entry naming its set).  Each states the reading
+ * of the pages it rests on.
+ *
  * Conventions shared by every call:
  *  - Every call that can fail returns an mlg_status; the library never
  *    aborts, asserts or prints.  The pages' `None` becomes MLG_ERR_EMPTY or
@@ -62,7 +69,7 @@ typedef int32_t mlg_status;
 #define MLG_ERR_INVALID_ARG (-1)      /* bad pointer, size or relation; the pages' None */
 #define MLG_ERR_EMPTY (-2)            /* empty input where the pages return None */
 #define MLG_ERR_CAP_ZERO (-3)         /* window cap of 0: the pages' panic */
-#define MLG_ERR_REFUSE (-4)           /* a decode batch the single-active fold cannot serve */
+#define MLG_ERR_REFUSE (-4)           /* a decode batch the installed adapter(s) cannot serve */
 #define MLG_ERR_UNSUPPORTED (-5)      /* alignment or size limit of this implementation */
 #define MLG_ERR_BUFFER_TOO_SMALL (-6) /* output buffer shorter than the result */
 #define MLG_ERR_CUDA (-7)             /* a CUDA runtime call failed; see mlg_last_cuda_error() */
@@ -143,7 +150,12 @@ MLG_API mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices, co
  *   n_adapters   >= 1; n_adapters * n_experts <= 2^30
  *   others       as for mlg_gather_bgmv
  * Errors as for mlg_gather_bgmv, plus INVALID_ARG for n_adapters < 1 and
- * UNSUPPORTED for more than 2^30 cells. */
+ * UNSUPPORTED for more than 2^30 cells.
+ * The prefill form needs no call of its own: sort the flat rows by cell
+ * (slot * n_experts + expert; rows of no cell after the last) into
+ * expert_offsets / src and call mlg_grouped_down or
+ * mlg_grouped_down_all_windows with n_experts = n_adapters * n_experts, the
+ * slot-major tables and the prefill row map of slots. */
 MLG_API mlg_status mlg_gather_bgmv_multi(const mlg_bf16 *x, const int32_t *indices,
                                          const int32_t *row_adapter, const uint64_t *a_table,
                                          const uint64_t *b_table, const float *scale_table,

@@ -149,6 +149,15 @@ def test_router_small_and_row_map():
     fh.check_fold(prob.base_bits(), w.base, ref, folded)
 
 
+@pytest.mark.parametrize("shape", [(77, 72, 64, 8), (300, 200, 264, 16), (1000, 1000, 128, 32),
+                                   (153, 520, 96, 64)], ids=lambda s: "x".join(map(str, s)))
+def test_router_shapes(shape):
+    """Ragged k tails (the x boxes read zeros past k_in), token counts that are
+    not a multiple of the tile height, every rank bucket."""
+    T, k_in, n_out, r = shape
+    _run_and_check(synth.custom_router(40 + T, T, k_in, n_out, r))
+
+
 def test_router_zero_cell_is_noop():
     from lora_moe_expert_gb300.device import FoldProblem
 

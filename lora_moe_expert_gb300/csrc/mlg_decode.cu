@@ -186,9 +186,11 @@ __device__ __forceinline__ void request_x(const DecodeParams &p, int warp, int l
 
 // This lane's base_out rows (rows 2c and 2c+1 of the pass) in 16-byte chunks:
 // columns blk*64 + 8g .. +7 of the warp's 64-column blocks, into registers.
+// Of the columns [col0, col0 + n_cols) only (the whole row in the single-table form).
 __device__ __forceinline__ void request_base(const DecodeParams &p, int warp, int g, int c,
                                              int n_g, const int *s_rows,
-                                             uint4 (&base_v)[kMaxBlocks][2], int (&my_row)[2]) {
+                                             uint4 (&base_v)[kMaxBlocks][2], int (&my_row)[2],
+                                             int col0, int n_cols) {
   my_row[0] = 2 * c < n_g ? s_rows[2 * c] : -1;
   my_row[1] = 2 * c + 1 < n_g ? s_rows[2 * c + 1] : -1;
 #pragma unroll
@@ -197,8 +199,9 @@ __device__ __forceinline__ void request_base(const DecodeParams &p, int warp, in
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       base_v[i][r] = make_uint4(0, 0, 0, 0);
-      if (my_row[r] >= 0 && col < p.n_out)
-        base_v[i][r] = ld_cg_v4(p.base_out + static_cast<size_t>(my_row[r]) * p.n_out + col);
+      if (my_row[r] >= 0 && col < n_cols)
+        base_v[i][r] =
+            ld_cg_v4(p.base_out + static_cast<size_t>(my_row[r]) * p.n_out + col0 + col);
     }
   }
 }
@@ -379,17 +382,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
   float scale = 0.f;
   bool pair = false;  // the pair of expert e was requested on bar_w
 
-  // Table entry of expert ex; on a foldable pair, request it (CTA-uniform).
+  // Columns of this CTA's current unit: [col0, col0 + n_cols).  The
+  // single-table form always takes whole rows; the multi-adapter form may
+  // split a cell's columns over two CTAs.
+  int col0_v = 0, n_cols_v = p.n_out;
+  auto col0 = [&]() { return MULTI ? col0_v : 0; };
+  auto n_cols = [&]() { return MULTI ? n_cols_v : p.n_out; };
+
+  // Table entry of expert ex; on a foldable pair, request it (CTA-uniform):
+  // all of A_e and the B_e rows of this unit's columns.
   auto request_pair = [&](int ex) -> bool {
     const uint64_t a_addr = __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + ex);
     const uint64_t b_addr = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ex);
     scale = __ldg(p.scale_table + ex);
     if (a_addr == 0 || b_addr == 0 || ((a_addr | b_addr) & 15u) != 0) return false;
-    if (warp == 0 && !bad) {  // the whole pair: one copy per A_e row, one for B_e
-      const uint32_t b_bytes = static_cast<uint32_t>(p.n_out) * RP * 2u;
+    if (warp == 0 && !bad) {  // one copy per A_e row, one for the B_e rows
+      const uint32_t b_bytes = static_cast<uint32_t>(n_cols()) * RP * 2u;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_w, RP * row_bytes_x + b_bytes);
-        bulk_g2s(smem_addr(sB), reinterpret_cast<const void *>(b_addr), b_bytes, bar_w);
+        bulk_g2s(smem_addr(sB),
+                 reinterpret_cast<const uint8_t *>(b_addr) + static_cast<size_t>(col0()) * RP * 2,
+                 b_bytes, bar_w);
       }
       __syncwarp();
       const uint8_t *A = reinterpret_cast<const uint8_t *>(a_addr);
@@ -472,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       const int n_g = min(kRows, g_end - g0);
       if (!issued) {
         request_x(p, warp, lane, n_g, row_bytes_x, bad, rows, sX, bar_x);
-        request_base(p, warp, g, c, n_g, rows, base_v, my_row);
+        request_base(p, warp, g, c, n_g, rows, base_v, my_row, col0(), n_cols());
       }
       issued = false;
       timed_out = false;
@@ -485,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
           bad = true;
           break;
         }
-        permute_b<RP>(smem + p.off_b, p.n_out);
+        permute_b<RP>(smem + p.off_b, n_cols());
       }
       if (!h_ready) {
         // One thread polls; the barrier passes what it observed to the others.
@@ -525,11 +538,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
         for (int i = 0; i < kMaxBlocks; ++i) {
           const int blk = warp + i * kWarps;
           uint4 nv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-          if (blk * 64 < p.n_out) {  // warp-uniform
+          if (blk * 64 < n_cols()) {  // warp-uniform
             float d[4][4];
-            expand_block<RP>(d, sB, hh, hl, blk, p.n_out);
-            const int col = blk * 64 + 8 * g;
-            const bool col_ok = col < p.n_out;
+            expand_block<RP>(d, sB, hh, hl, blk, n_cols());
+            const int col = col0() + blk * 64 + 8 * g;
+            const bool col_ok = col < col0() + n_cols();
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
               if (my_row[r] >= 0 && col_ok) {
@@ -627,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
         if (tid == 0) record_error(kErrWaitTimeout);
         bad = true;
       } else {
-        permute_b<RP>(smem + p.off_b, p.n_out);
+        permute_b<RP>(smem + p.off_b, n_cols());
       }
     }
     __syncthreads();
@@ -638,7 +651,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     if (n_spec > 0) request_x(p, warp, lane, n_spec, row_bytes_x, bad, s_spec + spec_g0, sX, bar_x);
     int idx0[kScanPer], ra0[kScanPer];
     scan_load(p, 0, idx0, ra0);
-    if (n_spec > 0) request_base(p, warp, g, c, n_spec, s_spec + spec_g0, base_v, my_row);
+    if (n_spec > 0)
+      request_base(p, warp, g, c, n_spec, s_spec + spec_g0, base_v, my_row, 0, p.n_out);
     // The speculative first pass's h, while the fresh routing loads are in
     // flight: its x rows land and are shrunk before the scan is read, and the
     // h is kept only if the scan confirms the rows (h_ready below).
@@ -745,8 +759,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       if (lane == 0) s_fold[(b >> 5) + warp] = m;
     }
     // Units: the foldable cells with a folding row, in cell order; the one of
-    // rank k goes to CTA k mod gridDim.x.  Returns this CTA's count.
+    // rank k < G goes to CTA k.  Cells past the first round of G are split by
+    // columns into two halves (when n_out is a multiple of 128), half j of
+    // the extra ones going to CTA j mod G, so no CTA folds a second whole
+    // cell while the rest wait.  An entry of s_units is cell | (half + 1) << 28
+    // (0: the whole cell).  Returns this CTA's count.
     const int G = static_cast<int>(gridDim.x);
+    const bool halves = p.n_out % 128 == 0;
     auto deal_units = [&](int me) -> int {
       for (int i = tid; i < p.n_experts; i += kThreads) hist[i] = 0;
       __syncthreads();
@@ -765,10 +784,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
           n_hit += s_cnt[0][w];
         }
         const int rank = before + __popc(m & ((1u << lane) - 1u));
-        if (f && rank % G == me && rank / G < kMaxUnits) s_units[rank / G] = ex;
+        if (f && (!halves || rank < G)) {
+          if (rank % G == me && rank / G < kMaxUnits) s_units[rank / G] = ex;
+        } else if (f) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = 2 * (rank - G) + h;
+            if (j % G == me && 1 + j / G < kMaxUnits) s_units[1 + j / G] = ex | ((h + 1) << 28);
+          }
+        }
         __syncthreads();
       }
-      return n_hit > me ? min(kMaxUnits, (n_hit - 1 - me) / G + 1) : 0;
+      if (!halves) return n_hit > me ? min(kMaxUnits, (n_hit - 1 - me) / G + 1) : 0;
+      const int extra = 2 * max(0, n_hit - G);  // half units past the first round
+      const int mine = (n_hit > me ? 1 : 0) + (extra > me ? (extra - 1 - me) / G + 1 : 0);
+      return min(kMaxUnits, mine);
     };
     // (spec_mode 1: no speculation; 2: another CTA's first cell, so that the
     // check after the wait fails)
@@ -793,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
           if (tid == 0) record_error(kErrWaitTimeout);
           bad = true;
         } else {
-          permute_b<RP>(smem + p.off_b, p.n_out);
+          permute_b<RP>(smem + p.off_b, n_cols());
         }
       }
     }
@@ -804,8 +834,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     // when the speculation picked it.
     n_mine = deal_units(me);
     for (int u = 0; u < n_mine && !bad; ++u) {
-      e = s_units[u];
-      if (u == 0 && spec_pair && e == e_spec) {
+      e = s_units[u] & 0x0fffffff;
+      const int half = (s_units[u] >> 28) - 1;  // -1: the whole cell
+      col0_v = half < 0 ? 0 : half * (p.n_out / 2);
+      n_cols_v = half < 0 ? p.n_out : p.n_out / 2;
+      if (u == 0 && spec_pair && e == e_spec && half < 0) {
         pair = true;  // landed and permuted before the wait; scale set by its request
         have_pair = true;
       } else {

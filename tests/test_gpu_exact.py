@@ -97,6 +97,13 @@ def test_gather_multi_exact(path):
         mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
 
 
+def test_gather_multi_halves_exact():
+    """The multi-adapter form's second-round cells folded in column halves, bit-exact."""
+    w = integerize(synth.custom_gather_multi(46, 96, 8, 128, 256, 512, 16, 4, adapted_frac=0.9),
+                   16)
+    _check_exact(w, lambda prob: prob.run())
+
+
 def test_grouped_exact():
     w = integerize(synth.custom_grouped(31, [120, 70, 90], 4, 10, 192, 320, 32, cap=100,
                                         adapted_frac=0.7, stream_base=[0, 1, 0]), 12)

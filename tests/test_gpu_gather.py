@@ -334,3 +334,12 @@ def test_multi_large_tables_fall_back_to_the_cluster_kernel():
     finally:
         mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
     assert np.array_equal(prob.base_bits(), w.base)
+
+
+@pytest.mark.parametrize("n_out", [1024, 264], ids=["halves", "whole"])
+def test_multi_second_round_cells(n_out):
+    """More hit cells than CTAs: past the first round the cells are split into
+    two column halves over two CTAs (n_out a multiple of 128) or dealt whole."""
+    w = synth.custom_gather_multi(91, 96, 8, 128, 256, n_out, 16, 4, adapted_frac=0.9)
+    _, stats, folded = _run_and_check(w)
+    assert folded.sum() > 0

@@ -766,10 +766,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     // (0: the whole cell).  Returns this CTA's count.
     const int G = static_cast<int>(gridDim.x);
     const bool halves = p.n_out % 128 == 0;
-    auto deal_units = [&](int me) -> int {
+    auto deal_units = [&](int me, const int (&idx0)[kScanPer], const int (&ra0)[kScanPer],
+                          bool have0) -> int {
       for (int i = tid; i < p.n_experts; i += kThreads) hist[i] = 0;
       __syncthreads();
-      scan_expert_rows(p, -1, 0, 0, s_rows, s_cnt, no_idx, no_idx, false, hist);
+      scan_expert_rows(p, -1, 0, 0, s_rows, s_cnt, idx0, ra0, have0, hist);
       int n_hit = 0;
       for (int b = 0; b < p.n_experts; b += kThreads) {
         const int ex = b + tid;
@@ -803,13 +804,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     // (spec_mode 1: no speculation; 2: another CTA's first cell, so that the
     // check after the wait fails)
     const int me = static_cast<int>(blockIdx.x);
-    int n_mine = spec ? deal_units(p.spec_mode == 2 ? (me + 1) % G : me) : 0;
+    // When the routing is one scan chunk, the values read here are kept: if
+    // they are unchanged after the wait, the units and the first cell's rows
+    // dealt from them stand without a second read.
+    int idx_s[kScanPer] = {}, ra_s[kScanPer] = {};
+    const bool snap = spec && p.spec_mode == 0 && p.n_slots <= kScanChunk;
+    if (snap) scan_load(p, 0, idx_s, ra_s);
+    int n_mine = spec ? deal_units(p.spec_mode == 2 ? (me + 1) % G : me, idx_s, ra_s, snap) : 0;
     const int e_spec = n_mine > 0 ? s_units[0] : -1;
     bool spec_pair = false;
+    int ns = 0;  // rows of the first cell (first kSpecRows of them in s_spec)
     if (e_spec >= 0) {
       spec_pair = request_pair(e_spec);
-      const int ns = scan_expert_rows(p, e_spec, 0, kSpecRows, s_spec, s_cnt, no_idx, no_idx,
-                                      false, nullptr);
+      ns = scan_expert_rows(p, e_spec, 0, kSpecRows, s_spec, s_cnt, idx_s, ra_s, snap, nullptr);
       if (warp == 1 && lane < min(ns, kRows)) {
         const int row = s_spec[lane];
         prefetch_l2(p.x + static_cast<size_t>(row / p.top_k) * p.k_in, row_bytes_x);
@@ -832,7 +839,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
 
     // ---- after the wait: the fresh unit list; the first cell's pair is kept
     // when the speculation picked it.
-    n_mine = deal_units(me);
+    bool same = snap;
+    if (same) {
+      int idx0[kScanPer], ra0[kScanPer];
+      scan_load(p, 0, idx0, ra0);
+#pragma unroll
+      for (int i = 0; i < kScanPer; ++i) same = same && idx0[i] == idx_s[i] && ra0[i] == ra_s[i];
+      same = !__syncthreads_or(!same);
+    }
+    if (!same) n_mine = deal_units(me, no_idx, no_idx, false);
     for (int u = 0; u < n_mine && !bad; ++u) {
       e = s_units[u] & 0x0fffffff;
       const int half = (s_units[u] >> 28) - 1;  // -1: the whole cell
@@ -847,9 +862,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
         pair = request_pair(e);
         have_pair = false;
       }
-      total = pair ? scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false,
-                                      nullptr)
-                   : 0;
+      if (u == 0 && same && e == e_spec && half < 0) {  // the speculative rows stand
+        if (tid < kSpecRows) s_rows[tid] = s_spec[tid];
+        __syncthreads();
+        total = pair ? ns : 0;
+      } else {
+        total = pair ? scan_expert_rows(p, e, 0, kSpecRows, s_rows, s_cnt, no_idx, no_idx, false,
+                                        nullptr)
+                     : 0;
+      }
       g_begin = 0;
       g_end = total;
       issued = false;

@@ -34,6 +34,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -154,7 +155,9 @@ class ClockSampler:
         self.gpu = gpu_index
         self.settle_s = settle_s
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_{os.getpid()}.csv")
+        # raw samples: a temporary file unless BENCH_CLOCKS_DIR names a folder to keep them in
+        folder = os.environ.get("BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(folder, f"bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:

@@ -343,3 +343,31 @@ def test_multi_second_round_cells(n_out):
     w = synth.custom_gather_multi(91, 96, 8, 128, 256, n_out, 16, 4, adapted_frac=0.9)
     _, stats, folded = _run_and_check(w)
     assert folded.sum() > 0
+
+
+@pytest.mark.parametrize("case", ["all_base", "zero_tables", "multi_all_base", "grouped_all_base"])
+def test_degenerate_batches_fold_nothing(case):
+    """Batches where no row folds still launch and leave every bit of base_out
+    (and the guard rows) as it was."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    if case == "all_base":
+        w = synth.custom_gather(61, 24, 4, 16, 256, 512, 16, base_frac=1.0)
+    elif case == "multi_all_base":
+        w = synth.custom_gather_multi(62, 24, 4, 16, 256, 512, 16, 3, base_frac=1.0)
+    elif case == "grouped_all_base":
+        w = synth.custom_grouped(63, [40, 70], 4, 12, 256, 512, 32, cap=64,
+                                 stream_base=[1, 1])
+    else:
+        w = synth.custom_gather(64, 24, 4, 16, 256, 512, 16)
+    prob = FoldProblem(w, guard_rows=2)
+    if case == "zero_tables":
+        prob.a_table.zero_()
+        prob.b_table.zero_()
+    ref, folded, _ = fh.oracle_reference(w)
+    if case != "zero_tables":
+        assert not folded.any()
+    prob.run()
+    torch.cuda.synchronize()
+    assert np.array_equal(prob.base_bits(), w.base)
+    assert np.all(prob.guard_bits() == 0x7FC1)

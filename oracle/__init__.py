@@ -41,7 +41,11 @@ OK, NONE, EMPTY, CAP_ZERO, REFUSE, TOO_SMALL = 0, -1, -2, -3, -4, -6
 
 
 def build(source: str = SOURCE, library: str = LIBRARY, extra_flags: Sequence[str] = ()) -> str:
-    """Compile the oracle with gcc (plain -O2: no fast-math, so no reassociation)."""
+    """Compile the oracle with gcc (plain -O2: no fast-math, so no reassociation).
+
+    -fopenmp lets the row loops run on several threads (oracle_set_threads);
+    each row is still computed by one thread in the serial order, so the
+    results do not depend on the thread count."""
     if (
         os.path.exists(library)
         and source == SOURCE
@@ -49,7 +53,8 @@ def build(source: str = SOURCE, library: str = LIBRARY, extra_flags: Sequence[st
         and os.path.getmtime(library) >= os.path.getmtime(source)
     ):
         return library
-    cmd = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", *extra_flags, "-o", library, source]
+    cmd = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-fopenmp", *extra_flags, "-o", library,
+           source]
     subprocess.run(cmd, check=True)
     return library
 
@@ -68,6 +73,8 @@ class Oracle:
     def __init__(self, library: Optional[str] = None):
         self.lib = ctypes.CDLL(library or build())
         L = self.lib
+        L.oracle_set_threads.argtypes = [_i32]
+        L.oracle_set_threads.restype = _i32
         L.oracle_resolve_moe_lora_route.argtypes = [_i32, _i32, _i32]
         L.oracle_resolve_moe_lora_route.restype = _i32
         L.oracle_ensure_decode_route_servable.argtypes = [_i32]
@@ -102,6 +109,11 @@ class Oracle:
         L.oracle_gather_fold_rows.restype = _i32
         L.oracle_grouped_fold_rows.argtypes = [_p] * 9 + [_i32, _p, _p] + [_i32] * 7
         L.oracle_grouped_fold_rows.restype = _i32
+
+    def set_threads(self, n: int) -> int:
+        """Threads of the row loops (n < 1: every core); returns the count in force
+        (1 for a build without OpenMP).  Results are the same bits for any count."""
+        return int(self.lib.oracle_set_threads(n))
 
     # ---- host rules -------------------------------------------------------
     def resolve_moe_lora_route(self, adapter_slot: int, active: int, has_moe_lora: bool) -> int:

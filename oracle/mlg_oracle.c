@@ -31,10 +31,19 @@
  * Status codes follow the library ABI's numbering so tests can compare them
  * directly: 0 ok, -1 invalid argument (the pages' None), -2 empty input,
  * -3 cap == 0 (the pages' panic), -4 refuse, -6 buffer too small.
+ *
+ * Threads: built with -fopenmp, the loops over output rows run in parallel
+ * (OpenMP, oracle_set_threads).  Every row is computed by one thread with the
+ * same sequence of operations as in a serial run, so the results are the same
+ * bits for any thread count; only the wall time changes.  Built without
+ * OpenMP the pragmas are ignored and the oracle is single-threaded.
  */
 #include <stdint.h>
 #include <stddef.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define OR_OK 0
 #define OR_NONE (-1)
@@ -46,6 +55,18 @@
 #define ROUTE_FOLD 0
 #define ROUTE_SKIP 1
 #define ROUTE_REFUSE 2
+
+/* Threads used by the row loops (1 without OpenMP).  n < 1 selects every
+ * core OpenMP reports.  Returns the thread count now in force. */
+int32_t oracle_set_threads(int32_t n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n >= 1 ? n : omp_get_num_procs());
+    return (int32_t)omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 /* bf16 -> double, exact: a bf16 is the top half of an IEEE binary32. */
 static double bf16_value(uint16_t bits) {
@@ -244,6 +265,7 @@ int32_t oracle_gather_fold(const uint16_t *x, const int32_t *indices, const int3
                            uint8_t *folded, int32_t n_slots, int32_t k_in, int32_t max_rank,
                            int32_t n_out, int32_t top_k, int32_t n_experts) {
     if (max_rank > 1024 || top_k < 1) return OR_NONE;
+#pragma omp parallel for schedule(dynamic, 8)
     for (int32_t row = 0; row < n_slots; ++row) {
         const uint16_t *base_row = base_in + (int64_t)row * n_out;
         double *ref_row = ref_out + (int64_t)row * n_out;
@@ -277,6 +299,7 @@ int32_t oracle_gather_fold_multi(const uint16_t *x, const int32_t *indices,
                                  int32_t n_slots, int32_t k_in, int32_t max_rank, int32_t n_out,
                                  int32_t top_k, int32_t n_experts, int32_t n_adapters) {
     if (max_rank > 1024 || top_k < 1 || n_adapters < 1) return OR_NONE;
+#pragma omp parallel for schedule(dynamic, 8)
     for (int32_t row = 0; row < n_slots; ++row) {
         const uint16_t *base_row = base_in + (int64_t)row * n_out;
         double *ref_row = ref_out + (int64_t)row * n_out;
@@ -318,6 +341,7 @@ int32_t oracle_grouped_fold(const uint16_t *x, const int32_t *expert_offsets, co
         int64_t lo = expert_offsets[e] > row_offset ? expert_offsets[e] : row_offset;
         int64_t hi = expert_offsets[e + 1] < row_end ? expert_offsets[e + 1] : row_end;
         if (!expert_folds(e, n_experts, a_table, b_table)) continue;
+#pragma omp parallel for schedule(dynamic, 8)
         for (int64_t r = lo; r < hi; ++r) {
             int32_t t = src[r] / top_k;
             if (row_adapter != NULL && row_adapter[t] < 0) continue;
@@ -354,6 +378,7 @@ int32_t oracle_grouped_fold_xrows(const uint16_t *x_rows, const int32_t *expert_
         int64_t lo = expert_offsets[e] > row_offset ? expert_offsets[e] : row_offset;
         int64_t hi = expert_offsets[e + 1] < row_end ? expert_offsets[e + 1] : row_end;
         if (!expert_folds(e, n_experts, a_table, b_table)) continue;
+#pragma omp parallel for schedule(dynamic, 8)
         for (int64_t r = lo; r < hi; ++r) {
             if (row_adapter != NULL && row_adapter[src[r] / top_k] < 0) continue;
             fold_one_row(x_rows + r * k_in, (const uint16_t *)(uintptr_t)a_table[e],
@@ -373,6 +398,7 @@ int32_t oracle_router_fold(const uint16_t *x, const int32_t *row_adapter, const 
                            const uint16_t *base_in, double *ref_out, uint8_t *folded,
                            int32_t n_tokens, int32_t k_in, int32_t max_rank, int32_t n_out) {
     if (max_rank > 1024) return OR_NONE;
+#pragma omp parallel for schedule(dynamic, 8)
     for (int32_t t = 0; t < n_tokens; ++t) {
         const uint16_t *base_row = base_in + (int64_t)t * n_out;
         double *ref_row = ref_out + (int64_t)t * n_out;
@@ -399,6 +425,7 @@ int32_t oracle_gather_fold_rows(const uint16_t *x, const int32_t *indices,
                                 double *ref_out, uint8_t *folded, int32_t k_in, int32_t max_rank,
                                 int32_t n_out, int32_t top_k, int32_t n_experts) {
     if (max_rank > 1024 || top_k < 1) return OR_NONE;
+#pragma omp parallel for schedule(dynamic, 8)
     for (int32_t i = 0; i < n_rows; ++i) {
         int32_t row = rows[i];
         int32_t t = row / top_k;
@@ -429,6 +456,7 @@ int32_t oracle_grouped_fold_rows(const uint16_t *x, const int32_t *expert_offset
                                  int32_t top_k, int32_t n_experts, int32_t row_offset,
                                  int32_t row_end) {
     if (max_rank > 1024 || top_k < 1) return OR_NONE;
+#pragma omp parallel for schedule(dynamic, 8)
     for (int32_t i = 0; i < n_rows; ++i) {
         int32_t r = rows[i];
         const uint16_t *base_row = base_rows + (int64_t)i * n_out;
@@ -466,6 +494,7 @@ int32_t oracle_grouped_fold_xrows_rows(const uint16_t *x_rows, const int32_t *ex
                                        int32_t n_out, int32_t top_k, int32_t n_experts,
                                        int32_t row_offset, int32_t row_end) {
     if (max_rank > 1024 || top_k < 1) return OR_NONE;
+#pragma omp parallel for schedule(dynamic, 8)
     for (int32_t i = 0; i < n_rows; ++i) {
         int32_t r = rows[i];
         const uint16_t *base_row = base_rows + (int64_t)i * n_out;

@@ -8,6 +8,16 @@ Comparison rules (the fold's contract):
 The 4e-3 bound: the output is one round-to-nearest-even to bf16 (half an ulp,
 2^-9 relative = 1.95e-3 of |ref| at most, 3.9e-3 absolute just below 2), so
 the fp32 arithmetic before the rounding may add up to ~9e-5 at |ref| ~ 1.
+
+That bound alone cannot tell a good pre-rounding value from a poor one: the
+final rounding's half ulp dominates it.  So every check also compares each
+folded element with RNE_bf16(ref), the correctly rounded exact value.  An
+element may differ from it only when ref lies within RNE_BAND * max(1, |ref|)
+of a rounding boundary (the midpoint between two adjacent bf16 values): an
+fp32 result a little off the exact value can fall on the other side of such
+a midpoint, nothing else can.  With h carried in fp32 (or as bf16 hi + lo,
+~2^-18 relative) the pre-rounding error of these workloads is ~1e-5 or less;
+h rounded to bf16 would err by ~2^-9 * |delta| (~1e-3), far outside the band.
 """
 from __future__ import annotations
 
@@ -17,6 +27,22 @@ import oracle
 from lora_moe_expert_gb300 import synth
 
 TOL = 4e-3
+RNE_BAND = 2.0 ** -14
+
+
+def rne_bf16_f64(ref: np.ndarray) -> np.ndarray:
+    """bf16 bits of fp64 values rounded to nearest-even, and each value's
+    distance to the nearest bf16 rounding boundary (midpoint).  The fp64 ->
+    fp32 step can only move a value onto a midpoint from within one fp32 ulp
+    of it, and such values lie inside any band the checks use."""
+    ref = np.asarray(ref, np.float64)
+    f32 = ref.astype(np.float32)
+    bits = synth.bf16_bits(f32)
+    u = f32.view(np.uint32)
+    lo = (u & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
+    hi = ((u & np.uint32(0xFFFF0000)) + np.uint32(0x10000)).view(np.float32).astype(np.float64)
+    mid = 0.5 * (lo + hi)
+    return bits, np.abs(ref - mid)
 
 
 def oracle_reference(w, o=None, row_offset=None, row_end=None):
@@ -55,8 +81,10 @@ def oracle_reference(w, o=None, row_offset=None, row_end=None):
 
 
 def check_fold(out_bits: np.ndarray, base_bits: np.ndarray, ref: np.ndarray,
-               folded: np.ndarray, tol: float = TOL) -> dict:
-    """Assert the comparison rules; returns error statistics."""
+               folded: np.ndarray, tol: float = TOL, band: float = RNE_BAND) -> dict:
+    """Assert the comparison rules; returns error statistics (rne_mismatch: folded
+    elements whose bits differ from RNE_bf16(ref), each within the band of a
+    rounding boundary)."""
     out_bits = np.asarray(out_bits, np.uint16)
     base_bits = np.asarray(base_bits, np.uint16)
     assert out_bits.shape == ref.shape == base_bits.shape
@@ -77,4 +105,14 @@ def check_fold(out_bits: np.ndarray, base_bits: np.ndarray, ref: np.ndarray,
             f"out={out.flat[worst]!r} ref={r.flat[worst]!r}")
         stats["max_err"] = float(err.max())
         stats["max_rel"] = float((err / bound).max())
+        rne, mid_dist = rne_bf16_f64(r)
+        miss = out_bits[folded] != rne
+        near = mid_dist <= band * np.maximum(1.0, np.abs(r))
+        far = miss & ~near
+        assert not far.any(), (
+            f"{int(far.sum())} folded elements differ from RNE_bf16(ref) away from a rounding "
+            f"boundary; first ref={r[far][0]!r} out={out[far][0]!r}")
+        stats["rne_mismatch"] = int(miss.sum())
+        stats["rne_mismatch_max_dist"] = float(
+            (mid_dist[miss] / np.maximum(1.0, np.abs(r[miss]))).max()) if miss.any() else 0.0
     return stats

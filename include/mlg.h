@@ -32,6 +32,22 @@
  *    enqueue only on the stream they are given, so each can be captured in a
  *    CUDA graph.  `stream` is a cudaStream_t passed as void* (0 = the legacy
  *    default stream).
+ *  - Early start (programmatic dependent launch).  Every fold kernel may
+ *    start while the kernel before it in the stream is still running and
+ *    waits for that kernel's completion (and the visibility of its writes)
+ *    before it reads the routing (indices, expert_offsets, src), the row map,
+ *    x or base_out, so those may be written by the preceding kernel.  The
+ *    grouped and router folds read everything else after that wait too.  The
+ *    decode folds (mlg_gather_bgmv, mlg_gather_bgmv_multi) do NOT: they read
+ *    a_table, b_table, scale_table and the A_e / B_e pairs those tables
+ *    point to BEFORE the wait, to overlap the pair traffic with the preceding
+ *    kernel.  Tables and pairs written by a copy (cudaMemcpy*, as the upload
+ *    helpers do) are safe, because a copy is never overlapped; a caller whose
+ *    preceding KERNEL writes the tables or the pair weights (a device-side
+ *    adapter install or rotation, a dequantisation kernel) must call
+ *    mlg_gather_bgmv_ex / mlg_gather_bgmv_multi_ex with
+ *    MLG_FOLD_AFTER_PRECEDING, which launches the fold without early start,
+ *    or it may fold stale tables or weights with no error reported.
  *  - All arguments are validated on the host before anything is enqueued or
  *    written; on any error nothing is launched and no output is written.
  *  - Device arrays are row-major.  bf16 values are raw IEEE bfloat16 bit
@@ -43,9 +59,13 @@
  *    fault on table contents they can check).  A non-zero, aligned cell must
  *    hold the device address of an array of the stated shape.
  *  - Rows that do not fold keep their input bits exactly (including -0.0).
- *  - Arithmetic: bf16 inputs, fp32 products and sums, the rank-r
- *    intermediate h kept in fp32 (never rounded to bf16), and one
- *    round-to-nearest-even to bf16 of base + scale * delta per element.
+ *  - Arithmetic: bf16 inputs, fp32 products and sums, and one
+ *    round-to-nearest-even to bf16 of base + scale * delta per element.  The
+ *    rank-r intermediate h is accumulated in fp32 and enters the expand
+ *    (a bf16 tensor-core product) as the sum of two bf16 values, hi = bf16(h)
+ *    and lo = bf16(h - hi): |h - hi - lo| <= 2^-18 |h|, so h is never
+ *    rounded to a single bf16 and the expand sees it at about fp32's
+ *    precision (2^-18 against fp32's 2^-24 relative).
  */
 #ifndef MLG_H_
 #define MLG_H_
@@ -162,6 +182,32 @@ MLG_API mlg_status mlg_gather_bgmv_multi(const mlg_bf16 *x, const int32_t *indic
                                          mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
                                          int32_t max_rank, int32_t n_out, int32_t top_k,
                                          int32_t n_experts, int32_t n_adapters, void *stream);
+
+/* Launch flags of the _ex decode entry points.
+ *   MLG_FOLD_AFTER_PRECEDING  launch without early start: the fold begins
+ *                             only once the preceding work in the stream has
+ *                             completed, so it may read tables and A_e / B_e
+ *                             pairs that the preceding kernel wrote (see
+ *                             "Early start" above).  Costs the overlap of
+ *                             the pair traffic with that kernel. */
+#define MLG_FOLD_AFTER_PRECEDING 1u
+
+/* mlg_gather_bgmv and mlg_gather_bgmv_multi with launch flags (0 or
+ * MLG_FOLD_AFTER_PRECEDING); with flags == 0 they are exactly the calls
+ * above.  Errors as for those calls, plus INVALID_ARG for an unknown flag. */
+MLG_API mlg_status mlg_gather_bgmv_ex(const mlg_bf16 *x, const int32_t *indices,
+                                      const int32_t *row_adapter, const uint64_t *a_table,
+                                      const uint64_t *b_table, const float *scale_table,
+                                      mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
+                                      int32_t max_rank, int32_t n_out, int32_t top_k,
+                                      int32_t n_experts, uint32_t flags, void *stream);
+MLG_API mlg_status mlg_gather_bgmv_multi_ex(const mlg_bf16 *x, const int32_t *indices,
+                                            const int32_t *row_adapter, const uint64_t *a_table,
+                                            const uint64_t *b_table, const float *scale_table,
+                                            mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
+                                            int32_t max_rank, int32_t n_out, int32_t top_k,
+                                            int32_t n_experts, int32_t n_adapters,
+                                            uint32_t flags, void *stream);
 
 /* moe_lora_grouped_down (moe_lora_grouped module index): the prefill-side fold
  * over expert-sorted rows r in the window [row_offset, row_end).  e is the
@@ -303,7 +349,10 @@ MLG_API mlg_status mlg_pack_expert_tables(const mlg_expert_entry *entries, size_
 
 /* Table upload: three cudaMemcpyAsync host-to-device copies of n_experts
  * entries on `stream`.  Staging in pinned memory is the caller's choice; with
- * pageable memory the copies are synchronous with respect to the host.
+ * pageable memory the copies are synchronous with respect to the host.  A
+ * fold enqueued after these copies always sees the new tables (copies are
+ * never overlapped by a fold's early start); tables written by a kernel need
+ * MLG_FOLD_AFTER_PRECEDING on the decode folds.
  * Errors: INVALID_ARG (NULL), CUDA. */
 MLG_API mlg_status mlg_upload_expert_tables(const uint64_t *a_host, const uint64_t *b_host,
                                     const float *scale_host, uint32_t n_experts,
@@ -349,39 +398,16 @@ MLG_API int32_t mlg_version(void);
  * of trapping: MLG_DEVERR_WAIT_TIMEOUT (a wait for a copy or an MMA ran past
  * its one-second limit; the kernel stopped issuing work and the affected rows
  * may be unfolded), MLG_DEVERR_TMEM_ALLOC (tensor memory could not be
- * allocated; the affected tiles were not folded).  Reads the OR of all bits
+ * allocated; the affected tiles were not folded), MLG_DEVERR_UNIT_DROPPED (a
+ * multi-adapter decode CTA was dealt more cells than it holds and left the
+ * excess unfolded; the launch-time shape check is meant to rule this out).
+ * Reads the OR of all bits
  * since the last clear into *flags_out and clears them when `clear` is
  * non-zero.  Synchronous (a device-to-host copy); not for the hot path. */
 #define MLG_DEVERR_WAIT_TIMEOUT 1u
 #define MLG_DEVERR_TMEM_ALLOC 2u
+#define MLG_DEVERR_UNIT_DROPPED 4u
 MLG_API mlg_status mlg_read_device_errors(uint32_t *flags_out, int32_t clear);
-
-/* Launch-shape knobs for benchmarking sweeps; 0 restores the automatic
- * choice.  Process-wide; set them only while no other thread launches folds.
- *   MLG_TUNE_GATHER_CLUSTER   CTAs per expert cluster of mlg_gather_bgmv (1, 2, 4, 8):
- *                             the cluster splits k_in (partial h summed on chip) and n_out
- *   MLG_TUNE_GATHER_NSPLIT    independent CTAs per expert and cluster rank of
- *                             mlg_gather_bgmv (1, 2, 4, 8): each computes all of h
- *                             and folds its own n_out slice
- *   MLG_TUNE_GROUPED_CTAS     persistent CTAs of the grouped and router folds
- *   MLG_TUNE_GATHER_PATH      kernel of mlg_gather_bgmv: 1 = one CTA per expert holding
- *                             the whole pair (max_rank 16 or 32, n_out <= 2048, the pair in
- *                             half an SM, n_experts <= SM count; else the fold returns
- *                             UNSUPPORTED), 2 = the cluster kernel (any shape)
- *   MLG_TUNE_GATHER_SPECULATION  row lists of the resident-pair kernel: 0 = scanned before
- *                             the preceding kernel completes and checked after it, 1 = scanned
- *                             after it only, 2 = the early scan reads another expert's rows so
- *                             that every check fails and the rows are requested again (a test
- *                             of that path; results are the same in all three modes).  In the
- *                             multi-adapter form the same modes pick the first cell whose pair
- *                             loads before the wait (2: another CTA's cell)
- * Errors: INVALID_ARG for an unknown knob or a value out of range. */
-#define MLG_TUNE_GATHER_CLUSTER 1
-#define MLG_TUNE_GROUPED_CTAS 2
-#define MLG_TUNE_GATHER_NSPLIT 3
-#define MLG_TUNE_GATHER_PATH 4
-#define MLG_TUNE_GATHER_SPECULATION 5
-MLG_API mlg_status mlg_set_tuning(int32_t knob, int32_t value);
 
 #ifdef __cplusplus
 }

@@ -29,11 +29,13 @@ MLG_ERR_BUFFER_TOO_SMALL = -6
 MLG_ERR_CUDA = -7
 MLG_ROUTE_FOLD, MLG_ROUTE_SKIP, MLG_ROUTE_REFUSE = 0, 1, 2
 MLG_MAX_RANK = 64
-MLG_TUNE_GATHER_CLUSTER = 1
-MLG_TUNE_GROUPED_CTAS = 2
-MLG_TUNE_GATHER_NSPLIT = 3
-MLG_TUNE_GATHER_PATH = 4
-MLG_TUNE_GATHER_SPECULATION = 5
+MLG_FOLD_AFTER_PRECEDING = 1
+# test and benchmark hooks (include/mlg_test.h; not part of the public interface)
+MLG_TEST_GATHER_CLUSTER = 1
+MLG_TEST_GROUPED_CTAS = 2
+MLG_TEST_GATHER_NSPLIT = 3
+MLG_TEST_GATHER_PATH = 4
+MLG_TEST_GATHER_SPECULATION = 5
 
 
 class MlgError(RuntimeError):
@@ -56,6 +58,8 @@ class Window(ctypes.Structure):
 _p, _i32, _u32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
 _SIGNATURES = {
     "mlg_gather_bgmv": ([_p] * 7 + [_i32] * 6 + [_p], _i32),
+    "mlg_gather_bgmv_ex": ([_p] * 7 + [_i32] * 6 + [_u32, _p], _i32),
+    "mlg_gather_bgmv_multi_ex": ([_p] * 7 + [_i32] * 7 + [_u32, _p], _i32),
     "mlg_grouped_down": ([_p] * 8 + [_i32] * 7 + [_p], _i32),
     "mlg_router_fold": ([_p] * 6 + [_i32] * 4 + [_p], _i32),
     "mlg_grouped_down_all_windows": ([_p] * 8 + [_i32] * 6 + [_u32, _p], _i32),
@@ -77,7 +81,7 @@ _SIGNATURES = {
     "mlg_last_cuda_error": ([], _i32),
     "mlg_version": ([], _i32),
     "mlg_read_device_errors": ([_p, _i32], _i32),
-    "mlg_set_tuning": ([_i32, _i32], _i32),
+    "mlg_test_set_knob": ([_i32, _i32], _i32),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -138,6 +142,26 @@ def mlg_gather_bgmv(x, indices, row_adapter, a_table, b_table, scale_table, base
                                  _addr(b_table), _addr(scale_table), _addr(base_out), n_slots,
                                  k_in, max_rank, n_out, top_k, n_experts, _stream(stream)),
            "mlg_gather_bgmv")
+
+
+def mlg_gather_bgmv_ex(x, indices, row_adapter, a_table, b_table, scale_table, base_out,
+                       n_slots, k_in, max_rank, n_out, top_k, n_experts, flags,
+                       stream=None) -> None:
+    _check(lib().mlg_gather_bgmv_ex(_addr(x), _addr(indices), _addr(row_adapter),
+                                    _addr(a_table), _addr(b_table), _addr(scale_table),
+                                    _addr(base_out), n_slots, k_in, max_rank, n_out, top_k,
+                                    n_experts, flags, _stream(stream)),
+           "mlg_gather_bgmv_ex")
+
+
+def mlg_gather_bgmv_multi_ex(x, indices, row_adapter, a_table, b_table, scale_table, base_out,
+                             n_slots, k_in, max_rank, n_out, top_k, n_experts, n_adapters,
+                             flags, stream=None) -> None:
+    _check(lib().mlg_gather_bgmv_multi_ex(_addr(x), _addr(indices), _addr(row_adapter),
+                                          _addr(a_table), _addr(b_table), _addr(scale_table),
+                                          _addr(base_out), n_slots, k_in, max_rank, n_out,
+                                          top_k, n_experts, n_adapters, flags, _stream(stream)),
+           "mlg_gather_bgmv_multi_ex")
 
 
 def mlg_gather_bgmv_multi(x, indices, row_adapter, a_table, b_table, scale_table, base_out,
@@ -308,5 +332,7 @@ def mlg_read_device_errors(clear: bool = True) -> int:
     return v.value
 
 
-def mlg_set_tuning(knob: int, value: int) -> None:
-    _check(lib().mlg_set_tuning(knob, value), "mlg_set_tuning")
+def mlg_test_set_knob(knob: int, value: int) -> None:
+    """Test / benchmark hook (include/mlg_test.h): process-wide, not thread-safe;
+    results never depend on it."""
+    _check(lib().mlg_test_set_knob(knob, value), "mlg_test_set_knob")

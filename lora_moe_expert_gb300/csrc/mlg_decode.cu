@@ -796,10 +796,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
         }
         __syncthreads();
       }
-      if (!halves) return n_hit > me ? min(kMaxUnits, (n_hit - 1 - me) / G + 1) : 0;
+      // The count before clamping to s_units: the host's eligibility check
+      // keeps it within kMaxUnits; a larger one is recorded, not hidden.
+      if (!halves) return n_hit > me ? (n_hit - 1 - me) / G + 1 : 0;
       const int extra = 2 * max(0, n_hit - G);  // half units past the first round
-      const int mine = (n_hit > me ? 1 : 0) + (extra > me ? (extra - 1 - me) / G + 1 : 0);
-      return min(kMaxUnits, mine);
+      return (n_hit > me ? 1 : 0) + (extra > me ? (extra - 1 - me) / G + 1 : 0);
     };
     // (spec_mode 1: no speculation; 2: another CTA's first cell, so that the
     // check after the wait fails)
@@ -811,6 +812,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     const bool snap = spec && p.spec_mode == 0 && p.n_slots <= kScanChunk;
     if (snap) scan_load(p, 0, idx_s, ra_s);
     int n_mine = spec ? deal_units(p.spec_mode == 2 ? (me + 1) % G : me, idx_s, ra_s, snap) : 0;
+    const int n_mine_spec = n_mine;
+    n_mine = min(kMaxUnits, n_mine);
     const int e_spec = n_mine > 0 ? s_units[0] : -1;
     bool spec_pair = false;
     int ns = 0;  // rows of the first cell (first kSpecRows of them in s_spec)
@@ -847,7 +850,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       for (int i = 0; i < kScanPer; ++i) same = same && idx0[i] == idx_s[i] && ra0[i] == ra_s[i];
       same = !__syncthreads_or(!same);
     }
-    if (!same) n_mine = deal_units(me, no_idx, no_idx, false);
+    const int n_dealt = same ? n_mine_spec : deal_units(me, no_idx, no_idx, false);
+    if (n_dealt > kMaxUnits && tid == 0) record_error(kErrUnitDropped);
+    n_mine = min(kMaxUnits, n_dealt);
     for (int u = 0; u < n_mine && !bad; ++u) {
       e = s_units[u] & 0x0fffffff;
       const int half = (s_units[u] >> 28) - 1;  // -1: the whole cell
@@ -913,7 +918,7 @@ uint32_t layout(DecodeParams &p, int rp) {
 }
 
 template <int RP, bool MULTI>
-cudaError_t launch(const DecodeParams &p, int grid, cudaStream_t stream) {
+cudaError_t launch(const DecodeParams &p, int grid, bool early, cudaStream_t stream) {
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
   int dev = 0;
@@ -933,7 +938,7 @@ cudaError_t launch(const DecodeParams &p, int grid, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = early ? 1 : 0;  // without early start griddepcontrol.wait returns at once
   return cudaLaunchKernelEx(&cfg, decode_fold_kernel<RP, MULTI>, p);
 }
 
@@ -972,7 +977,15 @@ bool decode_fold_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t
 bool decode_multi_eligible(int32_t k_in, int32_t max_rank, int32_t n_out, int32_t n_cells) {
   if (max_rank != 16 && max_rank != 32) return false;
   if (n_out > kMaxBlocks * kWarps * 64) return false;
-  if (n_cells > kMaxUnits * 2 * sm_count() || n_cells > kMaxCells) return false;
+  if (n_cells > kMaxCells) return false;
+  // Units of one CTA when every cell is hit: one cell per CTA in the first
+  // round, then (n_out a multiple of 128) two column halves per further cell
+  // dealt round-robin, else whole cells round-robin.
+  const int64_t G = 2 * static_cast<int64_t>(sm_count());
+  const int64_t worst = n_out % 128 == 0
+                            ? (n_cells > G ? 1 + (2 * (n_cells - G) + G - 1) / G : 1)
+                            : (n_cells + G - 1) / G;
+  if (worst > kMaxUnits) return false;
   if (static_cast<int64_t>(n_cells) * 4 > kWarps * kRows * (max_rank + 4) * 4) return false;
   DecodeParams p = {};
   p.k_in = k_in;
@@ -986,7 +999,7 @@ cudaError_t decode_fold_launch(const uint16_t *x, const int32_t *indices,
                                uint16_t *base_out, int32_t n_slots, int32_t k_in,
                                int32_t max_rank, int32_t n_out, int32_t top_k,
                                int32_t n_cells, int32_t e_model, int32_t n_adapters,
-                               cudaStream_t stream) {
+                               bool early, cudaStream_t stream) {
   DecodeParams p = {};
   p.x = x;
   p.indices = indices;
@@ -1006,10 +1019,12 @@ cudaError_t decode_fold_launch(const uint16_t *x, const int32_t *indices,
   layout(p, max_rank);
   if (n_adapters > 0) {  // cells dealt to two CTAs per SM
     const int grid = 2 * sm_count();
-    return max_rank == 16 ? launch<16, true>(p, grid, stream) : launch<32, true>(p, grid, stream);
+    return max_rank == 16 ? launch<16, true>(p, grid, early, stream)
+                          : launch<32, true>(p, grid, early, stream);
   }
   const int grid = decode_grid();  // owners, then helpers for experts with many rows
-  return max_rank == 16 ? launch<16, false>(p, grid, stream) : launch<32, false>(p, grid, stream);
+  return max_rank == 16 ? launch<16, false>(p, grid, early, stream)
+                        : launch<32, false>(p, grid, early, stream);
 }
 
 }  // namespace mlg

@@ -683,7 +683,7 @@ constexpr uint32_t kSmemTwoPerSm = 113 * 1024 - 3072;
 constexpr uint32_t kSmemLimit = 227 * 1024 - 3072;  // leaves room for the static part
 
 template <int RP>
-cudaError_t launch(const GatherParams &p, int cs, int clusters, cudaStream_t stream) {
+cudaError_t launch(const GatherParams &p, int cs, int clusters, bool early, cudaStream_t stream) {
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
   int dev = 0;
@@ -707,7 +707,7 @@ cudaError_t launch(const GatherParams &p, int cs, int clusters, cudaStream_t str
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = early ? 2 : 1;  // without early start griddepcontrol.wait returns at once
   return cudaLaunchKernelEx(&cfg, gather_fold_kernel<RP>, p);
 }
 
@@ -751,7 +751,10 @@ mlg_status gather_dispatch(const mlg_bf16 *x, const int32_t *indices, const int3
                            const uint64_t *a_table, const uint64_t *b_table,
                            const float *scale_table, mlg_bf16 *base_out, int32_t n_slots,
                            int32_t k_in, int32_t max_rank, int32_t n_out, int32_t top_k,
-                           int32_t n_experts, int32_t e_model, int32_t n_adapters, void *stream) {
+                           int32_t n_experts, int32_t e_model, int32_t n_adapters,
+                           uint32_t flags, void *stream) {
+  if ((flags & ~MLG_FOLD_AFTER_PRECEDING) != 0) return MLG_ERR_INVALID_ARG;
+  const bool early = (flags & MLG_FOLD_AFTER_PRECEDING) == 0;
   if (n_slots == 0 || n_experts == 0) return MLG_OK;
   if (!x || !indices || !row_adapter || !a_table || !b_table || !scale_table || !base_out)
     return MLG_ERR_INVALID_ARG;
@@ -765,7 +768,7 @@ mlg_status gather_dispatch(const mlg_bf16 *x, const int32_t *indices, const int3
   if (path != 2 && resident)
     return cuda_status(decode_fold_launch(x, indices, row_adapter, a_table, b_table, scale_table,
                                           base_out, n_slots, k_in, max_rank, n_out, top_k,
-                                          n_experts, e_model, n_adapters,
+                                          n_experts, e_model, n_adapters, early,
                                           static_cast<cudaStream_t>(stream)));
 
   GatherParams p = {};
@@ -816,10 +819,10 @@ mlg_status gather_dispatch(const mlg_bf16 *x, const int32_t *indices, const int3
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   switch (rp) {
-    case 16: err = launch<16>(p, cs, clusters, s); break;
-    case 32: err = launch<32>(p, cs, clusters, s); break;
-    case 48: err = launch<48>(p, cs, clusters, s); break;
-    default: err = launch<64>(p, cs, clusters, s); break;
+    case 16: err = launch<16>(p, cs, clusters, early, s); break;
+    case 32: err = launch<32>(p, cs, clusters, early, s); break;
+    case 48: err = launch<48>(p, cs, clusters, early, s); break;
+    default: err = launch<64>(p, cs, clusters, early, s); break;
   }
   return cuda_status(err);
 }
@@ -827,26 +830,27 @@ mlg_status gather_dispatch(const mlg_bf16 *x, const int32_t *indices, const int3
 }  // namespace
 }  // namespace mlg
 
-extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
-                                      const int32_t *row_adapter, const uint64_t *a_table,
-                                      const uint64_t *b_table, const float *scale_table,
-                                      mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
-                                      int32_t max_rank, int32_t n_out, int32_t top_k,
-                                      int32_t n_experts, void *stream) {
+namespace {
+
+mlg_status gather_single(const mlg_bf16 *x, const int32_t *indices, const int32_t *row_adapter,
+                         const uint64_t *a_table, const uint64_t *b_table,
+                         const float *scale_table, mlg_bf16 *base_out, int32_t n_slots,
+                         int32_t k_in, int32_t max_rank, int32_t n_out, int32_t top_k,
+                         int32_t n_experts, uint32_t flags, void *stream) {
   using namespace mlg;
   if (n_slots < 0 || n_experts < 0 || top_k < 1) return MLG_ERR_INVALID_ARG;
   const mlg_status shape = check_shapes(k_in, max_rank, n_out);
   if (shape != MLG_OK) return shape;
   return gather_dispatch(x, indices, row_adapter, a_table, b_table, scale_table, base_out,
-                         n_slots, k_in, max_rank, n_out, top_k, n_experts, n_experts, 0, stream);
+                         n_slots, k_in, max_rank, n_out, top_k, n_experts, n_experts, 0, flags,
+                         stream);
 }
 
-extern "C" mlg_status mlg_gather_bgmv_multi(const mlg_bf16 *x, const int32_t *indices,
-                                            const int32_t *row_adapter, const uint64_t *a_table,
-                                            const uint64_t *b_table, const float *scale_table,
-                                            mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
-                                            int32_t max_rank, int32_t n_out, int32_t top_k,
-                                            int32_t n_experts, int32_t n_adapters, void *stream) {
+mlg_status gather_multi(const mlg_bf16 *x, const int32_t *indices, const int32_t *row_adapter,
+                        const uint64_t *a_table, const uint64_t *b_table, const float *scale_table,
+                        mlg_bf16 *base_out, int32_t n_slots, int32_t k_in, int32_t max_rank,
+                        int32_t n_out, int32_t top_k, int32_t n_experts, int32_t n_adapters,
+                        uint32_t flags, void *stream) {
   using namespace mlg;
   if (n_slots < 0 || n_experts < 0 || n_adapters < 1 || top_k < 1) return MLG_ERR_INVALID_ARG;
   const int64_t cells = static_cast<int64_t>(n_experts) * n_adapters;
@@ -855,5 +859,48 @@ extern "C" mlg_status mlg_gather_bgmv_multi(const mlg_bf16 *x, const int32_t *in
   if (shape != MLG_OK) return shape;
   return gather_dispatch(x, indices, row_adapter, a_table, b_table, scale_table, base_out,
                          n_slots, k_in, max_rank, n_out, top_k, static_cast<int32_t>(cells),
-                         n_experts, n_adapters, stream);
+                         n_experts, n_adapters, flags, stream);
+}
+
+}  // namespace
+
+extern "C" mlg_status mlg_gather_bgmv(const mlg_bf16 *x, const int32_t *indices,
+                                      const int32_t *row_adapter, const uint64_t *a_table,
+                                      const uint64_t *b_table, const float *scale_table,
+                                      mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
+                                      int32_t max_rank, int32_t n_out, int32_t top_k,
+                                      int32_t n_experts, void *stream) {
+  return gather_single(x, indices, row_adapter, a_table, b_table, scale_table, base_out, n_slots,
+                       k_in, max_rank, n_out, top_k, n_experts, 0u, stream);
+}
+
+extern "C" mlg_status mlg_gather_bgmv_ex(const mlg_bf16 *x, const int32_t *indices,
+                                         const int32_t *row_adapter, const uint64_t *a_table,
+                                         const uint64_t *b_table, const float *scale_table,
+                                         mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
+                                         int32_t max_rank, int32_t n_out, int32_t top_k,
+                                         int32_t n_experts, uint32_t flags, void *stream) {
+  return gather_single(x, indices, row_adapter, a_table, b_table, scale_table, base_out, n_slots,
+                       k_in, max_rank, n_out, top_k, n_experts, flags, stream);
+}
+
+extern "C" mlg_status mlg_gather_bgmv_multi(const mlg_bf16 *x, const int32_t *indices,
+                                            const int32_t *row_adapter, const uint64_t *a_table,
+                                            const uint64_t *b_table, const float *scale_table,
+                                            mlg_bf16 *base_out, int32_t n_slots, int32_t k_in,
+                                            int32_t max_rank, int32_t n_out, int32_t top_k,
+                                            int32_t n_experts, int32_t n_adapters, void *stream) {
+  return gather_multi(x, indices, row_adapter, a_table, b_table, scale_table, base_out, n_slots,
+                      k_in, max_rank, n_out, top_k, n_experts, n_adapters, 0u, stream);
+}
+
+extern "C" mlg_status mlg_gather_bgmv_multi_ex(const mlg_bf16 *x, const int32_t *indices,
+                                               const int32_t *row_adapter,
+                                               const uint64_t *a_table, const uint64_t *b_table,
+                                               const float *scale_table, mlg_bf16 *base_out,
+                                               int32_t n_slots, int32_t k_in, int32_t max_rank,
+                                               int32_t n_out, int32_t top_k, int32_t n_experts,
+                                               int32_t n_adapters, uint32_t flags, void *stream) {
+  return gather_multi(x, indices, row_adapter, a_table, b_table, scale_table, base_out, n_slots,
+                      k_in, max_rank, n_out, top_k, n_experts, n_adapters, flags, stream);
 }

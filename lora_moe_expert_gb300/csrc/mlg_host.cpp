@@ -14,6 +14,7 @@
 
 #include "mlg.h"
 #include "mlg_internal.h"
+#include "mlg_test.h"
 
 namespace mlg {
 thread_local int32_t g_last_cuda_error = 0;
@@ -77,23 +78,27 @@ mlg_status mlg_build_moe_row_adapter_decode_multi(const int32_t *adapter_slots, 
   return MLG_OK;
 }
 
+// build_moe_row_adapter_host (moe_row_adapter.rs): the prefill map gives
+// every token of stream b the stream's adapter slot.  The boundaries must be
+// a valid prefix sum -- at least two of them, one slot per stream, starting
+// at 0 and never decreasing (so none is negative) -- or the page returns
+// None, here INVALID_ARG with nothing written.
 mlg_status mlg_build_moe_row_adapter_host(const int32_t *cu_seqlens, size_t n_cu,
                                           const int32_t *adapter_slots, size_t n_slots,
                                           int32_t *out, size_t cap, size_t *total_out) {
-  if (n_cu < 2 || cu_seqlens == nullptr) return MLG_ERR_INVALID_ARG;
-  const size_t batch = n_cu - 1;
-  if (n_slots != batch || adapter_slots == nullptr) return MLG_ERR_INVALID_ARG;
-  if (cu_seqlens[0] != 0) return MLG_ERR_INVALID_ARG;
-  // Every boundary is checked before the map is sized from the last one.
-  for (size_t b = 0; b < batch; ++b)
-    if (cu_seqlens[b] < 0 || cu_seqlens[b + 1] < cu_seqlens[b]) return MLG_ERR_INVALID_ARG;
-  const size_t total = static_cast<size_t>(cu_seqlens[batch]);
-  if (total_out != nullptr) *total_out = total;
-  if (cap < total) return MLG_ERR_BUFFER_TOO_SMALL;
-  if (total > 0 && out == nullptr) return MLG_ERR_INVALID_ARG;
-  for (size_t b = 0; b < batch; ++b) {
-    const int32_t slot = adapter_slots[b];
-    for (int32_t r = cu_seqlens[b]; r < cu_seqlens[b + 1]; ++r) out[r] = slot;
+  if (cu_seqlens == nullptr || adapter_slots == nullptr) return MLG_ERR_INVALID_ARG;
+  if (n_cu < 2 || n_slots + 1 != n_cu || cu_seqlens[0] != 0) return MLG_ERR_INVALID_ARG;
+  int32_t prev = 0;
+  for (size_t i = 1; i < n_cu; prev = cu_seqlens[i++])
+    if (cu_seqlens[i] < prev) return MLG_ERR_INVALID_ARG;
+  const size_t tokens = static_cast<size_t>(prev);
+  if (total_out != nullptr) *total_out = tokens;
+  if (cap < tokens) return MLG_ERR_BUFFER_TOO_SMALL;
+  if (tokens > 0 && out == nullptr) return MLG_ERR_INVALID_ARG;
+  size_t stream = 0;  // the stream whose [cu[b], cu[b+1]) holds token t
+  for (size_t t = 0; t < tokens; ++t) {
+    while (static_cast<size_t>(cu_seqlens[stream + 1]) <= t) ++stream;
+    out[t] = adapter_slots[stream];
   }
   return MLG_OK;
 }
@@ -224,27 +229,27 @@ extern "C" mlg_status mlg_read_device_errors(uint32_t *flags_out, int32_t clear)
   return MLG_OK;
 }
 
-extern "C" mlg_status mlg_set_tuning(int32_t knob, int32_t value) {
+extern "C" mlg_status mlg_test_set_knob(int32_t knob, int32_t value) {
   switch (knob) {
-    case MLG_TUNE_GATHER_CLUSTER:
+    case MLG_TEST_GATHER_CLUSTER:
       if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
         return MLG_ERR_INVALID_ARG;
       mlg::gather_set_cluster_override(value);
       return MLG_OK;
-    case MLG_TUNE_GATHER_NSPLIT:
+    case MLG_TEST_GATHER_NSPLIT:
       if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
         return MLG_ERR_INVALID_ARG;
       mlg::gather_set_nsplit_override(value);
       return MLG_OK;
-    case MLG_TUNE_GATHER_PATH:
+    case MLG_TEST_GATHER_PATH:
       if (value < 0 || value > 2) return MLG_ERR_INVALID_ARG;
       mlg::gather_set_path_override(value);
       return MLG_OK;
-    case MLG_TUNE_GATHER_SPECULATION:
+    case MLG_TEST_GATHER_SPECULATION:
       if (value < 0 || value > 2) return MLG_ERR_INVALID_ARG;
       mlg::gather_set_speculation(value);
       return MLG_OK;
-    case MLG_TUNE_GROUPED_CTAS:
+    case MLG_TEST_GROUPED_CTAS:
       if (value < 0 || value > 65535) return MLG_ERR_INVALID_ARG;
       mlg::grouped_set_ctas(value);
       return MLG_OK;

@@ -20,6 +20,7 @@ mlg_status cuda_status(cudaError_t err);
 enum DeviceError : uint32_t {
   kErrWaitTimeout = 1u,   // an mbarrier wait ran past its time limit
   kErrTmemAlloc = 2u,     // tensor-memory allocation did not succeed
+  kErrUnitDropped = 4u,   // a CTA was dealt more work units than it holds
 };
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -49,6 +50,6 @@ cudaError_t decode_fold_launch(const uint16_t *x, const int32_t *indices,
                                uint16_t *base_out, int32_t n_slots, int32_t k_in,
                                int32_t max_rank, int32_t n_out, int32_t top_k,
                                int32_t n_cells, int32_t e_model, int32_t n_adapters,
-                               cudaStream_t stream);
+                               bool early, cudaStream_t stream);
 
 }  // namespace mlg

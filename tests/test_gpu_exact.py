@@ -80,10 +80,10 @@ def test_gather_exact(shape, path):
     if path == 1 and r not in (16, 32):
         pytest.skip("the resident-pair kernel takes rank 16 or 32")
     try:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, path)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, path)
         _check_exact(w, lambda prob: prob.run())
     finally:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, 0)
 
 
 @pytest.mark.parametrize("path", [0, 1, 2])
@@ -91,10 +91,10 @@ def test_gather_multi_exact(path):
     w = integerize(synth.custom_gather_multi(45, 40, 4, 32, 256, 264, 16, 4, adapted_frac=0.8,
                                              base_frac=0.2, bad_ids=2), 15)
     try:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, path)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, path)
         _check_exact(w, lambda prob: prob.run())
     finally:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, 0)
 
 
 def test_gather_multi_halves_exact():

@@ -97,8 +97,8 @@ def test_split_configurations(cs, ns2):
     w = synth.custom_gather(77, 24, 8, 32, 1024, 512, 32, adapted_frac=0.8, base_frac=0.2)
     ref, folded, _ = fh.oracle_reference(w)
     try:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_CLUSTER, cs)
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_NSPLIT, ns2)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_CLUSTER, cs)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_NSPLIT, ns2)
         prob = FoldProblem(w)
         outs = []
         for _ in range(2):
@@ -109,8 +109,8 @@ def test_split_configurations(cs, ns2):
         fh.check_fold(outs[0], w.base, ref, folded)
         assert np.array_equal(outs[0], outs[1])
     finally:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_CLUSTER, 0)
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_NSPLIT, 0)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_CLUSTER, 0)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_NSPLIT, 0)
 
 
 def test_repeat_is_deterministic_and_negative_zero_kept():
@@ -188,10 +188,10 @@ def test_resident_and_cluster_kernels(shape, path):
     w = synth.custom_gather(300 + T, T, K, E, k_in, n_out, r, adapted_frac=adapted,
                             base_frac=base, pad=pad, bad_ids=bad)
     try:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, path)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, path)
         _run_and_check(w)
     finally:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, 0)
 
 
 @pytest.mark.parametrize("multi", [False, True], ids=["single", "multi"])
@@ -211,13 +211,13 @@ def test_speculation_modes_give_the_same_bits(mode, multi):
     outs = []
     try:
         for m in (0, mode):
-            mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_SPECULATION, m)
+            mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_SPECULATION, m)
             prob = FoldProblem(w)
             prob.run()
             torch.cuda.synchronize()
             outs.append(prob.base_bits())
     finally:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_SPECULATION, 0)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_SPECULATION, 0)
     assert np.array_equal(outs[0], outs[1])
     ref, folded, _ = fh.oracle_reference(w)
     fh.check_fold(outs[1], w.base, ref, folded)
@@ -257,12 +257,12 @@ def test_resident_kernel_rejects_other_shapes():
     w = synth.custom_gather(23, 8, 2, 4, 128, 128, 64)
     prob = FoldProblem(w)
     try:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 1)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, 1)
         with pytest.raises(mlg.MlgError) as ei:
             prob.run()
         assert ei.value.status == mlg.MLG_ERR_UNSUPPORTED
     finally:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, 0)
     assert np.array_equal(prob.base_bits(), w.base)
 
 
@@ -286,10 +286,10 @@ def test_gather_multi(shape, path):
     if path == 1 and r not in (16, 32):
         pytest.skip("the resident-pair kernel takes rank 16 or 32")
     try:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, path)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, path)
         _, stats, folded = _run_and_check(w)
     finally:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, 0)
     assert 0 < folded.sum()
 
 
@@ -327,12 +327,12 @@ def test_multi_large_tables_fall_back_to_the_cluster_kernel():
     _run_and_check(w)
     prob = FoldProblem(w)
     try:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 1)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, 1)
         with pytest.raises(mlg.MlgError) as ei:
             prob.run()
         assert ei.value.status == mlg.MLG_ERR_UNSUPPORTED
     finally:
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_PATH, 0)
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_PATH, 0)
     assert np.array_equal(prob.base_bits(), w.base)
 
 

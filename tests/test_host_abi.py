@@ -366,11 +366,11 @@ def test_status_strings_and_tuning(L):
     assert mlg.status_string(-99) == "unknown status"
     assert mlg.mlg_version() >= 10000
     with pytest.raises(mlg.MlgError):
-        mlg.mlg_set_tuning(99, 0)
+        mlg.mlg_test_set_knob(99, 0)
     with pytest.raises(mlg.MlgError):
-        mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_CLUSTER, 3)
-    mlg.mlg_set_tuning(mlg.MLG_TUNE_GATHER_CLUSTER, 0)
-    for knob in (mlg.MLG_TUNE_GATHER_PATH, mlg.MLG_TUNE_GATHER_SPECULATION):
+        mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_CLUSTER, 3)
+    mlg.mlg_test_set_knob(mlg.MLG_TEST_GATHER_CLUSTER, 0)
+    for knob in (mlg.MLG_TEST_GATHER_PATH, mlg.MLG_TEST_GATHER_SPECULATION):
         with pytest.raises(mlg.MlgError):
-            mlg.mlg_set_tuning(knob, 3)
-        mlg.mlg_set_tuning(knob, 0)
+            mlg.mlg_test_set_knob(knob, 3)
+        mlg.mlg_test_set_knob(knob, 0)

@@ -5,23 +5,33 @@
 
 A step is one pass of the hot path over one batch of synthetic input: one
 fold launch for the decode workloads, one launch that folds every row window
-for the prefill workloads, one router-fold launch for the router.  The default
-workload is the decode gather BGMV at the down-projection shape (64 tokens,
-top-8, 128 experts at rank 16, k_in 768, n_out 2048).
+for the prefill workloads, one router-fold launch for the router.  The
+headline workload is the largest configuration, the 163840-row prefill
+(16384 tokens, top-10, 512 experts at rank 32, k_in 512, n_out 2048); every
+other workload is measured in the same run under "workloads", each with the
+same set of figures.
 
-value      rows folded-or-skipped per second over the timed steps (all ranks),
-           device-timed with CUDA events around a CUDA-graph replay of the K
-           steps; the steps rotate over input sets whose total size exceeds L2
-           (each step's inputs are cold in L2), inputs resident in HBM.
+value      rows folded-or-skipped per second: the K steps are captured in one
+           CUDA graph, the graph is replayed R times, each replay timed with
+           CUDA events on its stream; the median replay sets the value, the
+           fastest and slowest are reported beside it.  The steps rotate over
+           input sets whose total exceeds L2 (each step's inputs are cold in
+           L2), inputs resident in HBM.
 e2e        the same metric through the C ABI with host buffers: per step the
            host route + row map and table packing, pinned host->device copies
            of x, routing, row map, tables and base_out, the fold, and the
            device->host copy of base_out, wall-clock timed with a device sync.
-roofline   algorithmic bytes of one launch / its mean duration vs the measured
-           HBM copy bandwidth of this GPU model (MEASURED_PEAKS.json).
+roofline   algorithmic bytes of one launch / its median duration vs the
+           measured HBM copy bandwidth of this GPU model (MEASURED_PEAKS.json).
+decode     besides the chained steps (one fold after another, where a fold's
+           early start overlaps its predecessor), each decode workload also
+           reports an isolated fold (the GPU idle before it, nothing to
+           overlap) and a contended one (each fold right after an HBM-bound
+           copy kernel moving the expert GEMM's bytes; the fold's incremental
+           time over the copies alone).
 cpu_baseline / --impl reference
-           the fp64 CPU oracle as it stands, single-threaded, on a bounded
-           sample of the same workload.
+           the fp64 CPU oracle as it stands, on a bounded sample of the same
+           workload, single-threaded and on all host cores (OpenMP over rows).
 Multi-GPU (torchrun): replicas -- every rank folds its own copy of the
 workload, no collective on the data path; barrier + max-over-ranks timing.
 """
@@ -45,8 +55,11 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE LoRA fold rows/s and achieved HBM GB/s (% of GB300 roofline), 1 GPU"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
-SOAK_S = 0.8  # seconds of untimed replays under the clock sampler before the timed region
+SOAK_S = 0.6  # seconds of untimed replays under the clock sampler before the timed region
 REF_TOTAL_S = 120.0  # wall-clock bound of the reference arm's timed steps
+REPLAYS = 10  # timed replays of the K-step graph (median reported, min / max beside it)
+DEFAULT_WORKLOAD = "prefill_large"
+DECODE = ("decode_down", "decode_gate_up", "decode_down_multi")
 
 # workload name -> (generator, description)
 WORKLOADS = {
@@ -206,13 +219,15 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle timing
-def time_oracle(w, budget_s=10.0):
+def time_oracle(w, budget_s=10.0, threads=1):
     """The fp64 oracle as it stands on host cores, on a bounded sample of the
     workload: whole-workload passes for small workloads, else a row sample
-    (sampled rows / elapsed).  Returns (rows_per_s, sample description)."""
+    (sampled rows / elapsed).  threads: OpenMP threads of the oracle's row
+    loops (0 = every core).  Returns (rows_per_s, sample description, threads)."""
     import oracle
 
     o = oracle.get()
+    used = o.set_threads(threads)
     he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
     at, bt, st = he.tables(o, length=(w.n_adapters * w.n_experts_model) if w.n_adapters else None)
     flops_row = 2 * w.max_rank * (w.k_in + w.n_out)
@@ -221,7 +236,7 @@ def time_oracle(w, budget_s=10.0):
     t0 = time.perf_counter()
     done = 0
     passes = 0
-    if full_cost <= 2e9:
+    if full_cost <= 2e9 * used:
         while time.perf_counter() - t0 < budget_s or passes == 0:
             if w.kind == "gather" and w.n_adapters:
                 _, ra = o.build_moe_row_adapter_decode_multi(w.adapter_slots, w.padded_n,
@@ -247,10 +262,12 @@ def time_oracle(w, budget_s=10.0):
             done += w.rows
             passes += 1
         dt = time.perf_counter() - t0
-        return done / dt, f"{passes} whole-workload pass(es) of {w.rows} rows in {dt:.1f} s"
-    chunk = 64
-    while time.perf_counter() - t0 < budget_s:
-        rows = np.sort(rng.choice(w.rows, size=chunk, replace=False)).astype(np.int32)
+        o.set_threads(0)
+        return (done / dt, f"{passes} whole-workload pass(es) of {w.rows} rows in {dt:.1f} s "
+                           f"on {used} thread(s)", used)
+    chunk = 64 * used
+    while time.perf_counter() - t0 < budget_s or done == 0:
+        rows = np.sort(rng.choice(w.rows, size=min(chunk, w.rows), replace=False)).astype(np.int32)
         if w.kind == "grouped" and w.x_rows is not None:
             ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
             o.grouped_fold_xrows_rows(w.x_rows, w.expert_offsets, w.src, ra, at, bt, st,
@@ -268,14 +285,27 @@ def time_oracle(w, budget_s=10.0):
         else:
             o.gather_fold_rows(w.x, np.zeros(w.rows, np.int32), None, at, bt, st, w.base[rows],
                                rows, w.k_in, w.max_rank, w.n_out, 1)
-        done += chunk
+        done += rows.size
     dt = time.perf_counter() - t0
-    return done / dt, f"{done} sampled rows of {w.rows} in {dt:.1f} s (row-by-row oracle)"
+    o.set_threads(0)
+    return (done / dt, f"{done} sampled rows of {w.rows} in {dt:.1f} s (row-by-row oracle) on "
+                       f"{used} thread(s)", used)
+
+
+def cpu_baseline(w, budget_s):
+    """The oracle on one host core and on all of them (same bits either way)."""
+    one, d1, _ = time_oracle(w, budget_s, threads=1)
+    alln, dn, used = time_oracle(w, budget_s, threads=0)
+    return {"value": alln, "unit": "rows/s", "cores": used, "kind": "oracle", "sample": dn,
+            "single_thread_value": one, "single_thread_sample": d1,
+            "host_cpu_count": os.cpu_count()}
 
 
 # ------------------------------------------------------------------ GPU arm
 def n_sets_for(w_bytes):
-    return max(1, min(32, int(np.ceil(2.0 * L2_BYTES / max(w_bytes, 1)))))
+    """Input sets the timed steps rotate over: at least two, and enough that
+    their total is twice the L2."""
+    return max(2, min(32, int(np.ceil(2.0 * L2_BYTES / max(w_bytes, 1)))))
 
 
 # The kernel that folds each named workload (the decode fold takes expert
@@ -284,17 +314,19 @@ def n_sets_for(w_bytes):
 KERNEL_OF = {"decode_down": "mlg_decode.cu", "decode_gate_up": "mlg_gather.cu",
              "tiny_decode": "mlg_gather.cu", "prefill_down": "mlg_grouped.cu",
              "prefill_large": "mlg_grouped.cu", "router": "mlg_grouped.cu",
-             "prefill_down_xrows": "mlg_grouped.cu", "decode_down_multi": "mlg_gather.cu"}
+             "prefill_down_xrows": "mlg_grouped.cu", "decode_down_multi": "mlg_decode.cu"}
 
 
 def kernel_source(workload):
     return "lora_moe_expert_gb300/csrc/" + KERNEL_OF[workload]
 
 
-def gpu_measure(name, steps, warmup, device, seed_base=1000, e2e=True):
-    import torch
-
-    import lora_moe_expert_gb300 as mlg
+def make_sets(name, device, seed_base):
+    """Device-resident input sets of a workload.  Sets past the first draw
+    fresh inputs when the workload is small; a workload larger than half the
+    L2 reuses the first set's host arrays in new device allocations (the
+    timing only needs distinct memory, and drawing them would take longer
+    than the measurement)."""
     from lora_moe_expert_gb300 import synth
     from lora_moe_expert_gb300.device import FoldProblem
 
@@ -304,57 +336,159 @@ def gpu_measure(name, steps, warmup, device, seed_base=1000, e2e=True):
     ws_bytes = (w0.x.nbytes + w0.base.nbytes + sum(e.A.nbytes + e.B.nbytes for e in w0.experts)
                 + (w0.x_rows.nbytes if w0.x_rows is not None else 0))
     nsets = n_sets_for(ws_bytes)
-    probs = [p0] + [FoldProblem(gen(seed=seed_base + i), device=device) for i in range(1, nsets)]
+    big = ws_bytes > L2_BYTES // 2
+    probs = [p0] + [FoldProblem(w0 if big else gen(seed=seed_base + i), device=device)
+                    for i in range(1, nsets)]
+    return probs, ws_bytes
+
+
+def _events(n):
+    import torch
+
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n)]
+
+
+def time_graph(graph, stream, replays, barrier=False, sampler=None):
+    """Milliseconds of each of `replays` timed replays of `graph` (CUDA events
+    on `stream`), after a soak of untimed replays (under the clock sampler
+    when one is given)."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+        stream.synchronize()
+        if sampler is not None:
+            t_soak = time.perf_counter()
+            while time.perf_counter() - t_soak < SOAK_S:
+                graph.replay()
+                stream.synchronize()
+    if barrier and torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev = _events(replays)
+    with torch.cuda.stream(stream):
+        for e0, e1 in ev:
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+
+def capture(fn, stream):
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    return g
+
+
+def time_isolated(probs, n, stream):
+    """Each fold alone: the GPU spins in a sleep kernel while the host enqueues
+    an event, the fold and an event, so the fold starts on an idle stream with
+    nothing to overlap.  Milliseconds per fold, n samples over the sets."""
+    import torch
+
+    ev = _events(n)
+    with torch.cuda.stream(stream):
+        for i, (e0, e1) in enumerate(ev):
+            torch.cuda._sleep(1000000)  # ~0.5 ms: the host enqueues the fold meanwhile
+            e0.record(stream)
+            probs[i % len(probs)].run(stream=stream)
+            e1.record(stream)
+    stream.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+
+def expert_gemm_bytes(w):
+    """Bytes of the expert GEMM a decode fold follows in a model: the weight
+    W_e [n_out, k_in] of every expert the routing hits (whether or not it is
+    adapted), x and the output rows."""
+    idx = w.indices.astype(np.int64)
+    hit = np.unique(idx[(idx >= 0) & (idx < w.n_experts_model)]).size
+    return hit * w.n_out * w.k_in * 2 + w.x.nbytes + w.base.nbytes
+
+
+def time_contended(probs, steps, stream, copy_bytes, replays):
+    """Each fold right after an HBM-bound copy kernel (an elementwise bf16
+    multiply by one, reading and writing copy_bytes / 2 each): the fold's
+    incremental milliseconds over the copies alone, per step."""
+    import torch
+
+    n = max(1, copy_bytes // 4)
+    src = torch.ones(n, dtype=torch.bfloat16, device=stream.device)
+    dst = torch.empty_like(src)
+
+    def copies_and_folds():
+        for i in range(steps):
+            torch.mul(src, 1.0, out=dst)
+            probs[i % len(probs)].run(stream=stream)
+
+    def copies():
+        for _ in range(steps):
+            torch.mul(src, 1.0, out=dst)
+
+    g_both, g_copy = capture(copies_and_folds, stream), capture(copies, stream)
+    t_both = statistics.median(time_graph(g_both, stream, replays))
+    t_copy = statistics.median(time_graph(g_copy, stream, replays))
+    del g_both, g_copy
+    return (t_both - t_copy) / steps, t_copy / steps
+
+
+def gpu_measure(name, steps, warmup, device, seed_base=1000, replays=REPLAYS, e2e=True,
+                decode_extra=True, barrier=False):
+    import torch
+
+    import lora_moe_expert_gb300 as mlg
+
+    probs, ws_bytes = make_sets(name, device, seed_base)
+    nsets = len(probs)
     # The input sets may differ in size (prefill lengths are drawn per seed):
     # the per-step figures are the mean over the steps the timed graph runs.
     alg = np.array([algorithmic(probs[i % nsets].w, probs[i % nsets].row_map_host,
                                 probs[i % nsets].tables_host) for i in range(steps)], np.float64)
     rows, folded, nbytes, flops = alg.mean(axis=0)
     launches_per_step = 1  # the grouped form folds all windows in one launch
+    w0 = probs[0].w
 
     stream = torch.cuda.Stream(device=device)
     with torch.cuda.stream(stream):
         for i in range(max(warmup, 3)):  # eager warm-up steps
             probs[i % nsets].run(stream=stream)
-        stream.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(steps):
-                probs[i % nsets].run(stream=stream)
-        for _ in range(max(warmup, 3)):  # warm-up replays of the timed graph
-            graph.replay()
-        stream.synchronize()
+    stream.synchronize()
     errors_before = mlg.mlg_read_device_errors(clear=True)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    # The clock sampler (100 ms period) runs from a soak of identical replays
-    # straight into the timed region, so its samples are taken under this load;
-    # a timed region of K short steps alone is shorter than one sample period.
+
+    def chain():
+        for i in range(steps):
+            probs[i % nsets].run(stream=stream)
+
+    graph = capture(chain, stream)
     with ClockSampler(torch.cuda.current_device(), settle_s=0.0) as clocks:
-        t_soak = time.perf_counter()
-        with torch.cuda.stream(stream):
-            while time.perf_counter() - t_soak < SOAK_S:
-                graph.replay()
-                stream.synchronize()
-        if torch.distributed.is_available() and torch.distributed.is_initialized():
-            torch.distributed.barrier()
-        torch.cuda.synchronize(device)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            graph.replay()
-            e1.record(stream)
-        stream.synchronize()
-    torch.cuda.synchronize(device)
-    ms_total = e0.elapsed_time(e1)
+        ms = time_graph(graph, stream, replays, barrier=barrier, sampler=clocks)
+    del graph
+    out = {"rows": rows, "folded_rows": folded, "alg_bytes": nbytes, "alg_flops": flops,
+           "rows_set0": w0.rows, "ms_replays": ms, "ms_total": statistics.median(ms),
+           "launches_per_step": launches_per_step, "replays": replays, "sets": nsets,
+           "set_bytes": ws_bytes, "clocks": clocks.summary(), "kind": w0.kind}
+    if decode_extra and name in DECODE:
+        iso = time_isolated(probs, 40, stream)
+        out["isolated_ms"] = statistics.median(iso)
+        out["isolated_ms_min"] = min(iso)
+        cb = expert_gemm_bytes(w0)
+        inc, copy_ms = time_contended(probs, min(steps, 20), stream, cb, max(3, replays // 2))
+        out["contended_ms"] = inc
+        out["contended_copy_bytes"] = cb
+        out["contended_copy_ms"] = copy_ms
     if mlg.mlg_read_device_errors(clear=True) or errors_before:
         raise RuntimeError("device error bits were set during the benchmark")
-    out = {"rows": rows, "folded_rows": folded, "alg_bytes": nbytes, "alg_flops": flops,
-           "rows_set0": w0.rows,
-           "ms_total": ms_total, "launches_per_step": launches_per_step, "sets": nsets,
-           "set_bytes": ws_bytes, "clocks": clocks.summary(), "kind": w0.kind}
     if e2e:
-        out["e2e"] = e2e_measure(probs[0], max(3, min(steps, 50)), device)
-    del graph
+        out["e2e"] = e2e_measure(probs[0], max(3, min(steps, 20 if w0.rows > 50000 else 50)),
+                                 device)
     return out
 
 
@@ -469,14 +603,15 @@ def run_reference(args):
     w = synth.NAMED[args.workload]()
     steps_rows = []
     for _ in range(args.warmup):
-        time_oracle(w, budget_s=0.0)
+        time_oracle(w, budget_s=0.0, threads=0)
     # Each step is a bounded sample: the whole timed run stays within about
     # REF_TOTAL_S whatever --steps is (at most --ref-budget seconds a step).
     budget = min(args.ref_budget, REF_TOTAL_S / max(args.steps, 1))
     t0 = time.perf_counter()
     samples = []
+    used = 1
     for _ in range(args.steps):
-        rps, desc = time_oracle(w, budget_s=budget)
+        rps, desc, used = time_oracle(w, budget_s=budget, threads=0)
         steps_rows.append(rps)
         samples.append(desc)
     total = time.perf_counter() - t0
@@ -486,9 +621,9 @@ def run_reference(args):
             "ms_per_step": 1e3 * total / max(args.steps, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "description": WORKLOADS[args.workload],
-                       "parallelism": "none (host oracle)"},
-            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                             "sample": samples[0]},
+                       "parallelism": "none (host oracle, OpenMP over rows)"},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": used, "kind": "oracle",
+                             "sample": samples[0], "host_cpu_count": os.cpu_count()},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -514,17 +649,55 @@ def profile_case(name, launches, device):
     return 0
 
 
+def summarize(name, r, peak, steps, cpu=None):
+    """Per-workload figures from one gpu_measure result."""
+    ms = r["ms_total"] / steps
+    per_launch = ms / r["launches_per_step"]
+    gbs = r["alg_bytes"] / r["launches_per_step"] / (per_launch * 1e-3) / 1e9
+    out = {"rows_per_s": r["rows"] / (ms * 1e-3), "us_per_step": ms * 1e3,
+           "us_per_step_min": min(r["ms_replays"]) / steps * 1e3,
+           "us_per_step_max": max(r["ms_replays"]) / steps * 1e3,
+           "replays": r["replays"], "launches_per_step": r["launches_per_step"],
+           "rows_per_step": r["rows"], "folded_rows_per_step": r["folded_rows"],
+           "alg_bytes_per_step": r["alg_bytes"], "achieved_gbs": gbs, "frac_of_peak": gbs / peak,
+           "tflops": r["alg_flops"] / (ms * 1e-3) / 1e12,
+           "traffic": recorded_traffic(kernel_source(name), name),
+           "l2": f"{r['sets']} rotating input sets of {r['set_bytes'] / 2**20:.0f} MiB",
+           "clocks": r["clocks"]}
+    if "isolated_ms" in r:
+        iso, con = r["isolated_ms"], r["contended_ms"]
+        out["isolated_us"] = iso * 1e3
+        out["isolated_us_min"] = r["isolated_ms_min"] * 1e3
+        out["isolated_frac_of_peak"] = r["alg_bytes"] / (iso * 1e-3) / 1e9 / peak
+        out["contended_us"] = con * 1e3
+        out["contended_frac_of_peak"] = (r["alg_bytes"] / (con * 1e-3) / 1e9 / peak
+                                         if con > 0 else None)
+        out["contended_copy_bytes"] = r["contended_copy_bytes"]
+        out["contended_copy_us"] = r["contended_copy_ms"] * 1e3
+    if "e2e" in r:
+        e = r["e2e"]
+        out["e2e"] = {"value": r["rows_set0"] / e["s_per_step"], "unit": "rows/s",
+                      "h2d_bytes_per_step": e["h2d_bytes_per_step"],
+                      "d2h_bytes_per_step": e["d2h_bytes_per_step"]}
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode_down", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--extra", default="decode_gate_up,decode_down_multi,prefill_down,prefill_down_xrows,"
-                                       "prefill_large,router",
+    ap.add_argument("--extra", default="decode_down,decode_gate_up,decode_down_multi,prefill_down,"
+                                       "prefill_down_xrows,router",
                     help="other workloads measured in the same run (comma list, or 'none')")
+    ap.add_argument("--replays", type=int, default=REPLAYS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=3.0,
+                    help="seconds of oracle work per (workload, thread count) sample")
     ap.add_argument("--ref-budget", type=float, default=10.0)
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="profiler case: run the workload's step this many times on cuda:0, "
@@ -551,7 +724,8 @@ def main():
         return profile_case(args.workload, args.profile_launches, device)
 
     main_res = gpu_measure(args.workload, args.steps, args.warmup, device,
-                           seed_base=replica_seed_base(rank))
+                           seed_base=replica_seed_base(rank), replays=args.replays,
+                           barrier=True)
     ms_step = max_over_ranks(main_res["ms_total"] / args.steps, device)
     main_res["e2e"]["s_per_step"] = max_over_ranks(main_res["e2e"]["s_per_step"], device)
     peak, peak_kind = measured_peaks()
@@ -559,20 +733,14 @@ def main():
     achieved = main_res["alg_bytes"] / main_res["launches_per_step"] / (per_launch_ms * 1e-3) / 1e9
     extras = {}
     if args.extra != "none" and rank == 0:
+        from lora_moe_expert_gb300 import synth
+
         for nm in [s for s in args.extra.split(",") if s and s != args.workload]:
             try:
-                r = gpu_measure(nm, 20, 3, device, e2e=False)
-                pl = r["ms_total"] / 20 / r["launches_per_step"]
-                a = r["alg_bytes"] / r["launches_per_step"] / (pl * 1e-3) / 1e9
-                extras[nm] = {"rows_per_s": r["rows"] / (r["ms_total"] / 20 * 1e-3),
-                              "us_per_step": r["ms_total"] / 20 * 1e3,
-                              "launches_per_step": r["launches_per_step"],
-                              "alg_bytes_per_step": r["alg_bytes"],
-                              "achieved_gbs": a, "frac_of_peak": a / peak,
-                              "tflops": r["alg_flops"] / (r["ms_total"] / 20 * 1e-3) / 1e12,
-                              "traffic": recorded_traffic(kernel_source(nm), nm),
-                              "l2": f"{r['sets']} rotating input sets of "
-                                    f"{r['set_bytes'] / 2**20:.0f} MiB"}
+                r = gpu_measure(nm, args.steps, 3, device, replays=args.replays)
+                cpu = None if args.no_cpu_baseline else cpu_baseline(synth.NAMED[nm](),
+                                                                      args.cpu_budget)
+                extras[nm] = summarize(nm, r, peak, args.steps, cpu)
             except Exception as ex:  # report, do not hide
                 extras[nm] = {"error": repr(ex)[:300]}
     if rank != 0:
@@ -584,9 +752,9 @@ def main():
     if not args.no_cpu_baseline:
         from lora_moe_expert_gb300 import synth
 
-        rps, desc = time_oracle(synth.NAMED[args.workload](), budget_s=10.0)
-        cpu = {"value": rps, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc}
+        cpu = cpu_baseline(synth.NAMED[args.workload](), args.cpu_budget)
     e2e = main_res["e2e"]
+    spread = [m / args.steps for m in main_res["ms_replays"]]
     line = {
         "metric": METRIC,
         "value": job_rows_per_s(main_res["rows"], ws, ms_step),
@@ -595,6 +763,8 @@ def main():
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms_step,
+        "ms_per_step_min": min(spread),
+        "ms_per_step_max": max(spread),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -605,7 +775,9 @@ def main():
                    "rows_note": "mean over the timed steps' input sets",
                    "l2": f"inputs rotate over {main_res['sets']} sets of "
                          f"{main_res['set_bytes'] / 2**20:.1f} MiB (> L2 in total)",
-                   "timing": "CUDA events around one CUDA-graph replay of the timed steps",
+                   "timing": f"CUDA events around each of {args.replays} replays of one "
+                             f"CUDA graph of the {args.steps} steps; median replay "
+                             f"(min / max beside it)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
@@ -617,7 +789,7 @@ def main():
                 "unit": "rows/s",
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},
-        "gpu_launches": args.steps * main_res["launches_per_step"],
+        "gpu_launches": args.replays * args.steps * main_res["launches_per_step"],
         "clocks": main_res["clocks"],
         "workloads": extras,
     }

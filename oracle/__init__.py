@@ -109,6 +109,8 @@ class Oracle:
         L.oracle_gather_fold_rows.restype = _i32
         L.oracle_grouped_fold_rows.argtypes = [_p] * 9 + [_i32, _p, _p] + [_i32] * 7
         L.oracle_grouped_fold_rows.restype = _i32
+        L.oracle_grouped_gemm_fold_xrows.argtypes = [_p] * 12 + [_i64] + [_i32] * 7
+        L.oracle_grouped_gemm_fold_xrows.restype = _i32
 
     def set_threads(self, n: int) -> int:
         """Threads of the row loops (n < 1: every core); returns the count in force
@@ -267,6 +269,31 @@ class Oracle:
                                                 at.size, row_offset, row_end)
         assert st == OK, st
         return ref, folded.astype(bool)
+
+    def grouped_gemm_fold_xrows(self, x_rows, expert_offsets, src, row_adapter, w_table,
+                                a_table, b_table, scale_table, out_in, k_in, max_rank, n_out,
+                                top_k, row_offset, row_end):
+        """Expert GEMM with the per-row x fold in its epilogue.  Returns
+        (ref fp64 [total_rows, n_out], written bool, folded bool); rows not
+        written keep out_in."""
+        x, out_in = self._u16(x_rows), self._u16(out_in)
+        off = np.ascontiguousarray(expert_offsets, np.int32)
+        src = np.ascontiguousarray(src, np.int32)
+        ra = None if row_adapter is None else np.ascontiguousarray(row_adapter, np.int32)
+        wt = np.ascontiguousarray(w_table, np.uint64)
+        at, bt = np.ascontiguousarray(a_table, np.uint64), np.ascontiguousarray(b_table, np.uint64)
+        st_ = np.ascontiguousarray(scale_table, np.float32)
+        assert wt.size == at.size == bt.size == st_.size
+        total = out_in.shape[0]
+        ref = np.empty((total, n_out), np.float64)
+        written = np.empty(total, np.uint8)
+        folded = np.empty(total, np.uint8)
+        st = self.lib.oracle_grouped_gemm_fold_xrows(
+            _ptr(x), _ptr(off), _ptr(src), _ptr(ra), _ptr(wt), _ptr(at), _ptr(bt), _ptr(st_),
+            _ptr(out_in), _ptr(ref), _ptr(written), _ptr(folded), total, k_in, max_rank, n_out,
+            top_k, at.size, row_offset, row_end)
+        assert st == OK, st
+        return ref, written.astype(bool), folded.astype(bool)
 
     def router_fold(self, x, row_adapter, a_table, b_table, scale_table, base, k_in, max_rank,
                     n_out):

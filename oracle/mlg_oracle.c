@@ -518,3 +518,74 @@ int32_t oracle_grouped_fold_xrows_rows(const uint16_t *x_rows, const int32_t *ex
     }
     return OR_OK;
 }
+
+/* The expert GEMM with the LoRA fold in its epilogue (per-row x form).
+ * [P2] moe_lora_grouped_down folds into base_out, which is the expert
+ * projection's output: base_out[r] = x_rows[r] @ W_e^T for a down projection
+ * whose input is the expert's intermediate row.  Computing both in one pass
+ * gives, for sorted row r in [row_offset, row_end) held by span e < n_experts
+ * whose weight cell w_table[e] is non-zero (W_e [n_out, k_in] bf16):
+ *     out[r, n] = sum_k x_rows[r, k] W_e[n, k]
+ *                 + [row folds] scale_e * sum_j h_j B_e[n, j],
+ *     h_j = sum_k x_rows[r, k] A_e[j, k],
+ * where the row folds under the per-row x fold's rules: expert e's a / b
+ * cells non-zero, src[r] >= 0, and (when given) row_adapter[src[r] / top_k]
+ * >= 0.  A row of a span whose weight cell is 0, or outside the window or
+ * every span, is not an output of this call and keeps its prior value
+ * (out_in).  `written[r]` marks rows given the GEMM result, `folded[r]` the
+ * rows that also took the delta.  Unrounded, like every fold here. */
+int32_t oracle_grouped_gemm_fold_xrows(const uint16_t *x_rows, const int32_t *expert_offsets,
+                                       const int32_t *src, const int32_t *row_adapter,
+                                       const uint64_t *w_table, const uint64_t *a_table,
+                                       const uint64_t *b_table, const float *scale_table,
+                                       const uint16_t *out_in, double *ref_out, uint8_t *written,
+                                       uint8_t *folded, int64_t total_rows, int32_t k_in,
+                                       int32_t max_rank, int32_t n_out, int32_t top_k,
+                                       int32_t n_experts, int32_t row_offset, int32_t row_end) {
+    if (max_rank > 1024 || top_k < 1) return OR_NONE;
+    for (int64_t r = 0; r < total_rows; ++r) {
+        copy_row(out_in + r * n_out, ref_out + r * n_out, n_out);
+        written[r] = 0;
+        folded[r] = 0;
+    }
+    for (int32_t e = 0; e < n_experts; ++e) {
+        int64_t lo = expert_offsets[e] > row_offset ? expert_offsets[e] : row_offset;
+        int64_t hi = expert_offsets[e + 1] < row_end ? expert_offsets[e + 1] : row_end;
+        if (w_table[e] == 0) continue;
+        const uint16_t *W = (const uint16_t *)(uintptr_t)w_table[e];
+        int lora = expert_folds(e, n_experts, a_table, b_table);
+#pragma omp parallel for schedule(dynamic, 8)
+        for (int64_t r = lo; r < hi; ++r) {
+            const uint16_t *xr = x_rows + r * k_in;
+            double *ref_row = ref_out + r * n_out;
+            for (int32_t n = 0; n < n_out; ++n) {
+                double g = 0.0;
+                for (int32_t k = 0; k < k_in; ++k)
+                    g += bf16_value(xr[k]) * bf16_value(W[(int64_t)n * k_in + k]);
+                ref_row[n] = g;
+            }
+            written[r] = 1;
+            int row_folds = lora && src[r] >= 0 &&
+                            (row_adapter == NULL || row_adapter[src[r] / top_k] >= 0);
+            if (!row_folds) continue;
+            const uint16_t *A = (const uint16_t *)(uintptr_t)a_table[e];
+            const uint16_t *B = (const uint16_t *)(uintptr_t)b_table[e];
+            double h[1024];
+            for (int32_t j = 0; j < max_rank; ++j) {
+                double acc = 0.0;
+                for (int32_t k = 0; k < k_in; ++k)
+                    acc += bf16_value(xr[k]) * bf16_value(A[(int64_t)j * k_in + k]);
+                h[j] = acc;
+            }
+            double scale = (double)scale_table[e];
+            for (int32_t n = 0; n < n_out; ++n) {
+                double d = 0.0;
+                for (int32_t j = 0; j < max_rank; ++j)
+                    d += h[j] * bf16_value(B[(int64_t)n * max_rank + j]);
+                ref_row[n] += scale * d;
+            }
+            folded[r] = 1;
+        }
+    }
+    return OR_OK;
+}

@@ -414,6 +414,101 @@ def pin_multi_adapter(o):
     assert st_ == 0 and np.array_equal(m, o.build_moe_row_adapter_decode(slots, 7, 0, True))
 
 
+class _Weights:
+    """Host copies of expert GEMM weights W_e [n_out, k_in] (bf16 bits) and the
+    table of their host addresses (0 = no weight for that expert)."""
+
+    def __init__(self, mats, n_table):
+        self.keep = []
+        self.table = np.zeros(n_table, np.uint64)
+        for e, m in mats.items():
+            m = np.ascontiguousarray(m, np.uint16)
+            self.keep.append(m)
+            self.table[e] = m.ctypes.data
+
+
+def pin_gemm_fold(o):
+    """The expert GEMM with the fold in its epilogue.  With the LoRA cells
+    zeroed it is numpy's float64 matmul of x_rows and W_e^T on the rows of
+    spans with a weight; with small integers (every GEMM value an exact bf16)
+    it equals the per-row x fold run on base = that GEMM result; with W_e a
+    permutation (out column n picks x column perm_e[n]) it equals the per-row
+    x fold on base = x_rows[:, perm_e]; rows of a span without a weight, and
+    rows outside the window, keep their prior bits."""
+    w = synth.custom_grouped(15, [13, 21, 7], top_k=3, n_experts=9, k_in=48, n_out=48,
+                             max_rank=8, cap=17, adapted_frac=0.7, stream_base=[0, 1, 0],
+                             per_row_x=True)
+    he = HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
+    at, bt, st = he.tables(o, length=w.n_experts_model)
+    E, R, K, N = w.n_experts_model, w.rows, w.k_in, w.n_out
+    ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+    rng = np.random.default_rng(8)
+    counts = np.diff(w.expert_offsets)
+    no_w = int(np.argmax(counts))  # the fullest span gets no weight
+    span = np.full(R, -1)
+    for e in range(E):
+        span[w.expert_offsets[e]:w.expert_offsets[e + 1]] = e
+    z = np.zeros(E, np.uint64)
+    # (a) LoRA off: a plain grouped matmul, rows without a weight untouched
+    mats = {e: _bits(rng.standard_normal((N, K)) / np.sqrt(K)) for e in range(E) if e != no_w}
+    W = _Weights(mats, E)
+    lo, hi = 2, R - 3
+    ref, written, folded = o.grouped_gemm_fold_xrows(w.x_rows, w.expert_offsets, w.src, ra,
+                                                     W.table, z, z, st, w.base, K, w.max_rank,
+                                                     N, w.top_k, lo, hi)
+    assert not folded.any()
+    for r in range(R):
+        e = span[r]
+        if lo <= r < hi and e >= 0 and e != no_w:
+            assert written[r]
+            exp = _f(w.x_rows[r:r + 1]) @ _f(mats[e]).T
+            assert np.allclose(ref[r], exp[0], rtol=1e-12, atol=1e-12), r
+        else:
+            assert not written[r] and np.array_equal(ref[r], _f(w.base[r])), r
+    # (b) small integers: GEMM exact in bf16, then the fold on that base
+    xi = _bits(rng.integers(-2, 3, (R, K)).astype(np.float32))
+    mats_i = {e: _bits(rng.integers(-1, 2, (N, K)).astype(np.float32)) for e in range(E)
+              if e != no_w}
+    Wi = _Weights(mats_i, E)
+    gemm = np.zeros((R, N), np.float64)
+    for r in range(R):
+        if span[r] >= 0 and span[r] != no_w:
+            gemm[r] = _f(xi[r:r + 1]) @ _f(mats_i[span[r]]).T
+    assert np.abs(gemm).max() < 256
+    base_g = np.where((span >= 0) & (span != no_w), 1, 0)[:, None] * gemm
+    base_bits = np.where(((span >= 0) & (span != no_w))[:, None], _bits(base_g), w.base)
+    ref, written, folded = o.grouped_gemm_fold_xrows(xi, w.expert_offsets, w.src, ra, Wi.table,
+                                                     at, bt, st, w.base, K, w.max_rank, N,
+                                                     w.top_k, 0, R)
+    ref_f, fold_f = o.grouped_fold_xrows(xi, w.expert_offsets, w.src, ra, at, bt, st, base_bits,
+                                         K, w.max_rank, N, w.top_k, 0, R)
+    assert folded.any() and (written & ~folded).any()
+    assert np.array_equal(folded, fold_f & written)
+    assert np.array_equal(ref[written], ref_f[written])
+    assert np.array_equal(ref[~written], _f(w.base[~written]))
+    # (c) permutation weights: out column n is x column perm_e[n] plus the delta
+    perms = {e: rng.permutation(K) for e in range(E) if e != no_w}
+    for p in perms.values():
+        assert np.any(p[p] != np.arange(K))  # not an involution, so a transpose shows
+    mats_p = {}
+    for e, p in perms.items():
+        m = np.zeros((N, K), np.float32)
+        m[np.arange(N), p] = 1.0
+        mats_p[e] = _bits(m)
+    Wp = _Weights(mats_p, E)
+    base_p = w.base.copy()
+    for r in range(R):
+        if span[r] >= 0 and span[r] != no_w:
+            base_p[r] = w.x_rows[r, perms[span[r]]]
+    ref, written, folded = o.grouped_gemm_fold_xrows(w.x_rows, w.expert_offsets, w.src, ra,
+                                                     Wp.table, at, bt, st, w.base, K,
+                                                     w.max_rank, N, w.top_k, 0, R)
+    ref_f, fold_f = o.grouped_fold_xrows(w.x_rows, w.expert_offsets, w.src, ra, at, bt, st,
+                                         base_p, K, w.max_rank, N, w.top_k, 0, R)
+    assert np.array_equal(ref[written], ref_f[written])
+    assert np.array_equal(folded, fold_f & written)
+
+
 ALL_PINS = [
     pin_route_truth_table,
     pin_decode_maps,
@@ -433,4 +528,5 @@ ALL_PINS = [
     pin_sampled_rows_match_full,
     pin_xrows_forms,
     pin_multi_adapter,
+    pin_gemm_fold,
 ]

@@ -53,6 +53,17 @@ MUTANTS = {
     "multi refusal dropped": ("if (adapter_slots[i] >= n_adapters) return OR_REFUSE;", ";"),
     "multi base requests kept": ("if (has_moe_lora && i < n_slots && adapter_slots[i] >= 0)",
                                  "if (has_moe_lora && i < n_slots)"),
+    "gemm W transposed": ("g += bf16_value(xr[k]) * bf16_value(W[(int64_t)n * k_in + k]);",
+                          "g += bf16_value(xr[k]) * bf16_value(W[(int64_t)k * n_out + n]);"),
+    "gemm last k dropped": ("for (int32_t k = 0; k < k_in; ++k)\n                    g +=",
+                            "for (int32_t k = 0; k + 1 < k_in; ++k)\n                    g +="),
+    "gemm delta unscaled": ("ref_row[n] += scale * d;", "ref_row[n] += d;"),
+    "gemm row map slot 0 skipped": ("row_adapter[src[r] / top_k] >= 0);",
+                                    "row_adapter[src[r] / top_k] > 0);"),
+    "gemm weightless rows zeroed": (
+        "if (w_table[e] == 0) continue;",
+        "if (w_table[e] == 0) { for (int64_t q = lo; q < hi; ++q) "
+        "for (int32_t n = 0; n < n_out; ++n) ref_out[q * n_out + n] = 0.0; continue; }"),
     "padding gets active": ("        } else {\n            out[i] = -1;\n        }",
                             "        } else {\n            out[i] = active;\n        }"),
 }

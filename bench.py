@@ -78,6 +78,8 @@ WORKLOADS = {
                      "rank 32, k_in 512, n_out 2048, skewed routing, windows of 32768 rows",
     "router": "router fold (one-entry route): 16384 tokens, k_in 2048, n_out 512, rank 32",
     "tiny_decode": "tiny decode gather fold: 4 tokens x top-2, 8 experts (2 unadapted), rank 8",
+    "prefill_down_fused": "expert GEMM with the fold in its epilogue, down-proj: prefill_down_xrows "
+                          "plus every expert's weight W_e [2048, 768]; out = x_rows W_e^T + fold",
 }
 
 
@@ -91,7 +93,18 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_HEADERS = ("lora_moe_expert_gb300/csrc/mlg_ptx.cuh", "lora_moe_expert_gb300/csrc/mlg_internal.h")
+def tensor_peak():
+    """Dense bf16 tensor TFLOP/s of this GPU model: the measured burst figure
+    (a kernel timed on its own), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+KERNEL_HEADERS = ("lora_moe_expert_gb300/csrc/mlg_ptx.cuh", "lora_moe_expert_gb300/csrc/mlg_internal.h",
+                  "lora_moe_expert_gb300/csrc/mlg_tiles.cuh")
 
 
 def source_hash(path):
@@ -153,6 +166,21 @@ def algorithmic(w, row_map, tables):
     idx_bytes = rows * 4 + (row_map.size * 4 if row_map is not None else 0) + E * 20
     if w.kind == "grouped":
         idx_bytes += (w.n_experts_model + 1) * 4
+    if w.weights is not None:
+        # expert GEMM with the fold: every row of a span with a weight is read
+        # (x_rows) and written once (out), each such expert's W_e is read once
+        e_span = np.repeat(np.arange(w.n_experts_model), np.diff(w.expert_offsets))
+        e_span = np.concatenate([e_span, np.full(rows - e_span.size, -1)])
+        has_w = np.array([int(v) in w.weights for v in e_span]) if rows else np.zeros(0, bool)
+        written = int(has_w.sum())
+        w_experts = np.unique(e_span[has_w]).size
+        ok &= has_w
+        folded = int(ok.sum())
+        experts = np.unique(e[ok]).size
+        nbytes = (written * k * 2 + w_experts * n * k * 2 + experts * r * (k + n) * 2
+                  + written * n * 2 + idx_bytes + E * 8)
+        flops = 2 * written * k * n + 2 * folded * r * (k + n)
+        return rows, folded, int(nbytes), int(flops)
     n_x = folded if w.x_rows is not None else tokens  # per-row x: one x row per folding row
     nbytes = n_x * k * 2 + experts * r * (k + n) * 2 + folded * n * 4 + idx_bytes
     flops = 2 * folded * r * (k + n)
@@ -314,7 +342,8 @@ def n_sets_for(w_bytes):
 KERNEL_OF = {"decode_down": "mlg_decode.cu", "decode_gate_up": "mlg_gather.cu",
              "tiny_decode": "mlg_gather.cu", "prefill_down": "mlg_grouped.cu",
              "prefill_large": "mlg_grouped.cu", "router": "mlg_grouped.cu",
-             "prefill_down_xrows": "mlg_grouped.cu", "decode_down_multi": "mlg_decode.cu"}
+             "prefill_down_xrows": "mlg_grouped.cu", "decode_down_multi": "mlg_decode.cu",
+             "prefill_down_fused": "mlg_gemm_fold.cu"}
 
 
 def kernel_source(workload):
@@ -484,6 +513,25 @@ def gpu_measure(name, steps, warmup, device, seed_base=1000, replays=REPLAYS, e2
         out["contended_ms"] = inc
         out["contended_copy_bytes"] = cb
         out["contended_copy_ms"] = copy_ms
+    if w0.weights is not None:
+        # the same step unfused: the plain expert GEMM (LoRA cells zero), then
+        # the per-row x fold reading its output back
+        def gemm_only():
+            for i in range(steps):
+                probs[i % nsets].run(stream=stream, lora=False)
+
+        def fold_only():
+            for i in range(steps):
+                q = probs[i % nsets]
+                mlg.mlg_grouped_down_xrows(q.x_rows, q.expert_offsets, q.src, q.row_adapter,
+                                           q.a_table, q.b_table, q.scale_table, q.base,
+                                           q.w.k_in, q.w.max_rank, q.w.n_out, q.w.top_k,
+                                           q.n_experts, 0, q.w.rows, q.w.cap, stream=stream)
+
+        for nm_, fn in (("gemm_only_ms", gemm_only), ("fold_only_ms", fold_only)):
+            g = capture(fn, stream)
+            out[nm_] = statistics.median(time_graph(g, stream, replays))
+            del g
     if mlg.mlg_read_device_errors(clear=True) or errors_before:
         raise RuntimeError("device error bits were set during the benchmark")
     if e2e:
@@ -674,6 +722,16 @@ def summarize(name, r, peak, steps, cpu=None):
                                          if con > 0 else None)
         out["contended_copy_bytes"] = r["contended_copy_bytes"]
         out["contended_copy_us"] = r["contended_copy_ms"] * 1e3
+    if "gemm_only_ms" in r:
+        out["gemm_only_us"] = r["gemm_only_ms"] / steps * 1e3
+        out["fold_only_us"] = r["fold_only_ms"] / steps * 1e3
+        out["unfused_us"] = out["gemm_only_us"] + out["fold_only_us"]
+        out["fused_speedup"] = out["unfused_us"] / out["us_per_step"]
+        out["tensor_tflops_peak"] = tensor_peak()[0]
+        t_hbm = r["alg_bytes"] / (peak * 1e9)
+        t_tc = r["alg_flops"] / (tensor_peak()[0] * 1e12)
+        out["bound"] = "hbm" if t_hbm >= t_tc else "tensor"
+        out["roofline_frac"] = max(t_hbm, t_tc) / (ms * 1e-3)
     if "e2e" in r:
         e = r["e2e"]
         out["e2e"] = {"value": r["rows_set0"] / e["s_per_step"], "unit": "rows/s",
@@ -692,7 +750,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--extra", default="decode_down,decode_gate_up,decode_down_multi,prefill_down,"
-                                       "prefill_down_xrows,router",
+                                       "prefill_down_xrows,router,prefill_down_fused",
                     help="other workloads measured in the same run (comma list, or 'none')")
     ap.add_argument("--replays", type=int, default=REPLAYS)
     ap.add_argument("--no-cpu-baseline", action="store_true")

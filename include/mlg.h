@@ -15,12 +15,14 @@
  * ensure_decode_route_servable, build_moe_row_adapter_host,
  * build_moe_row_adapter_decode).
  *
- * Two widened forms sit beside the pages' calls: a per-row x grouped fold
+ * Three widened forms sit beside the pages' calls: a per-row x grouped fold
  * (mlg_grouped_down_xrows: sorted row r reads x_rows[r], the input a down
- * projection has) and a multi-adapter decode fold (mlg_gather_bgmv_multi,
- * with mlg_build_moe_row_adapter_decode_multi: one table set per adapter
- * slot, each token's row-map entry naming its set).  Each states the reading
- * of the pages it rests on.
+ * projection has), the expert GEMM with that fold in its epilogue
+ * (mlg_grouped_gemm_fold_xrows: base_out produced and folded in one pass)
+ * and a multi-adapter decode fold (mlg_gather_bgmv_multi, with
+ * mlg_build_moe_row_adapter_decode_multi: one table set per adapter slot,
+ * each token's row-map entry naming its set).  Each states the reading of
+ * the pages it rests on.
  *
  * Conventions shared by every call:
  *  - Every call that can fail returns an mlg_status; the library never
@@ -275,6 +277,40 @@ MLG_API mlg_status mlg_grouped_down_xrows(const mlg_bf16 *x_rows, const int32_t 
                                           int32_t k_in, int32_t max_rank, int32_t n_out,
                                           int32_t top_k, int32_t n_experts, int32_t row_offset,
                                           int32_t row_end, uint32_t cap, void *stream);
+
+/* The expert GEMM with the fold in its epilogue (per-row x form).  The
+ * moe_lora_grouped module index folds into base_out (moe_lora_grouped_down),
+ * and base_out is the expert projection's output; computing both in one pass
+ * means base_out is written once instead of written, read back and written
+ * again.  For every sorted row r in [row_offset, row_end) held by span
+ * e < n_experts whose weight cell w_table[e] is non-zero:
+ *     out[r] = RNE_bf16( x_rows[r] @ W_e^T
+ *                        + [row folds] scale_e * (x_rows[r] @ A_e^T) @ B_e^T )
+ * with W_e [n_out, k_in] bf16 row-major at w_table[e], the products and sums
+ * in fp32 (tensor cores) and one rounding.  A row folds under the rules of
+ * mlg_grouped_down_xrows (LoRA cells non-zero, src[r] >= 0, row-map entry of
+ * its token not negative); a row that does not fold still gets the GEMM.
+ * Rows of a span whose weight cell is 0 (or not 16-byte aligned), rows
+ * outside the range and rows past expert_offsets[n_experts] are not outputs
+ * of this call: out keeps their bits.  The range is processed in windows of
+ * cap rows in ONE launch; the result does not depend on cap.
+ *
+ *   x_rows         device, [>= row_end, k_in] bf16, 16-byte aligned
+ *   w_table        device, [n_experts] uint64 addresses of W_e (0 = no weight)
+ *   expert_offsets, src, row_adapter, a/b/scale tables
+ *                  as for mlg_grouped_down_xrows (src non-NULL)
+ *   out            device, [>= row_end, n_out] bf16, written (not read), 16-byte aligned
+ * With every LoRA cell 0 this is a plain grouped expert GEMM.  Errors as for
+ * mlg_grouped_down_xrows. */
+MLG_API mlg_status mlg_grouped_gemm_fold_xrows(const mlg_bf16 *x_rows,
+                                               const int32_t *expert_offsets, const int32_t *src,
+                                               const int32_t *row_adapter,
+                                               const uint64_t *w_table, const uint64_t *a_table,
+                                               const uint64_t *b_table, const float *scale_table,
+                                               mlg_bf16 *out, int32_t k_in, int32_t max_rank,
+                                               int32_t n_out, int32_t top_k, int32_t n_experts,
+                                               int32_t row_offset, int32_t row_end, uint32_t cap,
+                                               void *stream);
 
 /* The router fold (MoeExpertRoute, moe_lora_grouped module index): a one-entry
  * route whose expert 0 is the router pair, so every token t folds

@@ -64,6 +64,7 @@ _SIGNATURES = {
     "mlg_router_fold": ([_p] * 6 + [_i32] * 4 + [_p], _i32),
     "mlg_grouped_down_all_windows": ([_p] * 8 + [_i32] * 6 + [_u32, _p], _i32),
     "mlg_grouped_down_xrows": ([_p] * 8 + [_i32] * 7 + [_u32, _p], _i32),
+    "mlg_grouped_gemm_fold_xrows": ([_p] * 9 + [_i32] * 7 + [_u32, _p], _i32),
     "mlg_resolve_moe_lora_route": ([_i32, _i32, _i32], _i32),
     "mlg_ensure_decode_route_servable": ([_i32], _i32),
     "mlg_build_moe_row_adapter_decode": ([_p, _sz, _sz, _i32, _i32, _p], _i32),
@@ -200,6 +201,16 @@ def mlg_grouped_down_xrows(x_rows, expert_offsets, src, row_adapter, a_table, b_
         _addr(x_rows), _addr(expert_offsets), _addr(src), _addr(row_adapter), _addr(a_table),
         _addr(b_table), _addr(scale_table), _addr(base_out), k_in, max_rank, n_out, top_k,
         n_experts, row_offset, row_end, cap, _stream(stream)), "mlg_grouped_down_xrows")
+
+
+def mlg_grouped_gemm_fold_xrows(x_rows, expert_offsets, src, row_adapter, w_table, a_table,
+                                b_table, scale_table, out, k_in, max_rank, n_out, top_k,
+                                n_experts, row_offset, row_end, cap, stream=None) -> None:
+    _check(lib().mlg_grouped_gemm_fold_xrows(
+        _addr(x_rows), _addr(expert_offsets), _addr(src), _addr(row_adapter), _addr(w_table),
+        _addr(a_table), _addr(b_table), _addr(scale_table), _addr(out), k_in, max_rank, n_out,
+        top_k, n_experts, row_offset, row_end, cap, _stream(stream)),
+        "mlg_grouped_gemm_fold_xrows")
 
 
 def mlg_router_fold(x, row_adapter, a_table, b_table, scale_table, base_out, n_tokens, k_in,

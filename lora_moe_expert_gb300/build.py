@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libmlg.so")
 
-SOURCES = ["mlg_host.cpp", "mlg_gather.cu", "mlg_decode.cu", "mlg_grouped.cu"]
+SOURCES = ["mlg_host.cpp", "mlg_gather.cu", "mlg_decode.cu", "mlg_grouped.cu", "mlg_gemm_fold.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -210,6 +210,7 @@ int32_t mlg_version(void) { return 10000; }
 namespace mlg {
 uint32_t gather_read_errors(bool clear);
 uint32_t grouped_read_errors(bool clear);
+uint32_t gemm_fold_read_errors(bool clear);
 void gather_set_cluster_override(int cs);
 void gather_set_nsplit_override(int ns2);
 void grouped_set_ctas(int ctas);
@@ -222,7 +223,7 @@ extern "C" mlg_status mlg_read_device_errors(uint32_t *flags_out, int32_t clear)
   if (flags_out == nullptr) return MLG_ERR_INVALID_ARG;
   cudaGetLastError();
   const uint32_t v = mlg::gather_read_errors(clear != 0) | mlg::grouped_read_errors(clear != 0) |
-                     mlg::decode_read_errors(clear != 0);
+                     mlg::decode_read_errors(clear != 0) | mlg::gemm_fold_read_errors(clear != 0);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return mlg::cuda_status(err);
   *flags_out = v;

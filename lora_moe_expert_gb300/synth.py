@@ -38,6 +38,9 @@ Shapes of the named workloads:
                        n_out 2048, windows of 32768 rows
 * ``router``           one-entry route over 16384 tokens, k_in 2048,
                        n_out 512, rank 32
+* ``prefill_down_fused`` ``prefill_down_xrows`` plus every expert's GEMM
+                       weight W_e [2048, 768] ~ N(0, 1/768): the expert GEMM
+                       with the fold in its epilogue
 """
 from __future__ import annotations
 
@@ -103,6 +106,10 @@ class Workload:
     # multi-adapter form: tables of n_adapters * n_experts_model cells, slot-major
     # (expert_id of an Expert is its cell, slot * n_experts_model + expert)
     n_adapters: int = 0
+    # expert GEMM weights for the fused GEMM + fold form: expert id -> W_e bits
+    # [n_out, k_in] (experts without an entry have no weight); base then holds
+    # the output buffer's prior contents, which rows without a weight keep
+    weights: Optional[dict] = None
 
     @property
     def rows(self) -> int:
@@ -211,6 +218,25 @@ def prefill_down_xrows(seed: int = 2) -> Workload:
     return w
 
 
+def add_expert_weights(w: Workload, seed: int, frac: float = 1.0) -> Workload:
+    """Give a per-row x prefill workload expert GEMM weights W_e ~ N(0, 1/k_in)
+    [n_out, k_in] for a seeded fraction of its experts (all by default)."""
+    rng = np.random.default_rng(seed)
+    E = w.n_experts_model
+    n = max(1, int(round(frac * E)))
+    ids = np.sort(rng.choice(E, size=n, replace=False)) if n < E else np.arange(E)
+    w.weights = {int(e): _normal_bf16(rng, (w.n_out, w.k_in), 1.0 / w.k_in) for e in ids}
+    return w
+
+
+def prefill_down_fused(seed: int = 2) -> Workload:
+    """prefill_down_xrows with every expert's down-projection weight: the
+    expert GEMM and the fold in one pass."""
+    w = prefill_down_xrows(seed)
+    w.name = "prefill_down_fused"
+    return add_expert_weights(w, seed + 7000)
+
+
 def prefill_large(seed: int = 4) -> Workload:
     rng = np.random.default_rng(seed)
     return _prefill("prefill_large", rng, np.array([16384]), 10, 512, 512, 2048, 32, 32768)
@@ -282,7 +308,8 @@ def decode_down_multi(seed: int = 6) -> Workload:
 def custom_grouped(seed: int, lengths, top_k: int, n_experts: int, k_in: int, n_out: int,
                    max_rank: int, cap: int, adapted_frac: float = 1.0,
                    stream_base: Optional[List[int]] = None,
-                   rank: Optional[int] = None, per_row_x: bool = False) -> Workload:
+                   rank: Optional[int] = None, per_row_x: bool = False,
+                   weight_frac: float = 0.0) -> Workload:
     """A packed prefill batch of arbitrary shape (for parity sweeps and edge cases)."""
     rng = np.random.default_rng(seed)
     n_adapt = max(1, int(round(adapted_frac * n_experts)))
@@ -298,6 +325,8 @@ def custom_grouped(seed: int, lengths, top_k: int, n_experts: int, k_in: int, n_
         w.stream_slots = np.array([-1 if b else 0 for b in stream_base], np.int32)
     if per_row_x:
         w.x_rows = _normal_bf16(rng, (w.rows, k_in))
+    if weight_frac > 0:
+        add_expert_weights(w, seed + 7000, weight_frac)
     return w
 
 
@@ -319,4 +348,5 @@ NAMED = {
     "decode_down_multi": decode_down_multi,
     "prefill_large": prefill_large,
     "router": router,
+    "prefill_down_fused": prefill_down_fused,
 }

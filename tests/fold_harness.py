@@ -45,8 +45,21 @@ def rne_bf16_f64(ref: np.ndarray) -> np.ndarray:
     return bits, np.abs(ref - mid)
 
 
+def weight_table(w, n_table):
+    """Host table of the host addresses of w.weights (0 = no weight), and the
+    arrays it points into (keep them alive while the oracle runs)."""
+    keep = [np.ascontiguousarray(w.weights[e], np.uint16) for e in sorted(w.weights)]
+    table = np.zeros(n_table, np.uint64)
+    for e, m in zip(sorted(w.weights), keep):
+        table[e] = m.ctypes.data
+    return table, keep
+
+
 def oracle_reference(w, o=None, row_offset=None, row_end=None):
-    """(ref fp64, folded bool, keepalive) for the whole workload."""
+    """(ref fp64, folded bool, keepalive) for the whole workload.  For the
+    expert GEMM with the fold (w.weights set) the mask marks the rows the
+    call writes (the GEMM rows, folded or not); every other row keeps its
+    bits."""
     o = o or oracle.get()
     he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
     if w.n_adapters:
@@ -58,6 +71,17 @@ def oracle_reference(w, o=None, row_offset=None, row_end=None):
                                           w.max_rank, w.n_out, w.top_k, w.n_experts_model,
                                           w.n_adapters)
         return ref, folded, (he, at.size)
+    if w.weights is not None:  # the expert GEMM with the fold in its epilogue
+        n_table = max(max(e.expert_id for e in w.experts) + 1, w.n_experts_model)
+        at, bt, st = he.tables(o, length=n_table)
+        wt, keep_w = weight_table(w, n_table)
+        ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+        lo = 0 if row_offset is None else row_offset
+        hi = w.rows if row_end is None else row_end
+        ref, written, _ = o.grouped_gemm_fold_xrows(w.x_rows, w.expert_offsets, w.src, ra, wt,
+                                                    at, bt, st, w.base, w.k_in, w.max_rank,
+                                                    w.n_out, w.top_k, lo, hi)
+        return ref, written, (he, at.size, keep_w)
     at, bt, st = he.tables(o)
     if w.kind == "gather":
         ra = o.build_moe_row_adapter_decode(w.adapter_slots, w.padded_n, w.active,

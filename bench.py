@@ -171,14 +171,14 @@ def algorithmic(w, row_map, tables):
         # (x_rows) and written once (out), each such expert's W_e is read once
         e_span = np.repeat(np.arange(w.n_experts_model), np.diff(w.expert_offsets))
         e_span = np.concatenate([e_span, np.full(rows - e_span.size, -1)])
-        has_w = np.array([int(v) in w.weights for v in e_span]) if rows else np.zeros(0, bool)
+        has_w = e_span >= 0
         written = int(has_w.sum())
         w_experts = np.unique(e_span[has_w]).size
         ok &= has_w
         folded = int(ok.sum())
         experts = np.unique(e[ok]).size
         nbytes = (written * k * 2 + w_experts * n * k * 2 + experts * r * (k + n) * 2
-                  + written * n * 2 + idx_bytes + E * 8)
+                  + written * n * 2 + idx_bytes)
         flops = 2 * written * k * n + 2 * folded * r * (k + n)
         return rows, folded, int(nbytes), int(flops)
     n_x = folded if w.x_rows is not None else tokens  # per-row x: one x row per folding row
@@ -363,7 +363,8 @@ def make_sets(name, device, seed_base):
     w0 = gen()
     p0 = FoldProblem(w0, device=device)
     ws_bytes = (w0.x.nbytes + w0.base.nbytes + sum(e.A.nbytes + e.B.nbytes for e in w0.experts)
-                + (w0.x_rows.nbytes if w0.x_rows is not None else 0))
+                + (w0.x_rows.nbytes if w0.x_rows is not None else 0)
+                + (w0.weights.nbytes if w0.weights is not None else 0))
     nsets = n_sets_for(ws_bytes)
     big = ws_bytes > L2_BYTES // 2
     probs = [p0] + [FoldProblem(w0 if big else gen(seed=seed_base + i), device=device)

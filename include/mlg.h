@@ -283,29 +283,31 @@ MLG_API mlg_status mlg_grouped_down_xrows(const mlg_bf16 *x_rows, const int32_t 
  * and base_out is the expert projection's output; computing both in one pass
  * means base_out is written once instead of written, read back and written
  * again.  For every sorted row r in [row_offset, row_end) held by span
- * e < n_experts whose weight cell w_table[e] is non-zero:
+ * e < n_experts:
  *     out[r] = RNE_bf16( x_rows[r] @ W_e^T
  *                        + [row folds] scale_e * (x_rows[r] @ A_e^T) @ B_e^T )
- * with W_e [n_out, k_in] bf16 row-major at w_table[e], the products and sums
- * in fp32 (tensor cores) and one rounding.  A row folds under the rules of
- * mlg_grouped_down_xrows (LoRA cells non-zero, src[r] >= 0, row-map entry of
- * its token not negative); a row that does not fold still gets the GEMM.
- * Rows of a span whose weight cell is 0 (or not 16-byte aligned), rows
- * outside the range and rows past expert_offsets[n_experts] are not outputs
- * of this call: out keeps their bits.  The range is processed in windows of
- * cap rows in ONE launch; the result does not depend on cap.
+ * with W_e [n_out, k_in] the expert's slice of the stacked weights, the
+ * products and sums in fp32 (tensor cores) and one rounding.  A row folds
+ * under the rules of mlg_grouped_down_xrows (LoRA cells non-zero, src[r] >= 0,
+ * row-map entry of its token not negative); a row that does not fold still
+ * gets the GEMM.  Rows outside the range and rows past
+ * expert_offsets[n_experts] are not outputs of this call: out keeps their
+ * bits.  The range is processed in windows of cap rows in ONE launch; the
+ * result does not depend on cap.
  *
  *   x_rows         device, [>= row_end, k_in] bf16, 16-byte aligned
- *   w_table        device, [n_experts] uint64 addresses of W_e (0 = no weight)
+ *   w_experts      device, [n_experts, n_out, k_in] bf16 (the experts' weights
+ *                  stacked, each row-major), 16-byte aligned; read only
  *   expert_offsets, src, row_adapter, a/b/scale tables
- *                  as for mlg_grouped_down_xrows (src non-NULL)
+ *                  as for mlg_grouped_down_xrows (src non-NULL); the tables
+ *                  have n_experts cells
  *   out            device, [>= row_end, n_out] bf16, written (not read), 16-byte aligned
  * With every LoRA cell 0 this is a plain grouped expert GEMM.  Errors as for
  * mlg_grouped_down_xrows. */
 MLG_API mlg_status mlg_grouped_gemm_fold_xrows(const mlg_bf16 *x_rows,
                                                const int32_t *expert_offsets, const int32_t *src,
                                                const int32_t *row_adapter,
-                                               const uint64_t *w_table, const uint64_t *a_table,
+                                               const mlg_bf16 *w_experts, const uint64_t *a_table,
                                                const uint64_t *b_table, const float *scale_table,
                                                mlg_bf16 *out, int32_t k_in, int32_t max_rank,
                                                int32_t n_out, int32_t top_k, int32_t n_experts,

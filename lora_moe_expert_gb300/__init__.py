@@ -203,11 +203,11 @@ def mlg_grouped_down_xrows(x_rows, expert_offsets, src, row_adapter, a_table, b_
         n_experts, row_offset, row_end, cap, _stream(stream)), "mlg_grouped_down_xrows")
 
 
-def mlg_grouped_gemm_fold_xrows(x_rows, expert_offsets, src, row_adapter, w_table, a_table,
+def mlg_grouped_gemm_fold_xrows(x_rows, expert_offsets, src, row_adapter, w_experts, a_table,
                                 b_table, scale_table, out, k_in, max_rank, n_out, top_k,
                                 n_experts, row_offset, row_end, cap, stream=None) -> None:
     _check(lib().mlg_grouped_gemm_fold_xrows(
-        _addr(x_rows), _addr(expert_offsets), _addr(src), _addr(row_adapter), _addr(w_table),
+        _addr(x_rows), _addr(expert_offsets), _addr(src), _addr(row_adapter), _addr(w_experts),
         _addr(a_table), _addr(b_table), _addr(scale_table), _addr(out), k_in, max_rank, n_out,
         top_k, n_experts, row_offset, row_end, cap, _stream(stream)),
         "mlg_grouped_gemm_fold_xrows")

@@ -4,8 +4,8 @@
 // moe_lora_grouped_down (moe_lora_grouped module index) folds into base_out,
 // and base_out is the expert projection's output.  Producing both in one
 // kernel removes base_out's round trip through HBM: for every expert-sorted
-// row r in [row_offset, row_end) held by span e < n_experts whose weight cell
-// w_table[e] is non-zero (W_e [n_out, k_in] bf16),
+// row r in [row_offset, row_end) held by span e < n_experts (W_e [n_out, k_in]
+// bf16, slice e of the stacked expert weights),
 //     out[r] = RNE_bf16( x_rows[r] @ W_e^T + [row folds] scale_e * (x_rows[r] @ A_e^T) @ B_e^T ),
 // a row folding under the per-row x fold's rules (non-zero, aligned LoRA
 // cells, src[r] >= 0 and a non-negative row-map entry for its token).
@@ -13,16 +13,18 @@
 // GB300 design (one CTA per SM, persistent over expert-aligned tiles of <= 128
 // rows that never cross a row window):
 //  * one shared-memory ring of stages, each an X box (128 rows x 64 k, TMA,
-//    128-byte swizzle) and a Y tile (up to 256 rows x 64 k, 16-byte cp.async
-//    into the same swizzle); per tile the ring carries, in order, the shrink's
-//    stages [X | A_e chunk], then for every 256-column output chunk the GEMM
-//    stages [X | W_e chunk] and one expand stage [- | B_e chunk];
+//    128-byte swizzle) and a Y tile (up to 256 rows x 64 k in the same
+//    swizzle); per tile the ring carries, in order, the shrink's stages
+//    [X | A_e chunk], then for every 256-column output chunk the GEMM stages
+//    [X | W_e chunk] and one expand stage [- | B_e chunk].  X and W_e come in
+//    as TMA boxes (W_e through one 3-D tensor map over the stacked weights);
+//    A_e and B_e, found through the tables at run time, by 16-byte cp.async;
 //  * warp 0 issues tcgen05.mma (kind::f16, cta_group::1): H = X A_e^T into a
 //    TMEM h buffer; per output chunk ACC = X W_e^T (M 128, N <= 256, K 64 a
 //    stage) into the TMEM accumulator, then ACC += [H_hi | H_lo] [B_e | B_e]^T
 //    with h split into two bf16 halves (about 2^-18 relative), so h enters
 //    the expand at about fp32 precision;
-//  * warps 1-2 fill the ring (warp 1 lane 0 issues the X boxes);
+//  * warps 1-2 fill the ring (warp 1 lane 0 issues the TMA boxes);
 //  * warps 4-11 split h (scaled, zero for rows that do not fold) into shared
 //    memory, and per output chunk read their 32 rows x 128 columns of the
 //    accumulator, release it, round once to bf16 and store the rows of the
@@ -60,7 +62,7 @@ struct FusedParams {
   const int32_t *offsets;        // [n_experts + 1]
   const int32_t *src;            // sorted row -> flat row (row map only)
   const int32_t *row_adapter;    // [n_tokens] or null
-  const uint64_t *w_table, *a_table, *b_table;
+  const uint64_t *a_table, *b_table;
   const float *scale_table;
   uint8_t *out;                  // bf16 [>= row_end, n_out], written
   int32_t k_in, rank, n_out, top_k, n_experts, row_offset, row_end;
@@ -101,7 +103,17 @@ __device__ __forceinline__ bool wait_f(FCtl &ctl, uint64_t &bar, uint32_t parity
   }
 }
 
-__device__ __forceinline__ bool weight_ok(uint64_t w) { return w != 0 && (w & 15u) == 0; }
+// 3-D TMA load (x innermost, then y, then z) into shared memory, completion
+// counted on `bar` in bytes, with an L2 cache hint.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, int32_t x,
+                                                 int32_t y, int32_t z, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
 
 __device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -113,7 +125,8 @@ __device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, ui
 // RP: rank rounded up to a multiple of 16.
 template <int RP>
 __global__ void __launch_bounds__(kThreadsF, 1)
-    gemm_fold_kernel(const __grid_constant__ CUtensorMap tmap_x, const FusedParams p) {
+    gemm_fold_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                     const __grid_constant__ CUtensorMap tmap_w, const FusedParams p) {
   constexpr int KEXP = (2 * RP + 63) / 64 * 64;  // expand K: [hi | lo | zero pad]
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ FCtl ctl;
@@ -138,6 +151,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     ctl.abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_x);
+    prefetch_tmap(&tmap_w);
   }
   __syncthreads();
   if (warp == 0) {
@@ -149,18 +163,14 @@ __global__ void __launch_bounds__(kThreadsF, 1)
   griddep_launch_dependents();
   griddep_wait();
 
-  // Tile table: an expert with a weight contributes ceil(rows in window / 128)
-  // tiles (0 without a weight); exclusive prefix over experts.
+  // Tile table: expert e contributes ceil(rows in window / 128) tiles;
+  // exclusive prefix over experts.
   {
     int carry = 0;
     for (int base = 0; base < n_e; base += kThreadsF) {
       const int e = base + tid;
       int n = 0;
-      if (e < n_e) {
-        const int lo = span_lo(p, e), hi = span_hi(p, e);
-        const uint64_t w = __ldg(reinterpret_cast<const unsigned long long *>(p.w_table) + e);
-        if (hi > lo && weight_ok(w)) n = span_tiles(p, lo, hi);
-      }
+      if (e < n_e) n = span_tiles(p, span_lo(p, e), span_hi(p, e));
       int incl = n;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -310,14 +320,17 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         --nq;
       }
     };
-    // Begin a stage: wait for it to be free; lane 0 of warp 1 issues the X box.
-    auto begin = [&](int r0, int k0, bool with_x) -> int {
+    // Begin a stage: wait for it to be free; lane 0 of warp 1 issues the X box
+    // and, for a GEMM stage (e >= 0), the W_e box of rows n0.. .
+    auto begin = [&](int r0, int k0, bool with_x, int e, int n0) -> int {
       const int st = it % p.nst;
       if (!wait_f(ctl, ctl.empty[st], ((it / p.nst) & 1) ^ 1)) return -1;
       if (with_x && pw == 0 && lane == 0) {
         const uint32_t full = smem_addr(&ctl.full[st]);
-        mbar_expect_tx(full, kXBytes);
-        tma_load_2d_hint(ring + st * p.stage_bytes, &tmap_x, k0, r0, full, once);
+        const uint32_t xs = ring + st * p.stage_bytes;
+        mbar_expect_tx(full, e >= 0 ? kXBytes + kYBytes : kXBytes);
+        tma_load_2d_hint(xs, &tmap_x, k0, r0, full, once);
+        if (e >= 0) tma_load_3d_hint(xs + kXBytes, &tmap_w, k0, n0, e, full, keep);
       }
       return st;
     };
@@ -329,15 +342,13 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     };
     for (int t = 0; t < n_tiles; ++t) {
       const FTile mt = my_tiles[t];
-      const uint8_t *W = reinterpret_cast<const uint8_t *>(
-          __ldg(reinterpret_cast<const unsigned long long *>(p.w_table) + mt.e));
       const uint8_t *A = reinterpret_cast<const uint8_t *>(
           __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + mt.e));
       const uint8_t *B = reinterpret_cast<const uint8_t *>(
           __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + mt.e));
       if (mt.lora) {  // [X | A_e rows 0..RP)
         for (int kc = 0; kc < p.kc_count; ++kc) {
-          const int st = begin(mt.r0, kc * 64, true);
+          const int st = begin(mt.r0, kc * 64, true, -1, 0);
           if (st < 0) goto fill_done;
           const uint32_t ys = ring + st * p.stage_bytes + kXBytes;
           const int kk = kc * 64 + 8 * c;
@@ -353,25 +364,13 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       }
       for (int nc = 0; nc < p.nc_count; ++nc) {
         const int n0 = nc * kNch;
-        for (int kc = 0; kc < p.kc_count; ++kc) {  // [X | W_e rows n0.., k chunk kc]
-          const int st = begin(mt.r0, kc * 64, true);
+        for (int kc = 0; kc < p.kc_count; ++kc) {  // [X | W_e rows n0.., k chunk kc]: TMA only
+          const int st = begin(mt.r0, kc * 64, true, mt.e, n0);
           if (st < 0) goto fill_done;
-          const uint32_t ys = ring + st * p.stage_bytes + kXBytes;
-          const int kk = kc * 64 + 8 * c;
-          const bool kin = kk < p.k_in;
-#pragma unroll 8
-          for (int i = 0; i < 32; ++i) {
-            const int row = pw * 128 + 4 * i + rq;
-            const int n = n0 + row;
-            const bool in = kin && n < p.n_out;
-            cp_async_16_hint(ys + sw128(row, c),
-                             W + (in ? (static_cast<size_t>(n) * p.k_in + kk) * 2 : 0),
-                             in ? 16u : 0u, keep);
-          }
           finish(st);
         }
         if (mt.lora) {  // [- | B_e rows n0.., rank columns (zero past rank)]
-          const int st = begin(0, 0, false);
+          const int st = begin(0, 0, false, -1, 0);
           if (st < 0) goto fill_done;
           const uint32_t ys = ring + st * p.stage_bytes + kXBytes;
           if (c < RP / 8) {
@@ -574,7 +573,7 @@ uint32_t gemm_fold_read_errors(bool clear) {
 
 extern "C" mlg_status mlg_grouped_gemm_fold_xrows(
     const mlg_bf16 *x_rows, const int32_t *expert_offsets, const int32_t *src,
-    const int32_t *row_adapter, const uint64_t *w_table, const uint64_t *a_table,
+    const int32_t *row_adapter, const mlg_bf16 *w_experts, const uint64_t *a_table,
     const uint64_t *b_table, const float *scale_table, mlg_bf16 *out, int32_t k_in,
     int32_t max_rank, int32_t n_out, int32_t top_k, int32_t n_experts, int32_t row_offset,
     int32_t row_end, uint32_t cap, void *stream) {
@@ -584,17 +583,16 @@ extern "C" mlg_status mlg_grouped_gemm_fold_xrows(
     return MLG_ERR_INVALID_ARG;
   const mlg_status shape = check_shapes(k_in, max_rank, n_out);
   if (shape != MLG_OK) return shape;
-  if (!x_rows || !expert_offsets || !src || !w_table || !a_table || !b_table || !scale_table ||
+  if (!x_rows || !expert_offsets || !src || !w_experts || !a_table || !b_table || !scale_table ||
       !out)
     return MLG_ERR_INVALID_ARG;
-  if (!aligned16(x_rows) || !aligned16(out)) return MLG_ERR_UNSUPPORTED;
+  if (!aligned16(x_rows) || !aligned16(out) || !aligned16(w_experts)) return MLG_ERR_UNSUPPORTED;
   if (row_end == row_offset || n_experts == 0) return MLG_OK;
   FusedParams p = {};
   p.x = reinterpret_cast<const uint8_t *>(x_rows);
   p.offsets = expert_offsets;
   p.src = src;
   p.row_adapter = row_adapter;
-  p.w_table = w_table;
   p.a_table = a_table;
   p.b_table = b_table;
   p.scale_table = scale_table;
@@ -627,6 +625,19 @@ extern "C" mlg_status mlg_grouped_gemm_fold_xrows(
   const cuuint32_t estr[2] = {1, 1};
   if (enc(&tmap_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<mlg_bf16 *>(x_rows), xdims,
           xstrides, xbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MLG_ERR_CUDA;
+  // W: the stacked expert weights [n_experts, n_out, k_in], boxes of 64 k x
+  // 256 rows of one expert (rows past n_out and k past k_in read as zero).
+  CUtensorMap tmap_w;
+  const cuuint64_t wdims[3] = {static_cast<cuuint64_t>(k_in), static_cast<cuuint64_t>(n_out),
+                               static_cast<cuuint64_t>(n_experts)};
+  const cuuint64_t wstrides[2] = {static_cast<cuuint64_t>(k_in) * 2,
+                                  static_cast<cuuint64_t>(k_in) * n_out * 2};
+  const cuuint32_t wbox[3] = {64, static_cast<cuuint32_t>(kNch), 1};
+  const cuuint32_t estr3[3] = {1, 1, 1};
+  if (enc(&tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<mlg_bf16 *>(w_experts), wdims,
+          wstrides, wbox, estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return MLG_ERR_CUDA;
 
@@ -669,7 +680,7 @@ extern "C" mlg_status mlg_grouped_gemm_fold_xrows(
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  using KernelFn = void (*)(CUtensorMap, FusedParams);
+  using KernelFn = void (*)(CUtensorMap, CUtensorMap, FusedParams);
   KernelFn fn;
   switch (p.r_pad) {
     case 16: fn = gemm_fold_kernel<16>; break;
@@ -677,7 +688,7 @@ extern "C" mlg_status mlg_grouped_gemm_fold_xrows(
     case 48: fn = gemm_fold_kernel<48>; break;
     default: fn = gemm_fold_kernel<64>; break;
   }
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, fn, tmap_x, p);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, fn, tmap_x, tmap_w, p);
   if (err != cudaSuccess) return cuda_status(err);
   return cuda_status(cudaGetLastError());
 }

@@ -64,24 +64,6 @@ class ExpertPool:
         self.nbytes = pos
 
 
-def _weight_pool(weights, n_table: int, device):
-    """Expert GEMM weights in one allocation (each 256-byte aligned) and the
-    host table of their device addresses, n_table long (0 = no weight)."""
-    ids = sorted(weights)
-    offs, pos = {}, 0
-    for e in ids:
-        offs[e] = pos
-        pos += (weights[e].nbytes + _ALIGN - 1) // _ALIGN * _ALIGN
-    host = np.zeros(max(pos, _ALIGN), np.uint8)
-    for e in ids:
-        host[offs[e]:offs[e] + weights[e].nbytes] = weights[e].view(np.uint8).reshape(-1)
-    buf = _dev(host, device)
-    table = np.zeros(max(n_table, max(ids) + 1 if ids else 0), np.uint64)
-    for e in ids:
-        table[e] = buf.data_ptr() + offs[e]
-    return buf, table
-
-
 class FoldProblem:
     def __init__(self, w, device="cuda", stream=None, guard_rows: int = 0,
                  pool: Optional[ExpertPool] = None):
@@ -93,8 +75,8 @@ class FoldProblem:
                                              self.pool.scale)
         if w.n_adapters:  # slot-major sets of n_experts_model cells; trailing holes are zero
             a, b, s = pad_tables(a, b, s, w.n_adapters * w.n_experts_model)
-        if w.weights is not None:  # one table length for the weights and the LoRA cells
-            a, b, s = pad_tables(a, b, s, max(a.size, w.n_experts_model))
+        if w.weights is not None:  # one table cell per expert of the stacked weights
+            a, b, s = pad_tables(a, b, s, w.n_experts_model)
         self.n_experts = int(a.size)
         self.a_table = torch.empty(self.n_experts, dtype=torch.int64, device=self.device)
         self.b_table = torch.empty(self.n_experts, dtype=torch.int64, device=self.device)
@@ -128,12 +110,12 @@ class FoldProblem:
             self.row_adapter = torch.empty(self.row_map_host.size, dtype=torch.int32,
                                            device=self.device)
             mlg.mlg_upload_row_adapter(self.row_map_host, self.row_adapter, stream=self._stream())
-        self.w_pool = None
-        self.w_table = None
+        self.w_experts = None
         self.zero_table = None
-        if w.weights is not None:  # expert GEMM weights: one pool, a table of addresses
-            self.w_pool, self.w_table_host = _weight_pool(w.weights, self.n_experts, self.device)
-            self.w_table = _dev(self.w_table_host.view(np.int64), self.device)
+        if w.weights is not None:  # the stacked expert GEMM weights
+            if w.weights.shape[0] != self.n_experts:
+                raise ValueError("stacked weights must cover every table cell")
+            self.w_experts = _bits_tensor(w.weights, self.device)
             self.zero_table = torch.zeros(self.n_experts, dtype=torch.int64, device=self.device)
 
     def _stream(self):
@@ -160,11 +142,11 @@ class FoldProblem:
             mlg.mlg_gather_bgmv(self.x, self.indices, self.row_adapter, self.a_table,
                                 self.b_table, self.scale_table, self.base, w.rows, w.k_in,
                                 w.max_rank, w.n_out, w.top_k, self.n_experts, stream=s)
-        elif w.kind == "grouped" and self.w_table is not None:
+        elif w.kind == "grouped" and self.w_experts is not None:
             ra = self.row_adapter if use_row_map else None
             a, b = (self.a_table, self.b_table) if lora else (self.zero_table, self.zero_table)
             mlg.mlg_grouped_gemm_fold_xrows(self.x_rows, self.expert_offsets, self.src, ra,
-                                            self.w_table, a, b, self.scale_table, self.base,
+                                            self.w_experts, a, b, self.scale_table, self.base,
                                             w.k_in, w.max_rank, w.n_out, w.top_k, self.n_experts,
                                             0, w.rows, w.cap, stream=s)
         elif w.kind == "grouped":

@@ -106,10 +106,10 @@ class Workload:
     # multi-adapter form: tables of n_adapters * n_experts_model cells, slot-major
     # (expert_id of an Expert is its cell, slot * n_experts_model + expert)
     n_adapters: int = 0
-    # expert GEMM weights for the fused GEMM + fold form: expert id -> W_e bits
-    # [n_out, k_in] (experts without an entry have no weight); base then holds
-    # the output buffer's prior contents, which rows without a weight keep
-    weights: Optional[dict] = None
+    # expert GEMM weights for the fused GEMM + fold form: bf16 bits
+    # [n_experts_model, n_out, k_in], the experts' W_e stacked; base then holds
+    # the output buffer's prior contents (rows outside the range keep them)
+    weights: Optional[np.ndarray] = None
 
     @property
     def rows(self) -> int:
@@ -218,14 +218,11 @@ def prefill_down_xrows(seed: int = 2) -> Workload:
     return w
 
 
-def add_expert_weights(w: Workload, seed: int, frac: float = 1.0) -> Workload:
-    """Give a per-row x prefill workload expert GEMM weights W_e ~ N(0, 1/k_in)
-    [n_out, k_in] for a seeded fraction of its experts (all by default)."""
+def add_expert_weights(w: Workload, seed: int) -> Workload:
+    """Give a per-row x prefill workload the stacked expert GEMM weights,
+    W_e ~ N(0, 1/k_in), [n_experts_model, n_out, k_in]."""
     rng = np.random.default_rng(seed)
-    E = w.n_experts_model
-    n = max(1, int(round(frac * E)))
-    ids = np.sort(rng.choice(E, size=n, replace=False)) if n < E else np.arange(E)
-    w.weights = {int(e): _normal_bf16(rng, (w.n_out, w.k_in), 1.0 / w.k_in) for e in ids}
+    w.weights = _normal_bf16(rng, (w.n_experts_model, w.n_out, w.k_in), 1.0 / w.k_in)
     return w
 
 
@@ -309,7 +306,7 @@ def custom_grouped(seed: int, lengths, top_k: int, n_experts: int, k_in: int, n_
                    max_rank: int, cap: int, adapted_frac: float = 1.0,
                    stream_base: Optional[List[int]] = None,
                    rank: Optional[int] = None, per_row_x: bool = False,
-                   weight_frac: float = 0.0) -> Workload:
+                   gemm_weights: bool = False) -> Workload:
     """A packed prefill batch of arbitrary shape (for parity sweeps and edge cases)."""
     rng = np.random.default_rng(seed)
     n_adapt = max(1, int(round(adapted_frac * n_experts)))
@@ -325,8 +322,8 @@ def custom_grouped(seed: int, lengths, top_k: int, n_experts: int, k_in: int, n_
         w.stream_slots = np.array([-1 if b else 0 for b in stream_base], np.int32)
     if per_row_x:
         w.x_rows = _normal_bf16(rng, (w.rows, k_in))
-    if weight_frac > 0:
-        add_expert_weights(w, seed + 7000, weight_frac)
+    if gemm_weights:
+        add_expert_weights(w, seed + 7000)
     return w
 
 

@@ -46,12 +46,14 @@ def rne_bf16_f64(ref: np.ndarray) -> np.ndarray:
 
 
 def weight_table(w, n_table):
-    """Host table of the host addresses of w.weights (0 = no weight), and the
-    arrays it points into (keep them alive while the oracle runs)."""
-    keep = [np.ascontiguousarray(w.weights[e], np.uint16) for e in sorted(w.weights)]
+    """Host table of the host addresses of each expert's slice of the stacked
+    w.weights (0 past them), and the array it points into (keep it alive
+    while the oracle runs)."""
+    keep = np.ascontiguousarray(w.weights, np.uint16)
     table = np.zeros(n_table, np.uint64)
-    for e, m in zip(sorted(w.weights), keep):
-        table[e] = m.ctypes.data
+    step = keep.shape[1] * keep.shape[2] * 2
+    for e in range(min(n_table, keep.shape[0])):
+        table[e] = keep.ctypes.data + e * step
     return table, keep
 
 
@@ -72,7 +74,7 @@ def oracle_reference(w, o=None, row_offset=None, row_end=None):
                                           w.n_adapters)
         return ref, folded, (he, at.size)
     if w.weights is not None:  # the expert GEMM with the fold in its epilogue
-        n_table = max(max(e.expert_id for e in w.experts) + 1, w.n_experts_model)
+        n_table = w.n_experts_model
         at, bt, st = he.tables(o, length=n_table)
         wt, keep_w = weight_table(w, n_table)
         ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)

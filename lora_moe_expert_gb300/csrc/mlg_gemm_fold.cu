@@ -19,11 +19,13 @@
 //    [X | W_e chunk] and one expand stage [- | B_e chunk].  X and W_e come in
 //    as TMA boxes (W_e through one 3-D tensor map over the stacked weights);
 //    A_e and B_e, found through the tables at run time, by 16-byte cp.async;
-//  * warp 0 issues tcgen05.mma (kind::f16, cta_group::1): H = X A_e^T into a
-//    TMEM h buffer; per output chunk ACC = X W_e^T (M 128, N <= 256, K 64 a
-//    stage) into the TMEM accumulator, then ACC += [H_hi | H_lo] [B_e | B_e]^T
+//  * warp 0 issues tcgen05.mma (kind::f16, cta_group::1): per output chunk
+//    ACC = X W_e^T (M 128, N <= 256, K 64 a stage) into one of two TMEM
+//    accumulators (all 512 columns), then ACC += [H_hi | H_lo] [B_e | B_e]^T
 //    with h split into two bf16 halves (about 2^-18 relative), so h enters
-//    the expand at about fp32 precision;
+//    the expand at about fp32 precision; h = X A_e^T itself is computed at
+//    the start of the tile into the first columns of the accumulator that
+//    the tile's first chunk then overwrites;
 //  * warps 1-2 fill the ring (warp 1 lane 0 issues the TMA boxes);
 //  * warps 4-11 split h (scaled, zero for rows that do not fold) into shared
 //    memory, and per output chunk read their 32 rows x 128 columns of the
@@ -51,7 +53,9 @@ constexpr int kNch = 256;            // output columns per accumulator chunk (th
 constexpr int kMaxStagesF = 4;
 constexpr int kMyTilesMaxF = 16;
 constexpr uint32_t kTmemColsF = 512;
-constexpr uint32_t kTmemAccF = 0, kTmemHF = 256;  // accumulator [0, 256), h [256, 256 + rank)
+// TMEM: two 256-column accumulators; a tile's h is computed into the first
+// columns of the accumulator its first output chunk will use.
+__device__ __forceinline__ uint32_t acc_col(int b) { return b ? 256u : 0u; }
 constexpr uint32_t kXBytes = kTileMF * 128;      // X box: 128 rows x 128 bytes
 constexpr uint32_t kYBytes = kNch * 128;         // Y tile: 256 rows x 128 bytes
 
@@ -69,14 +73,14 @@ struct FusedParams {
   int32_t win, tile_m;           // window length, rows per tile
   int32_t r_pad, k_exp;          // rank rounded up to 16; expand K of [hi | lo], padded to 64
   int32_t kc_count, nc_count;    // 64-wide k chunks, 256-column output chunks
-  int32_t nst, lag;              // ring stages; stages in flight before one is signalled
+  int32_t nst;                   // ring stages
   uint32_t stage_bytes;
   uint32_t off_ring, off_h, off_tab, off_my, smem_bytes;
 };
 
 struct FCtl {
   uint64_t full[kMaxStagesF], empty[kMaxStagesF];
-  uint64_t h_full, hs_full, hs_empty, acc_full, acc_empty, drain;
+  uint64_t h_full, hs_full, hs_empty, acc_full[2], acc_empty[2], drain;
   uint32_t tmem_base;
   volatile int abort_flag;
 };
@@ -115,6 +119,18 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap,
       : "memory");
 }
 
+// Arrive on `bar` once all cp.async copies this thread has issued so far have
+// landed; the arrival is one of the barrier's expected arrivals (no increment).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
@@ -145,8 +161,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     mbar_init(smem_addr(&ctl.h_full), 1);
     mbar_init(smem_addr(&ctl.hs_full), 4);
     mbar_init(smem_addr(&ctl.hs_empty), 1);
-    mbar_init(smem_addr(&ctl.acc_full), 1);
-    mbar_init(smem_addr(&ctl.acc_empty), kEpiWarpsF);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&ctl.acc_full[b]), 1);
+      mbar_init(smem_addr(&ctl.acc_empty[b]), kEpiWarpsF);
+    }
     mbar_init(smem_addr(&ctl.drain), 1);
     ctl.abort_flag = 0;
     fence_mbar_init();
@@ -224,25 +242,38 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       uint32_t it = 0, acc_it = 0, h_it = 0;
       for (int t = 0; t < n_tiles; ++t) {
         const FTile mt = my_tiles[t];
-        if (mt.lora) {  // H = X A_e^T
+        const int b0 = acc_it & 1;  // the accumulator of the tile's first chunk
+        if (mt.lora) {
+          // H = X A_e^T into the first columns of accumulator b0, once it is free
+          if (!wait_f(ctl, ctl.acc_empty[b0], ((acc_it >> 1) & 1) ^ 1)) goto mma_done;
+          tc_fence_after();
           for (int kc = 0; kc < p.kc_count; ++kc, ++it) {
             const int st = it % p.nst;
             if (!wait_f(ctl, ctl.full[st], (it / p.nst) & 1)) goto mma_done;
+            fence_proxy_async_smem();  // A_e came in by cp.async (generic proxy)
             tc_fence_after();
             const uint32_t xs = ring + st * p.stage_bytes, ys = xs + kXBytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              umma_bf16(tmem + kTmemHF, umma_desc_sw128(xs + k * 32), umma_desc_sw128(ys + k * 32),
-                        idesc_shrink, (kc | k) != 0);
+              umma_bf16(tmem + acc_col(b0), umma_desc_sw128(xs + k * 32),
+                        umma_desc_sw128(ys + k * 32), idesc_shrink, (kc | k) != 0);
             umma_commit(smem_addr(&ctl.empty[st]));
           }
           umma_commit(smem_addr(&ctl.h_full));
+          // the first chunk overwrites those columns: wait until the epilogue
+          // has read h out of them (and written its split to shared memory)
+          if (!wait_f(ctl, ctl.hs_full, h_it & 1)) goto mma_done;
+          tc_fence_after();
         }
         for (int nc = 0; nc < p.nc_count; ++nc, ++acc_it) {
+          const int b = acc_it & 1;
+          const uint32_t d = tmem + acc_col(b);
           const int ncols = min(kNch, (p.n_out - nc * kNch + 15) / 16 * 16);
           const uint32_t idesc = umma_idesc_bf16(kTileMF, ncols);
-          if (!wait_f(ctl, ctl.acc_empty, (acc_it & 1) ^ 1)) goto mma_done;
-          tc_fence_after();
+          if (!(mt.lora && nc == 0)) {  // (the lora tile's first buffer was waited for above)
+            if (!wait_f(ctl, ctl.acc_empty[b], ((acc_it >> 1) & 1) ^ 1)) goto mma_done;
+            tc_fence_after();
+          }
           for (int kc = 0; kc < p.kc_count; ++kc, ++it) {  // ACC = X W_e^T
             const int st = it % p.nst;
             if (!wait_f(ctl, ctl.full[st], (it / p.nst) & 1)) goto mma_done;
@@ -250,34 +281,29 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             const uint32_t xs = ring + st * p.stage_bytes, ys = xs + kXBytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              umma_bf16(tmem + kTmemAccF, umma_desc_sw128(xs + k * 32),
-                        umma_desc_sw128(ys + k * 32), idesc, (kc | k) != 0);
+              umma_bf16(d, umma_desc_sw128(xs + k * 32), umma_desc_sw128(ys + k * 32), idesc,
+                        (kc | k) != 0);
             umma_commit(smem_addr(&ctl.empty[st]));
           }
           if (mt.lora) {  // ACC += [H_hi | H_lo] [B_e | B_e]^T
-            if (nc == 0) {
-              if (!wait_f(ctl, ctl.hs_full, h_it & 1)) goto mma_done;
-              tc_fence_after();
-            }
             const int st = it % p.nst;
             if (!wait_f(ctl, ctl.full[st], (it / p.nst) & 1)) goto mma_done;
+            fence_proxy_async_smem();  // B_e came in by cp.async (generic proxy)
             tc_fence_after();
             const uint32_t ys = ring + st * p.stage_bytes + kXBytes;
 #pragma unroll
             for (int kk = 0; kk < RP; kk += 16) {
               const uint64_t bdesc = umma_desc_sw128(ys + kk * 2);
-              umma_bf16(tmem + kTmemAccF,
-                        umma_desc_sw128(h_base + (kk >> 6) * (kTileMF * 128) + (kk & 63) * 2),
+              umma_bf16(d, umma_desc_sw128(h_base + (kk >> 6) * (kTileMF * 128) + (kk & 63) * 2),
                         bdesc, idesc, true);
               const int kl = RP + kk;
-              umma_bf16(tmem + kTmemAccF,
-                        umma_desc_sw128(h_base + (kl >> 6) * (kTileMF * 128) + (kl & 63) * 2),
+              umma_bf16(d, umma_desc_sw128(h_base + (kl >> 6) * (kTileMF * 128) + (kl & 63) * 2),
                         bdesc, idesc, true);
             }
             umma_commit(smem_addr(&ctl.empty[st]));
             ++it;
           }
-          umma_commit(smem_addr(&ctl.acc_full));
+          umma_commit(smem_addr(&ctl.acc_full[b]));
         }
         if (mt.lora) {
           umma_commit(smem_addr(&ctl.hs_empty));
@@ -293,33 +319,19 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     // ================================================================ ring fill
     // The two warps split the Y rows (warp 1 the first half); lane c & 7 takes
     // 16-byte chunk c of a 128-byte row segment, four rows per instruction,
-    // so every copy instruction covers whole 128-byte segments.  A stage is
-    // signalled `lag` stages late (once the copies of the stages after it are
-    // issued), so lag + 1 stages are in flight.
+    // so every copy instruction covers whole 128-byte segments.  Every lane
+    // arrives on a stage's full barrier through cp.async.mbarrier.arrive, so
+    // the arrival lands when that lane's copies have; the TMA boxes complete
+    // on the same barrier by their bytes.  A stage is therefore ready as soon
+    // as its own data is, however far ahead the ring is filled.
     const int pw = warp - 1;
     const int c = lane & 7, rq = lane >> 3;
-    const uint64_t keep = l2_evict_last();    // W_e / A_e / B_e are re-read by the expert's tiles
-    const uint64_t once = l2_evict_first();   // each x row block is re-read only by this CTA
+    // x_rows of a tile are re-read for every output chunk (evict last); a W_e
+    // box is re-read only by the expert's other tiles, which run at the same
+    // time (evict normal); A_e / B_e are small and re-read (evict last).
+    const uint64_t keep = l2_evict_last();
+    const uint64_t wpol = l2_evict_normal_policy();
     uint32_t it = 0;
-    int q[kMaxStagesF] = {-1, -1, -1, -1};
-    int nq = 0;
-    auto signal_oldest = [&](bool all) {
-      while (nq > 0 && (all || nq > p.lag)) {
-        if (!all) {
-          switch (p.lag) {
-            case 1: cp_async_wait_group<1>(); break;
-            case 2: cp_async_wait_group<2>(); break;
-            default: cp_async_wait_group<3>(); break;
-          }
-        } else {
-          cp_async_wait_group<0>();
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(smem_addr(&ctl.full[q[0]]));
-        for (int i = 0; i + 1 < kMaxStagesF; ++i) q[i] = q[i + 1];
-        --nq;
-      }
-    };
     // Begin a stage: wait for it to be free; lane 0 of warp 1 issues the X box
     // and, for a GEMM stage (e >= 0), the W_e box of rows n0.. .
     auto begin = [&](int r0, int k0, bool with_x, int e, int n0) -> int {
@@ -329,16 +341,14 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         const uint32_t full = smem_addr(&ctl.full[st]);
         const uint32_t xs = ring + st * p.stage_bytes;
         mbar_expect_tx(full, e >= 0 ? kXBytes + kYBytes : kXBytes);
-        tma_load_2d_hint(xs, &tmap_x, k0, r0, full, once);
-        if (e >= 0) tma_load_3d_hint(xs + kXBytes, &tmap_w, k0, n0, e, full, keep);
+        tma_load_2d_hint(xs, &tmap_x, k0, r0, full, keep);
+        if (e >= 0) tma_load_3d_hint(xs + kXBytes, &tmap_w, k0, n0, e, full, wpol);
       }
       return st;
     };
     auto finish = [&](int st) {
-      cp_async_commit();
-      q[nq++] = st;
+      cp_async_arrive_noinc(smem_addr(&ctl.full[st]));
       ++it;
-      signal_oldest(false);
     };
     for (int t = 0; t < n_tiles; ++t) {
       const FTile mt = my_tiles[t];
@@ -390,8 +400,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       }
     }
   fill_done:
-    signal_oldest(true);
-    if (pw == 0 && lane == 0) {  // X boxes of stages issued but never consumed: let them land
+    cp_async_wait_group<0>();
+    if (pw == 0 && lane == 0) {  // TMA boxes of stages issued but never consumed: let them land
       for (uint32_t k = 0; k < static_cast<uint32_t>(p.nst) && k < it; ++k) {
         const uint32_t j = it - 1 - k;
         mbar_wait_bounded(smem_addr(&ctl.full[j % p.nst]), (j / p.nst) & 1);
@@ -438,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
 #pragma unroll
           for (int qq = 0; qq < RP / 16; ++qq) {
             float v[16];
-            tmem_ld16(lane_addr + kTmemHF + qq * 16, v);
+            tmem_ld16(lane_addr + acc_col(acc_it & 1) + qq * 16, v);
 #pragma unroll
             for (int i = 0; i < 16; ++i) h[qq * 16 + i] = v[i];
           }
@@ -472,7 +482,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       }
       // ---- output chunks: accumulator -> registers -> one rounding -> global
       for (int nc = 0; nc < p.nc_count; ++nc, ++acc_it) {
-        if (!wait_f(ctl, ctl.acc_full, acc_it & 1)) goto epi_done;
+        const int b = acc_it & 1;
+        if (!wait_f(ctl, ctl.acc_full[b], (acc_it >> 1) & 1)) goto epi_done;
         tc_fence_after();
         const int col0 = nc * kNch + sub * 128;
         uint32_t packed[64];
@@ -483,7 +494,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
               float u[16];
-              tmem_ld16(lane_addr + kTmemAccF + sub * 128 + half * 64 + qq * 16, u);
+              tmem_ld16(lane_addr + acc_col(b) + sub * 128 + half * 64 + qq * 16, u);
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[qq * 16 + i] = u[i];
             }
@@ -494,7 +505,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&ctl.acc_empty));
+        if (lane == 0) mbar_arrive(smem_addr(&ctl.acc_empty[b]));
         if (valid && col0 < p.n_out) {
           uint8_t *orow = p.out + (static_cast<size_t>(rg) * p.n_out + col0) * 2;
 #pragma unroll
@@ -542,7 +553,6 @@ uint32_t rup_f(uint32_t v, uint32_t m) { return (v + m - 1) / m * m; }
 
 uint32_t plan_f(FusedParams &p, int nst) {
   p.nst = nst;
-  p.lag = nst - 1;
   p.stage_bytes = kXBytes + kYBytes;
   uint32_t off = 0;
   p.off_ring = off;

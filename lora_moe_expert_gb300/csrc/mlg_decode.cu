@@ -596,6 +596,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     int idx_s[kScanPer] = {}, ra_s[kScanPer] = {};
     const bool snap = spec && p.n_slots <= kScanChunk;
     if (snap) scan_load(p, 0, idx_s, ra_s);
+    // An owner knows its expert without the routing: its table entry and pair
+    // are requested while the routing loads are in flight.
+    if (!helper) pair = request_pair(e);
     if (spec) {
       total = scan_expert_rows(p, helper ? -1 : spec_target(e), 0, kSpecRows, s_spec, s_cnt, idx_s,
                                ra_s, snap, s_hist);
@@ -616,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       __syncthreads();
       spec_role = s_role;
     }
-    if (e >= 0) pair = request_pair(e);
+    if (helper && e >= 0) pair = request_pair(e);
     // Rows of a split expert: the owner folds ranks [0, half), the helper
     // [half, total), half = ceil(total / 2); passes of up to 8 rows each.
     const bool spec_split = helper || spec_role == 1;

@@ -30,8 +30,9 @@
 //  * warps 4-11 split h (scaled, zero for rows that do not fold) into shared
 //    memory, and per output chunk read their 32 rows x 128 columns of the
 //    accumulator, release it, round once to bf16 and store the rows of the
-//    tile straight from registers (16-byte stores; rows past the tile and
-//    columns past n_out are never written).
+//    tile straight from registers (32-byte stores, whole sectors, when the
+//    rows are 32-byte aligned, else 16-byte; rows past the tile and columns
+//    past n_out are never written).
 // Every wait is bounded; a timeout sets an error bit and the CTA drains its
 // copies and exits instead of hanging.
 #include <cuda.h>
@@ -74,6 +75,7 @@ struct FusedParams {
   int32_t r_pad, k_exp;          // rank rounded up to 16; expand K of [hi | lo], padded to 64
   int32_t kc_count, nc_count;    // 64-wide k chunks, 256-column output chunks
   int32_t nst;                   // ring stages
+  int32_t v8;                    // 1: output rows 32-byte aligned (32-byte stores)
   uint32_t stage_bytes;
   uint32_t off_ring, off_h, off_tab, off_my, smem_bytes;
 };
@@ -131,10 +133,15 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
   return pol;
 }
 
-__device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
-               "r"(d)
+__device__ __forceinline__ void st_global_v4(void *p, const uint32_t *v) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+// One whole 32-byte sector (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
 
@@ -508,11 +515,15 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         if (lane == 0) mbar_arrive(smem_addr(&ctl.acc_empty[b]));
         if (valid && col0 < p.n_out) {
           uint8_t *orow = p.out + (static_cast<size_t>(rg) * p.n_out + col0) * 2;
+          if (p.v8) {  // whole sectors: each store is a full 32-byte sector of the row
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc)
-            if (col0 + 8 * cc < p.n_out)
-              st_global_v4(orow + cc * 16, packed[4 * cc], packed[4 * cc + 1], packed[4 * cc + 2],
-                           packed[4 * cc + 3]);
+            for (int cc = 0; cc < 8; ++cc)
+              if (col0 + 16 * cc < p.n_out) st_global_v8(orow + cc * 32, packed + 8 * cc);
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc)
+              if (col0 + 8 * cc < p.n_out) st_global_v4(orow + cc * 16, packed + 4 * cc);
+          }
         }
       }
     }
@@ -621,6 +632,7 @@ extern "C" mlg_status mlg_grouped_gemm_fold_xrows(
   p.k_exp = static_cast<int32_t>(rup_f(2 * p.r_pad, 64));
   p.kc_count = (k_in + 63) / 64;
   p.nc_count = (n_out + kNch - 1) / kNch;
+  p.v8 = (n_out % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 31u) == 0) ? 1 : 0;
   uint32_t total = plan_f(p, 4);
   if (total > kSmemLimitF) total = plan_f(p, 3);
   if (total > kSmemLimitF) total = plan_f(p, 2);

@@ -633,10 +633,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       prefetch_l2(p.base_out + static_cast<size_t>(row) * p.n_out, static_cast<uint32_t>(p.n_out) * 2u);
     }
     for (int i = tid; i < kMaxCtas; i += kThreads) s_hist[i] = 0;
-    // The pair lands while the preceding kernel runs; B_e into its bank-spread
-    // row slots.
-    if (pair) {  // one thread polls, pausing; the others sleep in the barrier
-      const bool t = tid == 0 && !mbar_wait_bounded_sleep(bar_w, ph_w, 128);
+    __syncthreads();
+    griddep_wait();  // routing, x and base_out may be written by the preceding kernel
+
+    // ---- after the wait: the speculative first pass's x and base_out rows, the
+    // fresh scan's loads and its base_out loads are all in flight together,
+    // and only then is the pair (requested at the start) waited for, so that
+    // none of these round trips queues behind it when nothing ran before.
+    if (n_spec > 0) request_x(p, warp, lane, n_spec, row_bytes_x, bad, s_spec + spec_g0, sX, bar_x);
+    int idx0[kScanPer], ra0[kScanPer];
+    scan_load(p, 0, idx0, ra0);
+    if (n_spec > 0)
+      request_base(p, warp, g, c, n_spec, s_spec + spec_g0, base_v, my_row, 0, p.n_out);
+    if (pair) {  // B_e into its bank-spread row slots once the pair has landed
+      const bool t = tid == 0 && !mbar_wait_bounded(bar_w, ph_w);
       ph_w ^= 1u;
       have_pair = true;
       if (__syncthreads_or(t)) {
@@ -646,16 +656,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
         permute_b<RP>(smem + p.off_b, n_cols());
       }
     }
-    __syncthreads();
-    griddep_wait();  // routing, x and base_out may be written by the preceding kernel
-
-    // ---- after the wait: the speculative first pass's x and base_out rows, the
-    // fresh scan's loads and its base_out loads are all in flight together.
-    if (n_spec > 0) request_x(p, warp, lane, n_spec, row_bytes_x, bad, s_spec + spec_g0, sX, bar_x);
-    int idx0[kScanPer], ra0[kScanPer];
-    scan_load(p, 0, idx0, ra0);
-    if (n_spec > 0)
-      request_base(p, warp, g, c, n_spec, s_spec + spec_g0, base_v, my_row, 0, p.n_out);
     // The speculative first pass's h, while the fresh routing loads are in
     // flight: its x rows land and are shrunk before the scan is read, and the
     // h is kept only if the scan confirms the rows (h_ready below).

@@ -525,15 +525,26 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
           const int row = (2 * i2) / RP, j = (2 * i2) % RP;
           float h0 = 0.f, h1 = 0.f;
           if (cs > 1) {
-            for (uint32_t rk = 0; rk < cs; ++rk) {  // fixed rank order
-              const uint32_t a = map_to_rank(local + (row * HS + j) * 4, rk);
-              float v0, v1;
-              asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
-                           : "=f"(v0), "=f"(v1)
-                           : "r"(a)
-                           : "memory");
-              h0 += v0;
-              h1 += v1;
+            // Every rank's partial is requested before any is added, so the
+            // remote round trips overlap; the sum is then taken in rank order.
+            float v0[8], v1[8];
+#pragma unroll
+            for (uint32_t rk = 0; rk < 8; ++rk) {
+              v0[rk] = v1[rk] = 0.f;
+              if (rk < cs) {
+                const uint32_t a = map_to_rank(local + (row * HS + j) * 4, rk);
+                asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                             : "=f"(v0[rk]), "=f"(v1[rk])
+                             : "r"(a)
+                             : "memory");
+              }
+            }
+#pragma unroll
+            for (uint32_t rk = 0; rk < 8; ++rk) {
+              if (rk < cs) {
+                h0 += v0[rk];
+                h1 += v1[rk];
+              }
             }
           } else {
             h0 = sHloc[row * HS + j];

@@ -359,6 +359,56 @@ def test_fold_validation_on_host(L):
     assert router(n_out=4) == mlg.MLG_ERR_UNSUPPORTED
     assert router(n_tokens=0) == mlg.MLG_OK
 
+    def gemm_fold(**kw):
+        args = {**ok, "expert_offsets": p, "src": p, "w": p, "row_offset": 0, "row_end": 100,
+                "cap": 32, **kw}
+        return L.mlg_grouped_gemm_fold_xrows(
+            args["x"], args["expert_offsets"], args["src"], args["row_adapter"], args["w"],
+            args["a_table"], args["b_table"], args["scale_table"], args["base_out"],
+            args["k_in"], args["max_rank"], args["n_out"], args["top_k"], args["n_experts"],
+            args["row_offset"], args["row_end"], args["cap"], 0)
+
+    assert gemm_fold(cap=0) == mlg.MLG_ERR_CAP_ZERO
+    assert gemm_fold(row_offset=7, row_end=6) == mlg.MLG_ERR_INVALID_ARG
+    assert gemm_fold(row_offset=-2) == mlg.MLG_ERR_INVALID_ARG
+    assert gemm_fold(top_k=0) == mlg.MLG_ERR_INVALID_ARG
+    assert gemm_fold(n_experts=-1) == mlg.MLG_ERR_INVALID_ARG
+    for name in ("x", "expert_offsets", "src", "w", "a_table", "b_table", "scale_table",
+                 "base_out"):
+        assert gemm_fold(**{name: None}) == mlg.MLG_ERR_INVALID_ARG, name
+    assert gemm_fold(x=p + 4) == mlg.MLG_ERR_UNSUPPORTED
+    assert gemm_fold(w=p + 8) == mlg.MLG_ERR_UNSUPPORTED
+    assert gemm_fold(base_out=p + 2) == mlg.MLG_ERR_UNSUPPORTED
+    assert gemm_fold(k_in=12) == mlg.MLG_ERR_UNSUPPORTED
+    assert gemm_fold(n_out=12) == mlg.MLG_ERR_UNSUPPORTED
+    assert gemm_fold(max_rank=72) == mlg.MLG_ERR_UNSUPPORTED
+    assert gemm_fold(row_offset=40, row_end=40) == mlg.MLG_OK  # empty range: nothing launched
+    assert gemm_fold(n_experts=0) == mlg.MLG_OK
+    assert gemm_fold(row_adapter=None, row_offset=3, row_end=3) == mlg.MLG_OK  # the map is optional
+
+    def gather_ex(flags, multi_form=False, **kw):
+        args = {**ok, **kw}
+        if multi_form:
+            return L.mlg_gather_bgmv_multi_ex(
+                args["x"], args["indices"], args["row_adapter"], args["a_table"], args["b_table"],
+                args["scale_table"], args["base_out"], args["n_slots"], args["k_in"],
+                args["max_rank"], args["n_out"], args["top_k"], args["n_experts"], 2, flags, 0)
+        return L.mlg_gather_bgmv_ex(args["x"], args["indices"], args["row_adapter"],
+                                    args["a_table"], args["b_table"], args["scale_table"],
+                                    args["base_out"], args["n_slots"], args["k_in"],
+                                    args["max_rank"], args["n_out"], args["top_k"],
+                                    args["n_experts"], flags, 0)
+
+    for multi_form in (False, True):
+        # unknown flags are rejected before anything else; known ones pass validation
+        assert gather_ex(2, multi_form) == mlg.MLG_ERR_INVALID_ARG
+        assert gather_ex(0x80000000, multi_form) == mlg.MLG_ERR_INVALID_ARG
+        assert gather_ex(2, multi_form, n_slots=0) == mlg.MLG_ERR_INVALID_ARG
+        assert gather_ex(mlg.MLG_FOLD_AFTER_PRECEDING, multi_form, n_slots=0) == mlg.MLG_OK
+        assert gather_ex(0, multi_form, top_k=0) == mlg.MLG_ERR_INVALID_ARG
+        assert gather_ex(mlg.MLG_FOLD_AFTER_PRECEDING, multi_form, x=p + 8) == \
+            mlg.MLG_ERR_UNSUPPORTED
+
 
 def test_status_strings_and_tuning(L):
     for st in range(-7, 1):

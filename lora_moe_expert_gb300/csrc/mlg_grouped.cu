@@ -111,13 +111,12 @@ __device__ __forceinline__ bool wait_bar(Ctl &ctl, uint64_t &bar, uint32_t parit
   }
 }
 
-// Per-CTA tile list entry, built once in the prologue: expert, rows, scale.
+// Per-CTA tile list entry, built once in the prologue: expert and rows.
 // Which rows fold is decided where it is needed: the X producers gather every
 // row of the tile (no round trip on the row map before the first copy), and
 // each epilogue lane reads its own rows' row-map entries once, up front.
 struct MyTile {
   int e, r0, r1;
-  float scale;
 };
 
 
@@ -224,7 +223,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (tid == 0) tile_start[n_e] = carry;
   }
   __syncthreads();
-  // This CTA's tiles (t = blockIdx.x + i * gridDim.x): expert, rows, scale.
+  // This CTA's tiles (t = blockIdx.x + i * gridDim.x): expert and rows.  (The
+  // scale is read by the epilogue, which needs it only for the first h split,
+  // so its round trip is not on the prologue's path.)
   MyTile *my_tiles = reinterpret_cast<MyTile *>(smem + p.off_my);
   const int n_tiles_all = tile_start[n_e];
   int my_count = 0;
@@ -236,7 +237,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
     my_tiles[tid].e = ti.e;
     my_tiles[tid].r0 = ti.r0;
     my_tiles[tid].r1 = ti.r1;
-    my_tiles[tid].scale = __ldg(p.scale_table + ti.e);
   }
   tc_fence_before();
   __syncthreads();
@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const int row = quarter * kBoxRows + lane;
       const int rg = ti.r0 + row;
       const bool folds = (fold_bits >> t) & 1u;
-      const float scale = ti.scale;
+      const float scale = __ldg(p.scale_table + ti.e);
       const int owned = min(max(ti.r1 - (ti.r0 + quarter * kBoxRows), 0), kBoxRows);
 
       // ---- h: tensor memory -> scaled, split into bf16 hi / lo -> shared memory

@@ -29,10 +29,11 @@
 //  * warps 1-2 fill the ring (warp 1 lane 0 issues the TMA boxes);
 //  * warps 4-11 split h (scaled, zero for rows that do not fold) into shared
 //    memory, and per output chunk read their 32 rows x 128 columns of the
-//    accumulator, release it, round once to bf16 and store the rows of the
-//    tile straight from registers (32-byte stores, whole sectors, when the
-//    rows are 32-byte aligned, else 16-byte; rows past the tile and columns
-//    past n_out are never written).
+//    accumulator, release it, round once to bf16 and store: a warp whose 32
+//    rows all belong to the tile writes 32 x 32 boxes into shared memory and
+//    TMA-stores them; a partial box is stored row by row from registers
+//    (32-byte stores when rows are 32-byte aligned); rows past the tile and
+//    columns past n_out are never written.
 // Every wait is bounded; a timeout sets an error bit and the CTA drains its
 // copies and exits instead of hanging.
 #include <cuda.h>
@@ -76,9 +77,12 @@ struct FusedParams {
   int32_t kc_count, nc_count;    // 64-wide k chunks, 256-column output chunks
   int32_t nst;                   // ring stages
   int32_t v8;                    // 1: output rows 32-byte aligned (32-byte stores)
+  int32_t staged;                // 1: whole 32-row boxes stored through shared memory by TMA
   uint32_t stage_bytes;
-  uint32_t off_ring, off_h, off_tab, off_my, smem_bytes;
+  uint32_t off_ring, off_h, off_stage, off_tab, off_my, smem_bytes;
 };
+
+constexpr uint32_t kStageBox = 32 * 64;  // one 32-row x 32-column bf16 output box (64B swizzle)
 
 struct FCtl {
   uint64_t full[kMaxStagesF], empty[kMaxStagesF];
@@ -149,7 +153,8 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v) {
 template <int RP>
 __global__ void __launch_bounds__(kThreadsF, 1)
     gemm_fold_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                     const __grid_constant__ CUtensorMap tmap_w, const FusedParams p) {
+                     const __grid_constant__ CUtensorMap tmap_w,
+                     const __grid_constant__ CUtensorMap tmap_out, const FusedParams p) {
   constexpr int KEXP = (2 * RP + 63) / 64 * 64;  // expand K: [hi | lo | zero pad]
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ FCtl ctl;
@@ -177,6 +182,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     fence_mbar_init();
     prefetch_tmap(&tmap_x);
     prefetch_tmap(&tmap_w);
+    if (p.staged) prefetch_tmap(&tmap_out);
   }
   __syncthreads();
   if (warp == 0) {
@@ -513,7 +519,31 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&ctl.acc_empty[b]));
-        if (valid && col0 < p.n_out) {
+        // A warp whose 32 rows all belong to the tile stores its boxes through
+        // shared memory (TMA clips columns past n_out); a partial box is stored
+        // row by row, so no row of another tile is written.
+        const bool whole = p.staged && mt.r0 + quarter * 32 + 32 <= mt.r1;
+        if (whole && col0 < p.n_out) {
+          uint8_t *stage = smem + p.off_stage + ew * kStageBox;
+          const uint32_t stage_addr = smem_addr(stage);
+#pragma unroll
+          for (int bx = 0; bx < 4; ++bx) {  // 32-column boxes of this warp's 128 columns
+            if (col0 + bx * 32 >= p.n_out) break;
+            if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
+            __syncwarp();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)  // 16-byte chunk cc of this lane's row, 64B swizzle
+              *reinterpret_cast<uint4 *>(stage + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(packed[bx * 16 + 4 * cc], packed[bx * 16 + 4 * cc + 1],
+                             packed[bx * 16 + 4 * cc + 2], packed[bx * 16 + 4 * cc + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_out, col0 + bx * 32, mt.r0 + quarter * 32, stage_addr);
+              bulk_commit();
+            }
+          }
+        } else if (valid && col0 < p.n_out) {
           uint8_t *orow = p.out + (static_cast<size_t>(rg) * p.n_out + col0) * 2;
           if (p.v8) {  // whole sectors: each store is a full 32-byte sector of the row
 #pragma unroll
@@ -528,6 +558,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       }
     }
   epi_done:
+    if (lane == 0) bulk_wait_all();  // this warp's output boxes have been written
     __syncwarp();
   }
   tc_fence_before();
@@ -558,18 +589,21 @@ EncodeTiledFnF encode_fn_f() {
   return fn;
 }
 
-constexpr uint32_t kSmemLimitF = 227 * 1024 - 2048;
+constexpr uint32_t kSmemLimitF = 227 * 1024 - 1024;  // less the kernel's static part
 
 uint32_t rup_f(uint32_t v, uint32_t m) { return (v + m - 1) / m * m; }
 
-uint32_t plan_f(FusedParams &p, int nst) {
+uint32_t plan_f(FusedParams &p, int nst, bool staged) {
   p.nst = nst;
+  p.staged = staged ? 1 : 0;
   p.stage_bytes = kXBytes + kYBytes;
   uint32_t off = 0;
   p.off_ring = off;
   off += nst * p.stage_bytes;
   p.off_h = off;
   off += kTileMF * p.k_exp * 2;
+  p.off_stage = off;  // 1024-aligned (the ring and h are multiples of 1 KB)
+  off += staged ? kEpiWarpsF * kStageBox : 0;
   p.off_tab = off;
   off += rup_f((p.n_experts + 1) * 4, 16);
   p.off_my = off;
@@ -633,10 +667,15 @@ extern "C" mlg_status mlg_grouped_gemm_fold_xrows(
   p.kc_count = (k_in + 63) / 64;
   p.nc_count = (n_out + kNch - 1) / kNch;
   p.v8 = (n_out % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 31u) == 0) ? 1 : 0;
-  uint32_t total = plan_f(p, 4);
-  if (total > kSmemLimitF) total = plan_f(p, 3);
-  if (total > kSmemLimitF) total = plan_f(p, 2);
-  if (total > kSmemLimitF) return MLG_ERR_UNSUPPORTED;
+  // Deepest ring first, output staging when it fits beside it.
+  static const int kPlans[][2] = {{4, 1}, {4, 0}, {3, 1}, {3, 0}, {2, 0}};
+  uint32_t total = 0;
+  bool fits = false;
+  for (const auto &pl : kPlans) {
+    total = plan_f(p, pl[0], pl[1] != 0);
+    if ((fits = total <= kSmemLimitF)) break;
+  }
+  if (!fits) return MLG_ERR_UNSUPPORTED;
 
   EncodeTiledFnF enc = encode_fn_f();
   if (enc == nullptr) return MLG_ERR_CUDA;
@@ -660,6 +699,16 @@ extern "C" mlg_status mlg_grouped_gemm_fold_xrows(
   const cuuint32_t estr3[3] = {1, 1, 1};
   if (enc(&tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<mlg_bf16 *>(w_experts), wdims,
           wstrides, wbox, estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MLG_ERR_CUDA;
+
+  // out: [row_end, n_out], 32 x 32 boxes, 64-byte swizzle (the staging layout)
+  CUtensorMap tmap_out;
+  const cuuint64_t odims[2] = {static_cast<cuuint64_t>(n_out), static_cast<cuuint64_t>(row_end)};
+  const cuuint64_t ostrides[1] = {static_cast<cuuint64_t>(n_out) * 2};
+  const cuuint32_t obox[2] = {32, 32};
+  if (enc(&tmap_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, odims, ostrides, obox, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return MLG_ERR_CUDA;
 
@@ -702,7 +751,7 @@ extern "C" mlg_status mlg_grouped_gemm_fold_xrows(
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  using KernelFn = void (*)(CUtensorMap, CUtensorMap, FusedParams);
+  using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, FusedParams);
   KernelFn fn;
   switch (p.r_pad) {
     case 16: fn = gemm_fold_kernel<16>; break;
@@ -710,7 +759,7 @@ extern "C" mlg_status mlg_grouped_gemm_fold_xrows(
     case 48: fn = gemm_fold_kernel<48>; break;
     default: fn = gemm_fold_kernel<64>; break;
   }
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, fn, tmap_x, tmap_w, p);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, fn, tmap_x, tmap_w, tmap_out, p);
   if (err != cudaSuccess) return cuda_status(err);
   return cuda_status(cudaGetLastError());
 }

@@ -22,7 +22,9 @@
 //    a double-buffered TMEM accumulator -- h is split into two bf16 halves so
 //    it enters the expand at ~2^-17 relative precision (kept fp32 in effect);
 //  * warps 1 and 3 gather the X rows via src and A_e chunks, warp 2 the B_e
-//    chunks, with 16-byte cp.async into 128-byte-swizzled K-major tiles; when
+//    chunks, with 16-byte cp.async into swizzled K-major tiles (X and A_e in
+//    128-byte rows; B_e in rows of 2 * rank bytes, 32- or 64-byte swizzle for
+//    rank 16 / 32, so a B_e stage takes a quarter / half the space); when
 //    a tile's x rows are rows r0.. of x (router, per-row x) they come in as
 //    64 x 64 TMA boxes instead;
 //  * warps 4-11 (two per TMEM lane quarter) scale and split h, then stream
@@ -294,7 +296,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           for (int kk = 0; kk < RP; kk += 16) {
             // hi half: H columns [0, RP); lo half: H columns [RP, 2 RP); both
             // against B_e's rank columns kk .. kk+15.
-            const uint64_t bdesc = umma_desc_sw128(bs + kk * 2);
+            const uint64_t bdesc = umma_desc_k<b_row_bytes(RP)>(bs + kk * 2);
             umma_bf16(d, umma_desc_sw128(h_base + (kk >> 6) * (kTileM * 128) + (kk & 63) * 2),
                       bdesc, idesc_expand, kk != 0);
             const int kl = RP + kk;
@@ -450,7 +452,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             const int n = n0 + i;
             const bool in = n < p.n_out;
             const uint8_t *brow = B + static_cast<size_t>(in ? n : 0) * p.rank * 2;
-            cp_async_16_hint(bs + sw128(i, c), brow + c * 16, in ? 16u : 0u, keep);
+            cp_async_16_hint(bs + swk<b_row_bytes(RP)>(i, c), brow + c * 16, in ? 16u : 0u,
+                             keep);
           }
         }
         cp_async_commit();
@@ -691,7 +694,8 @@ uint32_t plan(GroupedParams &p, int n_ch, int nxa, int nbs, int depth, int n_e) 
   p.depth = depth;
   p.nc_count = (p.n_out + n_ch - 1) / n_ch;
   p.xa_stage = rup(kTileM * 128 + p.r_pad * 128, 1024);
-  p.b_stage = rup(static_cast<uint32_t>(n_ch * 128), 1024);  // K = rank, padded to 64
+  // K = rank, in rows of b_row_bytes (32, 64 or 128 bytes)
+  p.b_stage = rup(static_cast<uint32_t>(n_ch * b_row_bytes(p.r_pad)), 1024);
   uint32_t off = 0;
   p.off_xa = off;
   off += nxa * p.xa_stage;
@@ -718,10 +722,15 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
   p.kc_count = (p.k_in + 63) / 64;
   p.nbx = (p.n_out + kBoxCols - 1) / kBoxCols;
   // Deepest rings that fit.  Rows whose x is wider than their base_out
-  // read-modify-write (router-like shapes) favour the X/A ring; the rest favour
-  // the base_out ring (HBM latency), then B_e stages (L2 latency).
-  static const int cand_base[][3] = {{2, 2, 4}, {3, 2, 4}, {3, 3, 3}, {2, 3, 3}, {2, 2, 3},
-                                     {2, 2, 2}};
+  // read-modify-write (router-like shapes) favour the X/A ring; the rest take
+  // four B_e stages (a tile's expand needs a fresh B_e chunk per accumulator
+  // chunk; with two stages that stream set the pace of the 163840-row
+  // prefill) beside a base_out ring four boxes deep per warp, which the
+  // compact B_e rows (b_row_bytes) leave room for: 305 us with {2, 2, 4},
+  // 274 us with {2, 4, 3}, 258 us with {2, 4, 4}; a ring two deep measured
+  // far slower (350 us).
+  static const int cand_base[][3] = {{2, 4, 4}, {2, 4, 3}, {2, 2, 4}, {3, 3, 3}, {2, 3, 3},
+                                     {2, 2, 3}, {2, 2, 2}};
   static const int cand_x[][3] = {{6, 2, 2}, {5, 2, 3}, {5, 2, 2}, {4, 2, 3}, {4, 2, 2},
                                   {3, 2, 2}, {2, 2, 2}};
   const bool x_heavy = static_cast<int64_t>(p.k_in) * 2 > static_cast<int64_t>(p.n_out) * 4;
@@ -730,7 +739,7 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
   const int n_chs[2] = {128, 64};
   for (int a = 0; a < 2 && !ok; ++a) {
     const int(*cand)[3] = x_heavy ? cand_x : cand_base;
-    const int nc = x_heavy ? 7 : 6;
+    const int nc = 7;
     for (int i = 0; i < nc; ++i) {
       total = plan(p, n_chs[a], cand[i][0], cand[i][1], cand[i][2], n_e);
       if ((ok = total <= kGSmemLimit)) break;

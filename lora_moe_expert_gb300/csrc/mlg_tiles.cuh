@@ -18,6 +18,35 @@ __device__ __forceinline__ uint32_t sw128(int row, int c) {
   return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4));
 }
 
+// The same for K-major tiles of RB-byte rows (RB = 32, 64 or 128) in the
+// matching 32-, 64- or 128-byte swizzle: 8-row atoms of 8 * RB bytes, the
+// 16-byte chunk index XORed with the address bits [7, ..) the swizzle mixes in.
+template <int RB>
+__device__ __forceinline__ uint32_t swk(int row, int c) {
+  static_assert(RB == 32 || RB == 64 || RB == 128, "row bytes");
+  const int x = RB == 128 ? (row & 7) : RB == 64 ? ((row >> 1) & 3) : ((row >> 2) & 1);
+  return static_cast<uint32_t>((row >> 3) * (8 * RB) + (row & 7) * RB + ((c ^ x) << 4));
+}
+
+// tcgen05 shared-memory matrix descriptor of such a tile (K-major, version 1,
+// start address in 16-byte units, SBO = one 8-row atom, layout code of the
+// swizzle: 2 = 128-byte, 4 = 64-byte, 6 = 32-byte).
+template <int RB>
+__device__ __forceinline__ uint64_t umma_desc_k(uint32_t smem_byte_addr) {
+  constexpr uint64_t kLayout = RB == 128 ? 2u : RB == 64 ? 4u : 6u;
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_byte_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;                  // LBO (unused for swizzled K-major)
+  d |= static_cast<uint64_t>((8u * RB) >> 4) << 32;      // SBO: 8 rows
+  d |= static_cast<uint64_t>(1u) << 46;                  // descriptor version
+  d |= kLayout << 61;
+  return d;
+}
+
+// Bytes per B_e row in the grouped kernels' expand tiles: the rank columns in
+// the narrowest swizzle that holds them (a rank of 48 takes 128-byte rows).
+__host__ __device__ constexpr int b_row_bytes(int rp) { return rp <= 16 ? 32 : rp <= 32 ? 64 : 128; }
+
 struct TileInfo {
   int e, r0, r1;
 };

@@ -32,7 +32,9 @@
 //    rows so that every lane ends with 8 adjacent output columns of two rows:
 //    base_out is read (into registers, right after the wait) and written with
 //    16-byte accesses, rounded once: RNE(base + scale * delta).  B_e sits in
-//    shared memory with its rows XOR-permuted for conflict-free loads;
+//    shared memory with its rows XOR-permuted for conflict-free loads: every
+//    thread copies its 16-byte pieces of B_e (cp.async) straight into their
+//    rows' slots, so no permutation pass follows the copy;
 //  * an expert with more than 6 rows gets a helper CTA (the SMs left over by
 //    the experts): the owner folds the first half of its rows, the helper the
 //    second, both deciding the split from the same per-expert row counts
@@ -238,23 +240,6 @@ __device__ __forceinline__ int b_slot(int r) {
   return r ^ ((r >> 3) & (RPC - 1));
 }
 
-// Permute B_e (bulk-copied row-major into sB) into the slots of b_slot, in
-// place: each warp moves 256-byte spans, 8 bytes per lane.
-template <int RP>
-__device__ __forceinline__ void permute_b(uint8_t *sB, int n_out) {
-  constexpr int RB = 2 * RP;  // bytes per B_e row
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int spans = n_out * RB / 256;  // n_out % 8 == 0 and RB >= 32
-  for (int sp = warp; sp < spans; sp += kWarps) {
-    const int byte = sp * 256 + lane * 8;
-    const int r = byte / RB, off = byte % RB;
-    const uint2 v = *reinterpret_cast<const uint2 *>(sB + byte);
-    __syncwarp();
-    *reinterpret_cast<uint2 *>(sB + b_slot<RP>(r) * RB + off) = v;
-    __syncwarp();
-  }
-}
-
 // The expand of one 64-column block: swapped operands, M = 16 B_e rows, N =
 // the 8 rows of the pass, K = rank, h as hi + lo, four m-tiles t.  M-row g of
 // tile t takes B_e row blk*64 + 8g + 2t and M-row g+8 the next one, so lane
@@ -356,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
   for (int i = tid; i < kMaxCtas; i += kThreads) s_hist[i] = 0;
   const uint32_t bar_w = smem_addr(&bars[0]), bar_x = smem_addr(&bars[1]);
   if (tid == 0) {
-    mbar_init(bar_w, 1);
+    mbar_init(bar_w, 1 + kThreads);  // the A_e copies' expect_tx + every thread's B_e copies
     mbar_init(bar_x, 1);
     fence_mbar_init();
   }
@@ -396,19 +381,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     const uint64_t b_addr = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ex);
     scale = __ldg(p.scale_table + ex);
     if (a_addr == 0 || b_addr == 0 || ((a_addr | b_addr) & 15u) != 0) return false;
-    if (warp == 0 && !bad) {  // one copy per A_e row, one for the B_e rows
-      const uint32_t b_bytes = static_cast<uint32_t>(n_cols()) * RP * 2u;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar_w, RP * row_bytes_x + b_bytes);
-        bulk_g2s(smem_addr(sB),
-                 reinterpret_cast<const uint8_t *>(b_addr) + static_cast<size_t>(col0()) * RP * 2,
-                 b_bytes, bar_w);
+    if (!bad) {
+      if (warp == 0) {  // one bulk copy per A_e row
+        if (lane == 0) mbar_arrive_expect_tx(bar_w, RP * row_bytes_x);
+        __syncwarp();
+        const uint8_t *A = reinterpret_cast<const uint8_t *>(a_addr);
+        for (int j = lane; j < RP; j += 32)
+          bulk_g2s(smem_addr(sA + j * p.stride_a), A + static_cast<size_t>(j) * row_bytes_x,
+                   row_bytes_x, bar_w);
       }
-      __syncwarp();
-      const uint8_t *A = reinterpret_cast<const uint8_t *>(a_addr);
-      for (int j = lane; j < RP; j += 32)
-        bulk_g2s(smem_addr(sA + j * p.stride_a), A + static_cast<size_t>(j) * row_bytes_x,
-                 row_bytes_x, bar_w);
+      // The B_e rows of this unit's columns, each 16-byte piece straight into
+      // its row's bank-spread slot (no permutation pass after it lands); every
+      // thread's copies complete on bar_w through cp.async.mbarrier.arrive.
+      constexpr int RB = 2 * RP;  // bytes per B_e row
+      const uint8_t *B = reinterpret_cast<const uint8_t *>(b_addr) + static_cast<size_t>(col0()) * RB;
+      const int pieces = n_cols() * RB / 16;
+      uint8_t *sBw = smem + p.off_b;
+      for (int i = tid; i < pieces; i += kThreads) {
+        const int r = (i * 16) / RB, off = (i * 16) % RB;
+        cp_async_16(smem_addr(sBw + b_slot<RP>(r) * RB + off), B + i * 16, 16u);
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar_w) : "memory");
     }
     return true;
   };
@@ -489,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       }
       issued = false;
       timed_out = false;
-      if (!have_pair) {  // the pair lands; B_e into its bank-spread row slots
+      if (!have_pair) {  // the pair lands (B_e already in its bank-spread row slots)
         timed_out = tid == 0 && !mbar_wait_bounded(bar_w, ph_w);
         ph_w ^= 1u;
         have_pair = true;
@@ -498,13 +491,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
           bad = true;
           break;
         }
-        permute_b<RP>(smem + p.off_b, n_cols());
       }
       if (!h_ready) {
         // One thread polls; the barrier passes what it observed to the others.
         timed_out = tid == 0 && !mbar_wait_bounded(bar_x, ph_x);
         ph_x ^= 1u;
-        if (__syncthreads_or(timed_out)) {  // (also orders the permuted B_e before its reads)
+        if (__syncthreads_or(timed_out)) {  // (also orders the landed B_e before its reads)
           if (tid == 0) record_error(kErrWaitTimeout);
           bad = true;
           break;
@@ -645,15 +637,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
     scan_load(p, 0, idx0, ra0);
     if (n_spec > 0)
       request_base(p, warp, g, c, n_spec, s_spec + spec_g0, base_v, my_row, 0, p.n_out);
-    if (pair) {  // B_e into its bank-spread row slots once the pair has landed
+    if (pair) {  // the pair has landed (B_e straight into its bank-spread row slots)
       const bool t = tid == 0 && !mbar_wait_bounded(bar_w, ph_w);
       ph_w ^= 1u;
       have_pair = true;
       if (__syncthreads_or(t)) {
         if (tid == 0) record_error(kErrWaitTimeout);
         bad = true;
-      } else {
-        permute_b<RP>(smem + p.off_b, n_cols());
       }
     }
     // The speculative first pass's h, while the fresh routing loads are in
@@ -835,8 +825,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
         if (__syncthreads_or(t)) {
           if (tid == 0) record_error(kErrWaitTimeout);
           bad = true;
-        } else {
-          permute_b<RP>(smem + p.off_b, n_cols());
         }
       }
     }
@@ -862,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
       col0_v = half < 0 ? 0 : half * (p.n_out / 2);
       n_cols_v = half < 0 ? p.n_out : p.n_out / 2;
       if (u == 0 && spec_pair && e == e_spec && half < 0) {
-        pair = true;  // landed and permuted before the wait; scale set by its request
+        pair = true;  // landed before the wait; scale set by its request
         have_pair = true;
       } else {
         fence_proxy_async_smem();  // the last unit's buffers were read: order before new copies

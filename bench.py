@@ -26,7 +26,8 @@ roofline   algorithmic bytes of one launch / its median duration vs the
 decode     besides the chained steps (one fold after another, where a fold's
            early start overlaps its predecessor), each decode workload also
            reports an isolated fold (the GPU idle before it, nothing to
-           overlap) and a contended one (each fold right after an HBM-bound
+           overlap; isolated_floor_us is the same measurement around a trivial
+           kernel, the event and launch latency included in it) and a contended one (each fold right after an HBM-bound
            copy kernel moving the expert GEMM's bytes; the fold's incremental
            time over the copies alone).
 cpu_baseline / --impl reference
@@ -418,10 +419,11 @@ def capture(fn, stream):
     return g
 
 
-def time_isolated(probs, n, stream):
+def time_isolated(probs, n, stream, body=None):
     """Each fold alone: the GPU spins in a sleep kernel while the host enqueues
     an event, the fold and an event, so the fold starts on an idle stream with
-    nothing to overlap.  Milliseconds per fold, n samples over the sets."""
+    nothing to overlap.  Milliseconds per fold, n samples over the sets.  With
+    `body`, the same measurement of body(i) instead of a fold."""
     import torch
 
     ev = _events(n)
@@ -429,10 +431,22 @@ def time_isolated(probs, n, stream):
         for i, (e0, e1) in enumerate(ev):
             torch.cuda._sleep(1000000)  # ~0.5 ms: the host enqueues the fold meanwhile
             e0.record(stream)
-            probs[i % len(probs)].run(stream=stream)
+            if body is None:
+                probs[i % len(probs)].run(stream=stream)
+            else:
+                body(i)
             e1.record(stream)
     stream.synchronize()
     return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+
+def isolated_floor(stream, n=40):
+    """The same isolated measurement around a trivial kernel (an add on 16
+    floats): the event and launch latency any kernel timed this way pays."""
+    import torch
+
+    t = torch.zeros(16, device=stream.device)
+    return statistics.median(time_isolated(None, n, stream, body=lambda i: t.add_(1)))
 
 
 def expert_gemm_bytes(w):
@@ -509,6 +523,7 @@ def gpu_measure(name, steps, warmup, device, seed_base=1000, replays=REPLAYS, e2
         iso = time_isolated(probs, 40, stream)
         out["isolated_ms"] = statistics.median(iso)
         out["isolated_ms_min"] = min(iso)
+        out["isolated_floor_ms"] = isolated_floor(stream)
         cb = expert_gemm_bytes(w0)
         inc, copy_ms = time_contended(probs, min(steps, 20), stream, cb, max(3, replays // 2))
         out["contended_ms"] = inc
@@ -717,6 +732,7 @@ def summarize(name, r, peak, steps, cpu=None):
         iso, con = r["isolated_ms"], r["contended_ms"]
         out["isolated_us"] = iso * 1e3
         out["isolated_us_min"] = r["isolated_ms_min"] * 1e3
+        out["isolated_floor_us"] = r["isolated_floor_ms"] * 1e3
         out["isolated_frac_of_peak"] = r["alg_bytes"] / (iso * 1e-3) / 1e9 / peak
         out["contended_us"] = con * 1e3
         out["contended_frac_of_peak"] = (r["alg_bytes"] / (con * 1e-3) / 1e9 / peak

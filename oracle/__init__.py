@@ -111,6 +111,8 @@ class Oracle:
         L.oracle_grouped_fold_rows.restype = _i32
         L.oracle_grouped_gemm_fold_xrows.argtypes = [_p] * 12 + [_i64] + [_i32] * 7
         L.oracle_grouped_gemm_fold_xrows.restype = _i32
+        L.oracle_grouped_gemm_fold_xrows_rows.argtypes = [_p] * 10 + [_i32, _p, _p, _p] + [_i32] * 7
+        L.oracle_grouped_gemm_fold_xrows_rows.restype = _i32
 
     def set_threads(self, n: int) -> int:
         """Threads of the row loops (n < 1: every core); returns the count in force
@@ -292,6 +294,30 @@ class Oracle:
             _ptr(x), _ptr(off), _ptr(src), _ptr(ra), _ptr(wt), _ptr(at), _ptr(bt), _ptr(st_),
             _ptr(out_in), _ptr(ref), _ptr(written), _ptr(folded), total, k_in, max_rank, n_out,
             top_k, at.size, row_offset, row_end)
+        assert st == OK, st
+        return ref, written.astype(bool), folded.astype(bool)
+
+    def grouped_gemm_fold_xrows_rows(self, x_rows, expert_offsets, src, row_adapter, w_table,
+                                     a_table, b_table, scale_table, prior_rows, rows, k_in,
+                                     max_rank, n_out, top_k, row_offset, row_end):
+        """The listed sorted rows of the expert GEMM with the fold; prior_rows
+        [len(rows), n_out] are their values before the call.  Returns (ref,
+        written, folded) for those rows."""
+        x, prior = self._u16(x_rows), self._u16(prior_rows)
+        off = np.ascontiguousarray(expert_offsets, np.int32)
+        src = np.ascontiguousarray(src, np.int32)
+        ra = None if row_adapter is None else np.ascontiguousarray(row_adapter, np.int32)
+        wt = np.ascontiguousarray(w_table, np.uint64)
+        at, bt = np.ascontiguousarray(a_table, np.uint64), np.ascontiguousarray(b_table, np.uint64)
+        st_ = np.ascontiguousarray(scale_table, np.float32)
+        rows = np.ascontiguousarray(rows, np.int32)
+        ref = np.empty((rows.size, n_out), np.float64)
+        written = np.empty(rows.size, np.uint8)
+        folded = np.empty(rows.size, np.uint8)
+        st = self.lib.oracle_grouped_gemm_fold_xrows_rows(
+            _ptr(x), _ptr(off), _ptr(src), _ptr(ra), _ptr(wt), _ptr(at), _ptr(bt), _ptr(st_),
+            _ptr(prior), _ptr(rows), rows.size, _ptr(ref), _ptr(written), _ptr(folded), k_in,
+            max_rank, n_out, top_k, at.size, row_offset, row_end)
         assert st == OK, st
         return ref, written.astype(bool), folded.astype(bool)
 

@@ -589,3 +589,65 @@ int32_t oracle_grouped_gemm_fold_xrows(const uint16_t *x_rows, const int32_t *ex
     }
     return OR_OK;
 }
+
+/* Sampled variant of the expert GEMM with the fold: the listed sorted rows
+ * only (one ref row per entry; `prior_rows` holds their prior values, which a
+ * row that is not an output keeps), each computed exactly as in
+ * oracle_grouped_gemm_fold_xrows. */
+int32_t oracle_grouped_gemm_fold_xrows_rows(const uint16_t *x_rows, const int32_t *expert_offsets,
+                                            const int32_t *src, const int32_t *row_adapter,
+                                            const uint64_t *w_table, const uint64_t *a_table,
+                                            const uint64_t *b_table, const float *scale_table,
+                                            const uint16_t *prior_rows, const int32_t *rows,
+                                            int32_t n_rows, double *ref_out, uint8_t *written,
+                                            uint8_t *folded, int32_t k_in, int32_t max_rank,
+                                            int32_t n_out, int32_t top_k, int32_t n_experts,
+                                            int32_t row_offset, int32_t row_end) {
+    if (max_rank > 1024 || top_k < 1) return OR_NONE;
+#pragma omp parallel for schedule(dynamic, 8)
+    for (int32_t i = 0; i < n_rows; ++i) {
+        int32_t r = rows[i];
+        double *ref_row = ref_out + (int64_t)i * n_out;
+        copy_row(prior_rows + (int64_t)i * n_out, ref_row, n_out);
+        written[i] = 0;
+        folded[i] = 0;
+        if (r < row_offset || r >= row_end) continue;
+        int32_t owner = -1;
+        for (int32_t e = 0; e < n_experts; ++e) {
+            if (expert_offsets[e] <= r && r < expert_offsets[e + 1]) {
+                owner = e;
+                break;
+            }
+        }
+        if (owner < 0 || w_table[owner] == 0) continue;
+        const uint16_t *W = (const uint16_t *)(uintptr_t)w_table[owner];
+        const uint16_t *xr = x_rows + (int64_t)r * k_in;
+        for (int32_t n = 0; n < n_out; ++n) {
+            double g = 0.0;
+            for (int32_t k = 0; k < k_in; ++k)
+                g += bf16_value(xr[k]) * bf16_value(W[(int64_t)n * k_in + k]);
+            ref_row[n] = g;
+        }
+        written[i] = 1;
+        if (!expert_folds(owner, n_experts, a_table, b_table) || src[r] < 0 ||
+            (row_adapter != NULL && row_adapter[src[r] / top_k] < 0))
+            continue;
+        const uint16_t *A = (const uint16_t *)(uintptr_t)a_table[owner];
+        const uint16_t *B = (const uint16_t *)(uintptr_t)b_table[owner];
+        double h[1024];
+        for (int32_t j = 0; j < max_rank; ++j) {
+            double acc = 0.0;
+            for (int32_t k = 0; k < k_in; ++k)
+                acc += bf16_value(xr[k]) * bf16_value(A[(int64_t)j * k_in + k]);
+            h[j] = acc;
+        }
+        double scale = (double)scale_table[owner];
+        for (int32_t n = 0; n < n_out; ++n) {
+            double d = 0.0;
+            for (int32_t j = 0; j < max_rank; ++j) d += h[j] * bf16_value(B[(int64_t)n * max_rank + j]);
+            ref_row[n] += scale * d;
+        }
+        folded[i] = 1;
+    }
+    return OR_OK;
+}

@@ -507,6 +507,17 @@ def pin_gemm_fold(o):
                                          base_p, K, w.max_rank, N, w.top_k, 0, R)
     assert np.array_equal(ref[written], ref_f[written])
     assert np.array_equal(folded, fold_f & written)
+    # the row-sampled entry point equals the corresponding rows of a windowed call
+    lo, hi = 3, R - 5
+    ref_w, wr_w, fo_w = o.grouped_gemm_fold_xrows(w.x_rows, w.expert_offsets, w.src, ra,
+                                                  W.table, at, bt, st, w.base, K, w.max_rank, N,
+                                                  w.top_k, lo, hi)
+    rows = np.array([0, 2, 3, 7, R - 6, R - 5, R - 1, 19, int(w.expert_offsets[no_w])], np.int32)
+    ref_s, wr_s, fo_s = o.grouped_gemm_fold_xrows_rows(w.x_rows, w.expert_offsets, w.src, ra,
+                                                       W.table, at, bt, st, w.base[rows], rows, K,
+                                                       w.max_rank, N, w.top_k, lo, hi)
+    assert np.array_equal(ref_s, ref_w[rows])
+    assert np.array_equal(wr_s, wr_w[rows]) and np.array_equal(fo_s, fo_w[rows])
 
 
 ALL_PINS = [

@@ -81,6 +81,9 @@ WORKLOADS = {
     "tiny_decode": "tiny decode gather fold: 4 tokens x top-2, 8 experts (2 unadapted), rank 8",
     "prefill_down_fused": "expert GEMM with the fold in its epilogue, down-proj: prefill_down_xrows "
                           "plus every expert's weight W_e [2048, 768]; out = x_rows W_e^T + fold",
+    "prefill_large_fused": "expert GEMM with the fold in its epilogue at the large prefill's scale: "
+                           "163840 sorted rows, x_rows [163840, 512], 512 experts' W_e [2048, 512], "
+                           "rank 32",
 }
 
 
@@ -258,8 +261,18 @@ def time_oracle(w, budget_s=10.0, threads=1):
     o = oracle.get()
     used = o.set_threads(threads)
     he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
-    at, bt, st = he.tables(o, length=(w.n_adapters * w.n_experts_model) if w.n_adapters else None)
+    length = (w.n_adapters * w.n_experts_model) if w.n_adapters else None
+    if w.weights is not None:  # one table cell per expert of the stacked weights
+        length = w.n_experts_model
+    at, bt, st = he.tables(o, length=length)
     flops_row = 2 * w.max_rank * (w.k_in + w.n_out)
+    if w.weights is not None:  # the expert GEMM as well
+        flops_row += 2 * w.k_in * w.n_out
+        keep = np.ascontiguousarray(w.weights, np.uint16)
+        wt = np.zeros(at.size, np.uint64)
+        step = keep.shape[1] * keep.shape[2] * 2
+        for e in range(min(at.size, keep.shape[0])):
+            wt[e] = keep.ctypes.data + e * step
     full_cost = w.rows * flops_row
     rng = np.random.default_rng(0)
     t0 = time.perf_counter()
@@ -277,6 +290,10 @@ def time_oracle(w, budget_s=10.0, threads=1):
                                                     w.has_moe_lora)
                 o.gather_fold(w.x, w.indices, ra, at, bt, st, w.base, w.k_in, w.max_rank,
                               w.n_out, w.top_k)
+            elif w.kind == "grouped" and w.weights is not None:
+                ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+                o.grouped_gemm_fold_xrows(w.x_rows, w.expert_offsets, w.src, ra, wt, at, bt, st,
+                                          w.base, w.k_in, w.max_rank, w.n_out, w.top_k, 0, w.rows)
             elif w.kind == "grouped" and w.x_rows is not None:
                 ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
                 o.grouped_fold_xrows(w.x_rows, w.expert_offsets, w.src, ra, at, bt, st, w.base,
@@ -297,7 +314,12 @@ def time_oracle(w, budget_s=10.0, threads=1):
     chunk = 64 * used
     while time.perf_counter() - t0 < budget_s or done == 0:
         rows = np.sort(rng.choice(w.rows, size=min(chunk, w.rows), replace=False)).astype(np.int32)
-        if w.kind == "grouped" and w.x_rows is not None:
+        if w.kind == "grouped" and w.weights is not None:
+            ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+            o.grouped_gemm_fold_xrows_rows(w.x_rows, w.expert_offsets, w.src, ra, wt, at, bt, st,
+                                           w.base[rows], rows, w.k_in, w.max_rank, w.n_out,
+                                           w.top_k, 0, w.rows)
+        elif w.kind == "grouped" and w.x_rows is not None:
             ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
             o.grouped_fold_xrows_rows(w.x_rows, w.expert_offsets, w.src, ra, at, bt, st,
                                       w.base[rows], rows, w.k_in, w.max_rank, w.n_out, w.top_k,
@@ -344,7 +366,7 @@ KERNEL_OF = {"decode_down": "mlg_decode.cu", "decode_gate_up": "mlg_gather.cu",
              "tiny_decode": "mlg_gather.cu", "prefill_down": "mlg_grouped.cu",
              "prefill_large": "mlg_grouped.cu", "router": "mlg_grouped.cu",
              "prefill_down_xrows": "mlg_grouped.cu", "decode_down_multi": "mlg_decode.cu",
-             "prefill_down_fused": "mlg_gemm_fold.cu"}
+             "prefill_down_fused": "mlg_gemm_fold.cu", "prefill_large_fused": "mlg_gemm_fold.cu"}
 
 
 def kernel_source(workload):
@@ -767,7 +789,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--extra", default="decode_down,decode_gate_up,decode_down_multi,prefill_down,"
-                                       "prefill_down_xrows,router,prefill_down_fused",
+                                       "prefill_down_xrows,router,prefill_down_fused,"
+                                       "prefill_large_fused",
                     help="other workloads measured in the same run (comma list, or 'none')")
     ap.add_argument("--replays", type=int, default=REPLAYS)
     ap.add_argument("--no-cpu-baseline", action="store_true")

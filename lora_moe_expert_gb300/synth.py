@@ -41,6 +41,9 @@ Shapes of the named workloads:
 * ``prefill_down_fused`` ``prefill_down_xrows`` plus every expert's GEMM
                        weight W_e [2048, 768] ~ N(0, 1/768): the expert GEMM
                        with the fold in its epilogue
+* ``prefill_large_fused`` ``prefill_large`` with a per-row input x_rows
+                       [163840, 512] and the 512 experts' weights
+                       W_e [2048, 512] ~ N(0, 1/512), the same fused form
 """
 from __future__ import annotations
 
@@ -239,6 +242,17 @@ def prefill_large(seed: int = 4) -> Workload:
     return _prefill("prefill_large", rng, np.array([16384]), 10, 512, 512, 2048, 32, 32768)
 
 
+def prefill_large_fused(seed: int = 4) -> Workload:
+    """The large prefill as the expert GEMM with the fold in its epilogue: a
+    per-row input x_rows [163840, 512] and the 512 experts' stacked weights
+    W [512, 2048, 512]."""
+    w = prefill_large(seed)
+    rng = np.random.default_rng(seed + 5000)
+    w.name = "prefill_large_fused"
+    w.x_rows = _normal_bf16(rng, (w.rows, w.k_in))
+    return add_expert_weights(w, seed + 7000)
+
+
 def router(seed: int = 4) -> Workload:
     rng = np.random.default_rng(seed + 1000)
     T, k_in, n_out, r = 16384, 2048, 512, 32
@@ -346,4 +360,5 @@ NAMED = {
     "prefill_large": prefill_large,
     "router": router,
     "prefill_down_fused": prefill_down_fused,
+    "prefill_large_fused": prefill_large_fused,
 }

@@ -187,3 +187,32 @@ def test_graph_replay_matches_eager():
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(prob.base_bits(), eager)
+
+
+def test_prefill_large_fused_full():
+    """The expert GEMM with the fold at the large prefill's scale (163840 sorted
+    rows, 512 experts, W_e 2048 x 512, rank 32), in the benchmark's launch
+    configuration, checked in every element: the oracle (all host cores)
+    computes every sorted row in chunks."""
+    from lora_moe_expert_gb300.device import FoldProblem
+
+    w = synth.prefill_large_fused()
+    prob = FoldProblem(w, guard_rows=2)
+    prob.run()
+    torch.cuda.synchronize()
+    got = prob.base_bits()
+    assert np.all(prob.guard_bits() == 0x7FC1), "guard rows changed"
+    o = oracle.get()
+    o.set_threads(0)
+    he = oracle.HostExperts([(e.expert_id, e.A, e.B, e.scale) for e in w.experts])
+    at, bt, st = he.tables(o, length=prob.n_experts)
+    wt, keep = fh.weight_table(w, prob.n_experts)
+    ra = o.build_moe_row_adapter_host(w.cu_seqlens, w.stream_slots)
+    chunk = 16384
+    for r0 in range(0, w.rows, chunk):
+        rows = np.arange(r0, min(r0 + chunk, w.rows), dtype=np.int32)
+        ref, written, folded = o.grouped_gemm_fold_xrows_rows(
+            w.x_rows, w.expert_offsets, w.src, ra, wt, at, bt, st, w.base[rows], rows, w.k_in,
+            w.max_rank, w.n_out, w.top_k, 0, w.rows)
+        assert written.all() and folded.all()
+        fh.check_fold(got[rows], w.base[rows], ref, written)

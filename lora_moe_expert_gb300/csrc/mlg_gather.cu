@@ -16,8 +16,9 @@
 //        columns [q*ks, (q+1)*ks); the partial h are summed through
 //        distributed shared memory in a fixed rank order; chosen when A_e
 //        dominates (gate / up projections);
-//  * loads and stores are TMA bulk copies issued by one warp with mbarrier
-//    completion; the weights are requested as soon as the table is read, and
+//  * loads and stores are TMA bulk copies with mbarrier completion (the A_e
+//    rows spread over every warp); the weights are requested as soon as the
+//    table is read, and
 //    the B_e fragments of the expand are loaded straight into registers;
 //  * programmatic dependent launch: the table read and the weight requests
 //    happen before griddepcontrol.wait, so they overlap the preceding kernel;
@@ -350,17 +351,18 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
         for (uint32_t o = 0; o < bb; o += 8192) prefetch_l2(B2 + o, min(8192u, bb - o));
       }
     }
+    // A_e k slice: one bulk copy per rank row, issued by eight lanes of every
+    // warp (a single warp issuing all of them stalls for ~2 us on the copy
+    // engine's queue, and every warp then waits for it at the routing scan).
+    // The byte count is posted before the barrier, so it precedes every copy.
+    if (tid == 0 && !bad) mbar_arrive_expect_tx(bar_w, ksv > 0 ? r * ksv * 2u : 0u);
     fence_proxy_async_smem();  // earlier generic accesses before new async writes
     __syncthreads();
-    if (warp == 0 && !bad) {  // A_e k slice: one bulk copy per rank row
-      const uint32_t bytes = ksv > 0 ? r * ksv * 2u : 0u;
-      if (lane == 0) mbar_arrive_expect_tx(bar_w, bytes);
-      __syncwarp();
+    if (!bad && ksv > 0 && lane < 8) {
       const uint8_t *A = reinterpret_cast<const uint8_t *>(a_addr);
-      if (ksv > 0)
-        for (int j = lane; j < r; j += 32)
-          bulk_g2s(smem_addr(sA + j * p.stride_a), A + (static_cast<size_t>(j) * p.k_in + k0) * 2,
-                   ksv * 2u, bar_w);
+      for (int j = warp * 8 + lane; j < r; j += kWarps * 8)
+        bulk_g2s(smem_addr(sA + j * p.stride_a), A + (static_cast<size_t>(j) * p.k_in + k0) * 2,
+                 ksv * 2u, bar_w);
     }
     // B_e fragments of this warp's first m-tiles, straight into registers
     const uint8_t *B = reinterpret_cast<const uint8_t *>(b_addr);

@@ -40,8 +40,8 @@
  *    before it reads the routing (indices, expert_offsets, src), the row map,
  *    x or base_out, so those may be written by the preceding kernel.  The
  *    grouped and router folds read everything else after that wait too.  The
- *    decode folds (mlg_gather_bgmv, mlg_gather_bgmv_multi) do NOT: they read
- *    a_table, b_table, scale_table and the A_e / B_e pairs those tables
+ *    decode folds (mlg_gather_bgmv, mlg_gather_bgmv_multi) do NOT: they may
+ *    read a_table, b_table, scale_table and the A_e / B_e pairs those tables
  *    point to BEFORE the wait, to overlap the pair traffic with the preceding
  *    kernel.  Tables and pairs written by a copy (cudaMemcpy*, as the upload
  *    helpers do) are safe, because a copy is never overlapped; a caller whose

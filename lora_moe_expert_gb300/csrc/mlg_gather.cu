@@ -17,12 +17,13 @@
 //        distributed shared memory in a fixed rank order; chosen when A_e
 //        dominates (gate / up projections);
 //  * loads and stores are TMA bulk copies with mbarrier completion (the A_e
-//    rows spread over every warp); the weights are requested as soon as the
-//    table is read, and
-//    the B_e fragments of the expand are loaded straight into registers;
-//  * programmatic dependent launch: the table read and the weight requests
-//    happen before griddepcontrol.wait, so they overlap the preceding kernel;
-//    routing, x and base_out are read only after it;
+//    rows spread over every warp); the B_e fragments of the expand are loaded
+//    straight into registers;
+//  * programmatic dependent launch: the table read and the compaction of the
+//    experts that fold happen before griddepcontrol.wait, so they overlap the
+//    preceding kernel; after it the routing loads go out first, then the
+//    weight copies, so the routing scan does not wait behind the pair stream;
+//    x, base_out and the B_e fragments follow the scan;
 //  * shrink h = x A_e^T on the tensor cores (mma.sync m16n8k16 bf16 -> fp32,
 //    M = rank, N = rows; decode has 1..32 rows per expert, below any tcgen05
 //    M); expand with swapped operands (M = 16 rows of B_e, N = rows, K = rank)
@@ -351,6 +352,15 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
         for (uint32_t o = 0; o < bb; o += 8192) prefetch_l2(B2 + o, min(8192u, bb - o));
       }
     }
+    // Routing, x and base_out may be written by the preceding kernel.  The
+    // routing loads go out first: issued after the weight copies they would
+    // queue behind the whole pair stream (~3 us) on their way back.
+    if (!waited) {
+      griddep_wait();
+      waited = true;
+    }
+    int idx0[kScanPer], ra0[kScanPer];
+    scan_load(p, 0, idx0, ra0);
     // A_e k slice: one bulk copy per rank row, issued by eight lanes of every
     // warp (a single warp issuing all of them stalls for ~2 us on the copy
     // engine's queue, and every warp then waits for it at the routing scan).
@@ -364,29 +374,17 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
         bulk_g2s(smem_addr(sA + j * p.stride_a), A + (static_cast<size_t>(j) * p.k_in + k0) * 2,
                  ksv * 2u, bar_w);
     }
-    // B_e fragments of this warp's first m-tiles, straight into registers
+    // B_e fragments go straight into registers once the first row group's x
+    // and base_out copies are out (their loads would delay the routing scan).
     const uint8_t *B = reinterpret_cast<const uint8_t *>(b_addr);
     const int mtn = (nsv + 15) / 16;
     uint32_t bf[MPP][KST][4];
-    int bf_pass = 0;  // which pass of m-tiles bf holds
-#pragma unroll
-    for (int i = 0; i < MPP; ++i) {
-      const int m = warp + i * kWarps;
-      if (m < mtn) load_b_frags<KST>(B, n0 + m * 16 + g, p.n_out, r, c, bf[i]);
-    }
-
-    // Routing, x and base_out may be written by the preceding kernel.
-    if (!waited) {
-      griddep_wait();
-      waited = true;
-    }
+    int bf_pass = -1;  // which pass of m-tiles bf holds (none yet)
     const bool count = n_helpers > 0 && !help;  // an owner also counts every expert's rows
     if (count) {
       for (int i = tid; i < p.n_experts; i += kThreads) s_hist[i] = 0;
       __syncthreads();
     }
-    int idx0[kScanPer], ra0[kScanPer];
-    scan_load(p, 0, idx0, ra0);
     const int total = scan_rows(p, e, 0, kMaxRowGroup, idx0, ra0, true, s_rows, s_cnt,
                                 count ? s_hist : nullptr);
     // Rows of this unit: [0, total), or a half of them when the expert is split.
@@ -435,6 +433,14 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
             bulk_g2s(smem_addr(sBase + lane * p.stride_base),
                      p.base_out + static_cast<size_t>(row) * p.n_out + n0, nsv * 2u, bar_x);
         }
+      }
+      if (bf_pass != 0) {  // B_e fragments of this warp's first m-tiles
+#pragma unroll
+        for (int i = 0; i < MPP; ++i) {
+          const int m = warp + i * kWarps;
+          if (m < mtn) load_b_frags<KST>(B, n0 + m * 16 + g, p.n_out, r, c, bf[i]);
+        }
+        bf_pass = 0;
       }
       bool timed_out = false;
       if (!bad && !have_weights) timed_out = !mbar_wait_bounded(bar_w, ph_w);

@@ -474,31 +474,52 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
         kq = warp / units;
       }
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      // A warp with one unit splits its k blocks over both accumulators (two
-      // independent MMA chains), added in a fixed order afterwards.
+      // A warp with one unit spreads its MMAs over four accumulators (four
+      // independent chains: the two MMAs of a k block, even and odd blocks),
+      // added in a fixed order afterwards.
       const bool dual = my_units[1] < 0;
       if (!bad && my_units[0] >= 0) {
         const int kb_lo = kq * kblocks / ksplit, kb_hi = (kq + 1) * kblocks / ksplit;
-#pragma unroll 4
-        for (int kb = kb_lo; kb < kb_hi; ++kb) {
-          const uint32_t kbyte = (kb * 32 + 8 * c) * 2;
+        if (dual) {
+          float ex[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          const int u = my_units[0], mt = u % MT, nt = u / MT;
+          const uint8_t *ra = sA + (mt * 16 + g) * p.stride_a, *rb = ra + 8 * p.stride_a;
+          const uint8_t *rx = sX + (nt * 8 + g) * p.stride_a;
+#pragma unroll 2
+          for (int kb = kb_lo; kb < kb_hi; kb += 2) {
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int u = dual ? my_units[0] : my_units[i];
-            if (u < 0 || (dual && i != ((kb - kb_lo) & 1))) continue;
-            const int mt = u % MT, nt = u / MT;
-            const uint4 pa = *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g) * p.stride_a + kbyte);
-            const uint4 qa =
-                *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g + 8) * p.stride_a + kbyte);
-            const uint4 sx = *reinterpret_cast<const uint4 *>(sX + (nt * 8 + g) * p.stride_a + kbyte);
-            mma_bf16_16816(acc[i], pa.x, qa.x, pa.y, qa.y, sx.x, sx.y);
-            mma_bf16_16816(acc[i], pa.z, qa.z, pa.w, qa.w, sx.z, sx.w);
+            for (int q = 0; q < 2; ++q) {
+              if (kb + q >= kb_hi) continue;
+              const uint32_t kbyte = ((kb + q) * 32 + 8 * c) * 2;
+              const uint4 pa = *reinterpret_cast<const uint4 *>(ra + kbyte);
+              const uint4 qa = *reinterpret_cast<const uint4 *>(rb + kbyte);
+              const uint4 sx = *reinterpret_cast<const uint4 *>(rx + kbyte);
+              mma_bf16_16816(acc[q], pa.x, qa.x, pa.y, qa.y, sx.x, sx.y);
+              mma_bf16_16816(ex[q], pa.z, qa.z, pa.w, qa.w, sx.z, sx.w);
+            }
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) acc[0][v] = (acc[0][v] + ex[0][v]) + (acc[1][v] + ex[1][v]);
+        } else {
+#pragma unroll 4
+          for (int kb = kb_lo; kb < kb_hi; ++kb) {
+            const uint32_t kbyte = (kb * 32 + 8 * c) * 2;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int u = my_units[i];
+              if (u < 0) continue;
+              const int mt = u % MT, nt = u / MT;
+              const uint4 pa =
+                  *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g) * p.stride_a + kbyte);
+              const uint4 qa =
+                  *reinterpret_cast<const uint4 *>(sA + (mt * 16 + g + 8) * p.stride_a + kbyte);
+              const uint4 sx =
+                  *reinterpret_cast<const uint4 *>(sX + (nt * 8 + g) * p.stride_a + kbyte);
+              mma_bf16_16816(acc[i], pa.x, qa.x, pa.y, qa.y, sx.x, sx.y);
+              mma_bf16_16816(acc[i], pa.z, qa.z, pa.w, qa.w, sx.z, sx.w);
+            }
           }
         }
-      }
-      if (dual) {
-#pragma unroll
-        for (int v = 0; v < 4; ++v) acc[0][v] += acc[1][v];
       }
       // acc[i] = (rank mt*16+g, row nt*8+2c), (.., +1), (rank +8, row), (rank +8, row +1)
       float *dst = (ksplit == 1) ? sHloc : sP + kq * (ntr * 8 * HS);
@@ -595,10 +616,13 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
             // All MMAs of the pass first, then every base element is read, then
             // every result written: the shared-memory round trips overlap instead
             // of forming one load -> store chain per element.
+            // The hi and lo halves accumulate in separate registers (two
+            // independent MMA chains per m-tile), summed in a fixed order.
             float d[MPP][4];
 #pragma unroll
             for (int i = 0; i < MPP; ++i) {
               const int m = warp + (pass * MPP + i) * kWarps;
+              float dl[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
               for (int u = 0; u < 4; ++u) d[i][u] = 0.f;
               if (m >= mtn) continue;
@@ -606,9 +630,11 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
               for (int st = 0; st < KST; ++st) {
                 mma_bf16_16816(d[i], bf[i][st][0], bf[i][st][1], bf[i][st][2], bf[i][st][3],
                                hh[st][0], hh[st][1]);
-                mma_bf16_16816(d[i], bf[i][st][0], bf[i][st][1], bf[i][st][2], bf[i][st][3],
+                mma_bf16_16816(dl, bf[i][st][0], bf[i][st][1], bf[i][st][2], bf[i][st][3],
                                hl[st][0], hl[st][1]);
               }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) d[i][u] += dl[u];
             }
             // d[i] = (n m*16+g, row nt*8+2c), (n, row+1), (n+8, row), (n+8, row+1)
             constexpr int CH = MPP < 4 ? MPP : 4;  // m-tiles per batch of loads (registers)

@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(kThreads, 2) gather_fold_kernel(const GatherPa
   bool waited = false;  // griddep_wait() done (before the first routing / x / base read)
 
   // Units are (expert, n slice) pairs over the experts whose cells fold
-  // (tables are never written by the preceding kernel: read before the wait),
+  // (tables are read before the wait: under early start the caller's contract
+  // is that the preceding kernel does not write them),
   // so no cluster spends a round on an expert that folds nothing.  With
   // hit_compact (sparse tables: many cells, few rows each) the routing is
   // read first and only cells with a folding row become units, so no pair is

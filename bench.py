@@ -580,7 +580,12 @@ def gpu_measure(name, steps, warmup, device, seed_base=1000, replays=REPLAYS, e2
 
 def e2e_measure(prob, steps, device):
     """Through the public API with host buffers: route + map and table packing on
-    the host, pinned H2D copies of the step's inputs, the fold, D2H of base_out."""
+    the host, pinned H2D copies of the step's inputs, the fold, D2H of base_out.
+    A prefill workload with more than one row window runs the range calls on
+    pieces of at most 8192 rows (inside windows), so piece i's rows go up while
+    piece i-1 folds and piece i-2's come back, on three streams; the
+    GEMM + fold form writes every row of its spans, so its base_out is not
+    uploaded."""
     import torch
 
     import lora_moe_expert_gb300 as mlg
@@ -623,9 +628,12 @@ def e2e_measure(prob, steps, device):
             if m is not None:
                 mlg.mlg_upload_row_adapter(m, prob.row_adapter, stream=s)
                 h2d += m.nbytes
-            d_x.view(torch.int16).copy_(h_x, non_blocking=True)
-            prob.base.view(torch.int16).copy_(h_base, non_blocking=True)
-            h2d += h_x.numel() * 2 + h_base.numel() * 2
+            if windows is None or not xrows:  # token x: the whole of it, before any window
+                d_x.view(torch.int16).copy_(h_x, non_blocking=True)
+                h2d += h_x.numel() * 2
+            if windows is None:
+                prob.base.view(torch.int16).copy_(h_base, non_blocking=True)
+                h2d += h_base.numel() * 2
             if h_idx is not None:
                 prob.indices.copy_(h_idx, non_blocking=True)
                 h2d += h_idx.numel() * 4
@@ -633,10 +641,71 @@ def e2e_measure(prob, steps, device):
                 prob.expert_offsets.copy_(h_off, non_blocking=True)
                 prob.src.copy_(h_src, non_blocking=True)
                 h2d += h_off.numel() * 4 + h_src.numel() * 4
-            prob.run(stream=s)
-            h_out.copy_(prob.base.view(torch.int16), non_blocking=True)
-            d2h += h_out.numel() * 2
+            if windows is None:
+                prob.run(stream=s)
+                h_out.copy_(prob.base.view(torch.int16), non_blocking=True)
+                d2h += h_out.numel() * 2
+        if windows is not None:
+            windowed(s)
         s.synchronize()
+        if windows is not None:
+            s_cmp.synchronize()
+            s_d2h.synchronize()
+
+    # Windowed prefill forms: the window calls of the public API let window
+    # i's base_out rows (and per-row x) go up while window i-1 folds and
+    # window i-2's rows come back, on three streams (a caller's own pipeline).
+    # The fused form writes every row, so its base_out is never uploaded.
+    windows = None
+    if w.kind == "grouped" and len(prob.windows) > 1:
+        # pieces of at most 8192 rows inside each window (a call may take any
+        # sub-range of a window: every row's result is independent of it)
+        windows = []
+        for (a0, a1) in prob.windows:
+            n_p = -(-(a1 - a0) // 8192)
+            windows += [(a0 + (a1 - a0) * i // n_p, a0 + (a1 - a0) * (i + 1) // n_p)
+                        for i in range(n_p)]
+        s_cmp = torch.cuda.Stream(device=device)
+        s_d2h = torch.cuda.Stream(device=device)
+    fused = prob.w_experts is not None
+
+    def windowed(s_up):
+        nonlocal h2d, d2h
+        ra = prob.row_adapter
+        for (r0, r1) in windows:
+            with torch.cuda.stream(s_up):
+                if xrows:
+                    prob.x_rows[r0:r1].view(torch.int16).copy_(h_x[r0:r1], non_blocking=True)
+                    h2d += (r1 - r0) * h_x.shape[1] * 2
+                if not fused:
+                    prob.base[r0:r1].view(torch.int16).copy_(h_base[r0:r1], non_blocking=True)
+                    h2d += (r1 - r0) * h_base.shape[1] * 2
+                up = torch.cuda.Event()
+                up.record(s_up)
+            s_cmp.wait_event(up)
+            with torch.cuda.stream(s_cmp):
+                if fused:
+                    mlg.mlg_grouped_gemm_fold_xrows(prob.x_rows, prob.expert_offsets, prob.src, ra,
+                                                    prob.w_experts, prob.a_table, prob.b_table,
+                                                    prob.scale_table, prob.base, w.k_in,
+                                                    w.max_rank, w.n_out, w.top_k, prob.n_experts,
+                                                    r0, r1, w.cap, stream=s_cmp)
+                elif xrows:
+                    mlg.mlg_grouped_down_xrows(prob.x_rows, prob.expert_offsets, prob.src, ra,
+                                               prob.a_table, prob.b_table, prob.scale_table,
+                                               prob.base, w.k_in, w.max_rank, w.n_out, w.top_k,
+                                               prob.n_experts, r0, r1, w.cap, stream=s_cmp)
+                else:
+                    mlg.mlg_grouped_down(prob.x, prob.expert_offsets, prob.src, ra, prob.a_table,
+                                         prob.b_table, prob.scale_table, prob.base, w.k_in,
+                                         w.max_rank, w.n_out, w.top_k, prob.n_experts, r0, r1,
+                                         stream=s_cmp)
+                done = torch.cuda.Event()
+                done.record(s_cmp)
+            s_d2h.wait_event(done)
+            with torch.cuda.stream(s_d2h):
+                h_out[r0:r1].copy_(prob.base[r0:r1].view(torch.int16), non_blocking=True)
+                d2h += (r1 - r0) * h_out.shape[1] * 2
 
     for _ in range(3):
         step()

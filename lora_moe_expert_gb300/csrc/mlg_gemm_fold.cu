@@ -11,7 +11,9 @@
 // cells, src[r] >= 0 and a non-negative row-map entry for its token).
 //
 // GB300 design (one CTA per SM, persistent over expert-aligned tiles of <= 128
-// rows that never cross a row window):
+// rows that never cross a row window, dealt round-robin; the tiles of a last,
+// partial round are split into pieces of their output chunks so that no CTA
+// idles for a whole tile time):
 //  * one shared-memory ring of stages, each an X box (128 rows x 64 k, TMA,
 //    128-byte swizzle) and a Y tile (up to 256 rows x 64 k in the same
 //    swizzle); per tile the ring carries, in order, the shrink's stages
@@ -96,6 +98,7 @@ struct FTile {
   int e, r0, r1;
   float scale;
   int lora;
+  int nc0, nc1;  // the output chunks this CTA computes: [nc0, nc1)
 };
 
 __device__ __forceinline__ bool wait_f(FCtl &ctl, uint64_t &bar, uint32_t parity) {
@@ -224,14 +227,29 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     if (tid == 0) tile_start[n_e] = carry;
   }
   __syncthreads();
+  // This CTA's work: tile c + i G of every full round i (all output chunks).
+  // A tile costs about the same whatever its rows (its MMAs are per 128-row
+  // tile), so a last round of R < G tiles would leave G - R CTAs idle for a
+  // whole tile time (the 163840-row prefill: 1526 tiles on 152 SMs, 11 tile
+  // times where 10.04 would do).  Its tiles are split instead into P pieces
+  // of their output chunks, P = min(chunks, G / R), piece u going to CTA u
+  // (each piece recomputes its tile's h; rows and results are unchanged).
   FTile *my_tiles = reinterpret_cast<FTile *>(smem + p.off_my);
   const int n_tiles_all = tile_start[n_e];
-  int my_count = 0;
-  if (static_cast<int>(blockIdx.x) < n_tiles_all)
-    my_count = min(kMyTilesMaxF, (n_tiles_all - 1 - static_cast<int>(blockIdx.x)) /
-                                         static_cast<int>(gridDim.x) + 1);
+  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  const int q_full = n_tiles_all / G, rest = n_tiles_all % G;
+  const int pieces = rest > 0 ? max(1, min(p.nc_count, G / rest)) : 1;
+  const bool has_piece = cta < rest * pieces;
+  const int my_count = min(kMyTilesMaxF, q_full + (has_piece ? 1 : 0));
   if (tid < my_count) {
-    const TileInfo ti = tile_info(p, tile_start, n_e, blockIdx.x + tid * gridDim.x);
+    int t = cta + tid * G, nc0 = 0, nc1 = p.nc_count;
+    if (tid == q_full) {  // this CTA's piece of a last-round tile
+      const int j = cta % pieces;
+      t = q_full * G + cta / pieces;
+      nc0 = j * p.nc_count / pieces;
+      nc1 = (j + 1) * p.nc_count / pieces;
+    }
+    const TileInfo ti = tile_info(p, tile_start, n_e, t);
     const uint64_t a = __ldg(reinterpret_cast<const unsigned long long *>(p.a_table) + ti.e);
     const uint64_t b = __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ti.e);
     my_tiles[tid].e = ti.e;
@@ -239,6 +257,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     my_tiles[tid].r1 = ti.r1;
     my_tiles[tid].scale = __ldg(p.scale_table + ti.e);
     my_tiles[tid].lora = cells_fold(a, b) ? 1 : 0;
+    my_tiles[tid].nc0 = nc0;
+    my_tiles[tid].nc1 = nc1;
   }
   tc_fence_before();
   __syncthreads();
@@ -278,12 +298,12 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           if (!wait_f(ctl, ctl.hs_full, h_it & 1)) goto mma_done;
           tc_fence_after();
         }
-        for (int nc = 0; nc < p.nc_count; ++nc, ++acc_it) {
+        for (int nc = mt.nc0; nc < mt.nc1; ++nc, ++acc_it) {
           const int b = acc_it & 1;
           const uint32_t d = tmem + acc_col(b);
           const int ncols = min(kNch, (p.n_out - nc * kNch + 15) / 16 * 16);
           const uint32_t idesc = umma_idesc_bf16(kTileMF, ncols);
-          if (!(mt.lora && nc == 0)) {  // (the lora tile's first buffer was waited for above)
+          if (!(mt.lora && nc == mt.nc0)) {  // (the lora tile's first buffer was waited for above)
             if (!wait_f(ctl, ctl.acc_empty[b], ((acc_it >> 1) & 1) ^ 1)) goto mma_done;
             tc_fence_after();
           }
@@ -385,7 +405,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           finish(st);
         }
       }
-      for (int nc = 0; nc < p.nc_count; ++nc) {
+      for (int nc = mt.nc0; nc < mt.nc1; ++nc) {
         const int n0 = nc * kNch;
         for (int kc = 0; kc < p.kc_count; ++kc) {  // [X | W_e rows n0.., k chunk kc]: TMA only
           const int st = begin(mt.r0, kc * 64, true, mt.e, n0);
@@ -494,7 +514,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         ++h_it;
       }
       // ---- output chunks: accumulator -> registers -> one rounding -> global
-      for (int nc = 0; nc < p.nc_count; ++nc, ++acc_it) {
+      for (int nc = mt.nc0; nc < mt.nc1; ++nc, ++acc_it) {
         const int b = acc_it & 1;
         if (!wait_f(ctl, ctl.acc_full[b], (acc_it >> 1) & 1)) goto epi_done;
         tc_fence_after();

@@ -13,7 +13,9 @@
 //  * tiles are expert-aligned runs of <= 128 sorted rows (one tcgen05 M), so
 //    a tile never mixes experts and every output row has one owner; the tile
 //    list is built on the device from expert_offsets and the tables (no host
-//    copy), and persistent CTAs (one per SM) walk it round-robin.  The setup
+//    copy), and persistent CTAs (one per SM) walk it round-robin (the tiles
+//    of a last, partial round split into pieces of their expand chunks over
+//    the idle CTAs).  The setup
 //    that reads none of the fold's inputs runs before griddepcontrol.wait, so
 //    it overlaps the preceding kernel (programmatic dependent launch);
 //  * warp 0 issues the tensor-core work: shrink H = X A_e^T (M=128, N=rank,
@@ -119,6 +121,7 @@ __device__ __forceinline__ bool wait_bar(Ctl &ctl, uint64_t &bar, uint32_t parit
 // each epilogue lane reads its own rows' row-map entries once, up front.
 struct MyTile {
   int e, r0, r1;
+  int nc0, nc1;  // the expand chunks this CTA folds: [nc0, nc1)
 };
 
 
@@ -228,17 +231,32 @@ __global__ void __launch_bounds__(kGThreads, 1)
   // This CTA's tiles (t = blockIdx.x + i * gridDim.x): expert and rows.  (The
   // scale is read by the epilogue, which needs it only for the first h split,
   // so its round trip is not on the prologue's path.)
+  // Full rounds: tile c + i G, all expand chunks.  The tiles of a last,
+  // partial round of R < G tiles are split into P = min(chunks, G / R) pieces
+  // of their expand chunks, piece u to CTA u (each piece recomputes its
+  // tile's h and folds its own columns), so the CTAs holding one tile more
+  // than the rest do not set the step alone (the 163840-row prefill: 1526
+  // tiles on 152 SMs, and its last CTAs to finish were those with 11 tiles).
   MyTile *my_tiles = reinterpret_cast<MyTile *>(smem + p.off_my);
   const int n_tiles_all = tile_start[n_e];
-  int my_count = 0;
-  if (static_cast<int>(blockIdx.x) < n_tiles_all)
-    my_count = min(p.my_cap, (n_tiles_all - 1 - static_cast<int>(blockIdx.x)) /
-                                     static_cast<int>(gridDim.x) + 1);
+  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  const int q_full = n_tiles_all / G, rest = n_tiles_all % G;
+  const int pieces = rest > 0 ? max(1, min(p.nc_count, G / rest)) : 1;
+  const int my_count = min(p.my_cap, q_full + (cta < rest * pieces ? 1 : 0));
   if (tid < my_count) {
-    const TileInfo ti = tile_info(p, tile_start, n_e, blockIdx.x + tid * gridDim.x);
+    int t = cta + tid * G, nc0 = 0, nc1 = p.nc_count;
+    if (tid == q_full) {  // this CTA's piece of a last-round tile
+      const int j = cta % pieces;
+      t = q_full * G + cta / pieces;
+      nc0 = j * p.nc_count / pieces;
+      nc1 = (j + 1) * p.nc_count / pieces;
+    }
+    const TileInfo ti = tile_info(p, tile_start, n_e, t);
     my_tiles[tid].e = ti.e;
     my_tiles[tid].r0 = ti.r0;
     my_tiles[tid].r1 = ti.r1;
+    my_tiles[tid].nc0 = nc0;
+    my_tiles[tid].nc1 = nc1;
   }
   tc_fence_before();
   __syncthreads();
@@ -284,7 +302,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         if (!wait_bar(ctl, ctl.hs_full, t & 1)) goto mma_done;
         tc_fence_after();
-        for (int nc = 0; nc < p.nc_count; ++nc, ++b_it, ++acc_it) {
+        for (int nc = my_tiles[t].nc0; nc < my_tiles[t].nc1; ++nc, ++b_it, ++acc_it) {
           const int st = b_it % p.nbs;
           const int ab = acc_it & 1;
           if (!wait_bar(ctl, ctl.b_full[st], (b_it / p.nbs) & 1)) goto mma_done;
@@ -440,7 +458,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const MyTile ti = my_tiles[t];
       const uint8_t *B = reinterpret_cast<const uint8_t *>(
           __ldg(reinterpret_cast<const unsigned long long *>(p.b_table) + ti.e));
-      for (int nc = 0; nc < p.nc_count; ++nc, ++it) {
+      for (int nc = ti.nc0; nc < ti.nc1; ++nc, ++it) {
         const int st = it % p.nbs;
         if (!wait_bar(ctl, ctl.b_empty[st], ((it / p.nbs) & 1) ^ 1)) goto prod_b_done;
         const uint32_t bs = b_base + st * p.b_stage;
@@ -486,18 +504,21 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const uint64_t stream_policy = l2_evict_first();  // base_out is touched once
     uint32_t tile_it = 0, acc_it = 0;
     // box sequence of this warp: (tile, box column) over tiles with rows here
+    // (a tile's boxes: the 64-column boxes of its expand chunks [nc0, nc1))
     int ld_t = 0, ld_b = sub, ld_y = 0;
     uint32_t ld_count = 0, box_it = 0;
+    auto box_hi = [&](const MyTile &ti) { return min(p.nbx, ti.nc1 * (p.n_ch / kBoxCols)); };
     auto ld_advance = [&](bool first) {
       if (!first) {
         ld_b += 2;
-        if (ld_b < p.nbx) return;
-        ld_b = sub;
+        if (ld_b < box_hi(my_tiles[ld_t])) return;
         ++ld_t;
       }
       for (; ld_t < n_tiles; ++ld_t) {
         const MyTile ti = my_tiles[ld_t];
-        if (ld_b < p.nbx && ti.r1 > ti.r0 + quarter * kBoxRows) {
+        const int b0 = ti.nc0 * (p.n_ch / kBoxCols);
+        ld_b = b0 + ((sub - b0) & 1);  // this warp's first box (its column parity)
+        if (ld_b < box_hi(ti) && ti.r1 > ti.r0 + quarter * kBoxRows) {
           ld_y = ti.r0 + quarter * kBoxRows;
           return;
         }
@@ -585,7 +606,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       }
 
       // ---- expand epilogue: base_out boxes of this warp's rows -------------
-      for (int nc = 0; nc < p.nc_count; ++nc, ++acc_it) {
+      for (int nc = ti.nc0; nc < ti.nc1; ++nc, ++acc_it) {
         const int ab = acc_it & 1;
         if (!wait_bar(ctl, ctl.acc_full[ab], (acc_it >> 1) & 1)) goto epi_done;
         tc_fence_after();

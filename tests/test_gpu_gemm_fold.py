@@ -43,6 +43,8 @@ SHAPES = [
     ([200, 300], 8, 64, 128, 136, 16, 1 << 20, 0.9, None),
     ([1], 1, 1, 64, 64, 8, 1, 1.0, None),
     ([600, 700], 8, 16, 768, 2048, 16, 8192, 1.0, None),
+    ([90, 333], 4, 9, 136, 264, 24, 150, 0.8, [0, 1]),
+    ([257, 129], 2, 5, 200, 520, 56, 4096, 1.0, None),
 ]
 
 

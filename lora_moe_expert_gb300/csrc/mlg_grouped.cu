@@ -984,10 +984,11 @@ extern "C" mlg_status mlg_router_fold(const mlg_bf16 *x, const int32_t *row_adap
   p.row_end = n_tokens;
   p.win = n_tokens;
   // One span: tiles just tall enough that every SM gets at most one (whole
-  // 16-row steps), so no SM idles while others fold a second tile.
+  // 4-row steps, so that nearly every SM gets one), so no SM idles while
+  // others fold a second tile.
   const int64_t per_sm = (static_cast<int64_t>(n_tokens) + sm_count() - 1) / sm_count();
   p.tile_m = static_cast<int32_t>(
-      std::min<int64_t>(kTileM, std::max<int64_t>(16, (per_sm + 15) / 16 * 16)));
+      std::min<int64_t>(kTileM, std::max<int64_t>(16, (per_sm + 3) / 4 * 4)));
   p.x_tma = 1;
   return launch_grouped(p, static_cast<cudaStream_t>(stream));
 }

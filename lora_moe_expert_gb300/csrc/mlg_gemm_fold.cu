@@ -128,12 +128,6 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap,
       : "memory");
 }
 
-// Arrive on `bar` once all cp.async copies this thread has issued so far have
-// landed; the arrival is one of the barrier's expected arrivals (no increment).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));

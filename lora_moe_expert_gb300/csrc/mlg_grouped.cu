@@ -80,7 +80,6 @@ struct GroupedParams {
   int32_t n_ch;                  // expand N per accumulator chunk (64 or 128)
   int32_t kc_count, nc_count, nbx;  // k chunks, n chunks, 64-column boxes per row
   int32_t nxa, nbs, depth;       // ring stages
-  int32_t xa_lag;                // X/A stages in flight before one is signalled
   uint32_t xa_stage, b_stage;    // bytes per stage
   uint32_t off_xa, off_b, off_h, off_base, off_tab, off_my, smem_bytes;
   int32_t my_cap;                // tiles per CTA the tile list holds
@@ -279,6 +278,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       int sh_t = 0, sh_kc = 0;  // next shrink chunk to issue: tile, k chunk
       auto issue_shrink_chunk = [&]() {
         const int st = xa_it % p.nxa;
+        fence_proxy_async_smem();  // A_e (and gathered x) came in by cp.async (generic proxy)
         tc_fence_after();
         const uint32_t xs = xa_base + st * p.xa_stage;
         const uint32_t as = xs + kTileM * 128;
@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const int ab = acc_it & 1;
           if (!wait_bar(ctl, ctl.b_full[st], (b_it / p.nbs) & 1)) goto mma_done;
           if (!wait_bar(ctl, ctl.acc_empty[ab], ((acc_it >> 1) & 1) ^ 1)) goto mma_done;
+          fence_proxy_async_smem();  // B_e came in by cp.async (generic proxy)
           tc_fence_after();
           const uint32_t bs = b_base + st * p.b_stage;
           const uint32_t d = tmem + (ab ? kTmemAcc1 : kTmemAcc0);
@@ -338,15 +339,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
   } else if (warp == 1 || warp == 3) {
     // ================================================================ X / A_e producers
     // Warp 1 gathers tile rows 0-63 and A_e rows 0-31, warp 3 rows 64-127 and
-    // A_e rows 32-63.  A stage is signalled xa_lag stages late (once the copies
-    // of the stages after it are issued), so xa_lag + 1 stages are in flight.
+    // A_e rows 32-63.  Every lane arrives on a stage's full barrier through
+    // cp.async.mbarrier.arrive (the arrival lands when that lane's copies have)
+    // and x boxes complete on it by their bytes, so a stage is ready as soon as
+    // its own data is, however many stages are in flight.
     const int half = warp == 1 ? 0 : 1;
     const uint64_t keep = l2_evict_last();  // A_e (and token x rows) are re-read by other tiles
     // a per-row x row (and a router row) is read once
     const uint64_t xpol = (p.x_per_row || XTMA) ? l2_evict_first() : keep;
     uint32_t it = 0;
-    int q[6] = {-1, -1, -1, -1, -1, -1};  // issued, not yet signalled stages (q[0] oldest)
-    int nq = 0;
     // x token of this lane's two rows, loaded one tile ahead
     auto tokens = [&](int t, int (&tok)[2]) {
 #pragma unroll
@@ -416,44 +417,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
                              A + (static_cast<size_t>(ja) * p.k_in + (in ? kk : 0)) * 2,
                              in ? 16u : 0u, keep);
         }
-        cp_async_commit();
-        if (nq == p.xa_lag) {  // oldest pending stage: <= xa_lag newer groups remain
-          switch (p.xa_lag) {
-            case 1: cp_async_wait_group<1>(); break;
-            case 2: cp_async_wait_group<2>(); break;
-            case 3: cp_async_wait_group<3>(); break;
-            case 4: cp_async_wait_group<4>(); break;
-            default: cp_async_wait_group<5>(); break;
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(smem_addr(&ctl.xa_full[q[0]]));
-#pragma unroll
-          for (int i = 0; i < 5; ++i) q[i] = q[i + 1];
-          --nq;
-        }
-        q[nq++] = st;
+        cp_async_arrive_noinc(smem_addr(&ctl.xa_full[st]));
       }
     }
   prod_a_done:
     cp_async_wait_group<0>();
-    fence_proxy_async_smem();
-    for (int i = 0; i < nq; ++i) mbar_arrive(smem_addr(&ctl.xa_full[q[i]]));
-    if constexpr (XTMA) {  // this warp's boxes of the unsignalled stages: let them land
-      if (lane == 0)
-        for (int j = 0; j < nq; ++j) {
-          const uint32_t k = it - nq + j;
+    if constexpr (XTMA) {  // this warp's boxes of the last stages: let them land
+      if (lane == 0) {
+        const uint32_t nl = it < static_cast<uint32_t>(p.nxa) ? it : static_cast<uint32_t>(p.nxa);
+        for (uint32_t j = 0; j < nl; ++j) {
+          const uint32_t k = it - nl + j;
           mbar_wait_bounded(smem_addr(&ctl.xa_full[k % p.nxa]), (k / p.nxa) & 1);
         }
+      }
     }
   } else if (warp == 2) {
     // ================================================================ B_e producer
-    // One B_e tile [n_ch rows x rank] per accumulator chunk, signalled `lag`
-    // stages late so lag + 1 stages are in flight.
+    // One B_e tile [n_ch rows x rank] per accumulator chunk; each lane's
+    // arrival on the stage's full barrier lands when its copies have.
     uint32_t it = 0;
     const int rc = p.rank / 8;  // 16-byte chunks per B_e row
     const uint64_t keep = l2_evict_last();
-    const int lag = p.nbs >= 3 ? 2 : 1;
-    int q0 = -1, q1 = -1, nq = 0;  // issued, not yet signalled stages (q0 oldest)
     for (int t = 0; t < n_tiles; ++t) {
       const MyTile ti = my_tiles[t];
       const uint8_t *B = reinterpret_cast<const uint8_t *>(
@@ -474,23 +458,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
                              keep);
           }
         }
-        cp_async_commit();
-        if (nq == lag) {  // the oldest pending stage has landed once <= lag groups remain
-          if (lag == 2) cp_async_wait_group<2>(); else cp_async_wait_group<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(smem_addr(&ctl.b_full[q0]));
-          q0 = q1;
-          --nq;
-        }
-        if (nq == 0) q0 = st; else q1 = st;
-        ++nq;
+        cp_async_arrive_noinc(smem_addr(&ctl.b_full[st]));
       }
     }
   prod_b_done:
     cp_async_wait_group<0>();
-    fence_proxy_async_smem();
-    if (nq >= 1) mbar_arrive(smem_addr(&ctl.b_full[q0]));
-    if (nq >= 2) mbar_arrive(smem_addr(&ctl.b_full[q1]));
   } else if (warp >= 4) {
     // ================================================================ epilogue
     // Eight warps: warp w reads TMEM lanes [32 (w % 4), +32) (its tile rows);
@@ -766,7 +738,6 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
       if ((ok = total <= kGSmemLimit)) break;
     }
   }
-  p.xa_lag = p.nxa - 1 < 3 ? p.nxa - 1 : 3;
   if (!ok) return MLG_ERR_UNSUPPORTED;
 
   CUtensorMap tmap;

@@ -204,6 +204,12 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
+// Arrive on `bar` once all cp.async copies this thread has issued so far have
+// landed; the arrival is one of the barrier's expected arrivals (no increment).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

@@ -280,10 +280,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             fence_proxy_async_smem();  // A_e came in by cp.async (generic proxy)
             tc_fence_after();
             const uint32_t xs = ring + st * p.stage_bytes, ys = xs + kXBytes;
+            const uint64_t ad = umma_desc_sw128(xs), bd = umma_desc_sw128(ys);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              umma_bf16(tmem + acc_col(b0), umma_desc_sw128(xs + k * 32),
-                        umma_desc_sw128(ys + k * 32), idesc_shrink, (kc | k) != 0);
+              umma_bf16(tmem + acc_col(b0), ad + 2 * k, bd + 2 * k, idesc_shrink, (kc | k) != 0);
             umma_commit(smem_addr(&ctl.empty[st]));
           }
           umma_commit(smem_addr(&ctl.h_full));
@@ -306,10 +306,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             if (!wait_f(ctl, ctl.full[st], (it / p.nst) & 1)) goto mma_done;
             tc_fence_after();
             const uint32_t xs = ring + st * p.stage_bytes, ys = xs + kXBytes;
+            const uint64_t ad = umma_desc_sw128(xs), bd = umma_desc_sw128(ys);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_bf16(d, umma_desc_sw128(xs + k * 32), umma_desc_sw128(ys + k * 32), idesc,
-                        (kc | k) != 0);
+            for (int k = 0; k < 4; ++k) umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kc | k) != 0);
             umma_commit(smem_addr(&ctl.empty[st]));
           }
           if (mt.lora) {  // ACC += [H_hi | H_lo] [B_e | B_e]^T

@@ -714,17 +714,19 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
   p.k_exp = static_cast<int>(rup(2 * p.r_pad, 64));
   p.kc_count = (p.k_in + 63) / 64;
   p.nbx = (p.n_out + kBoxCols - 1) / kBoxCols;
-  // Deepest rings that fit.  Rows whose x is wider than their base_out
-  // read-modify-write (router-like shapes) favour the X/A ring; the rest take
-  // four B_e stages (a tile's expand needs a fresh B_e chunk per accumulator
-  // chunk; with two stages that stream set the pace of the 163840-row
-  // prefill) beside a base_out ring four boxes deep per warp, which the
-  // compact B_e rows (b_row_bytes) leave room for: 305 us with {2, 2, 4},
-  // 274 us with {2, 4, 3}, 258 us with {2, 4, 4}; a ring two deep measured
-  // far slower (350 us).
+  // Deepest rings that fit, as {X/A stages, B_e stages, base_out boxes per
+  // warp}.  Rows whose x is wider than their base_out read-modify-write
+  // (router-like shapes) take {4, 2, 3}: the 16384-token router measured
+  // 26.5 us with {6, 2, 2} and 25.3 us with {4, 2, 3}; three X/A stages or
+  // four boxes were slower.  The rest take four B_e stages (a tile's expand
+  // needs a fresh B_e chunk per accumulator chunk; with two stages that
+  // stream set the pace of the 163840-row prefill) beside a base_out ring
+  // four boxes deep per warp, which the compact B_e rows (b_row_bytes) leave
+  // room for: 305 us with {2, 2, 4}, 274 us with {2, 4, 3}, 258 us with
+  // {2, 4, 4}; a ring two deep measured far slower (350 us).
   static const int cand_base[][3] = {{2, 4, 4}, {2, 4, 3}, {2, 2, 4}, {3, 3, 3}, {2, 3, 3},
                                      {2, 2, 3}, {2, 2, 2}};
-  static const int cand_x[][3] = {{6, 2, 2}, {5, 2, 3}, {5, 2, 2}, {4, 2, 3}, {4, 2, 2},
+  static const int cand_x[][3] = {{4, 2, 3}, {6, 2, 2}, {5, 2, 2}, {4, 2, 2}, {3, 2, 3},
                                   {3, 2, 2}, {2, 2, 2}};
   const bool x_heavy = static_cast<int64_t>(p.k_in) * 2 > static_cast<int64_t>(p.n_out) * 4;
   bool ok = false;

@@ -723,9 +723,11 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
   // stream set the pace of the 163840-row prefill) beside a base_out ring
   // four boxes deep per warp, which the compact B_e rows (b_row_bytes) leave
   // room for: 305 us with {2, 2, 4}, 274 us with {2, 4, 3}, 258 us with
-  // {2, 4, 4}; a ring two deep measured far slower (350 us).
-  static const int cand_base[][3] = {{2, 4, 4}, {2, 4, 3}, {2, 2, 4}, {3, 3, 3}, {2, 3, 3},
-                                     {2, 2, 3}, {2, 2, 2}};
+  // {2, 4, 4}; a ring two deep measured far slower (350 us).  Where a third
+  // X/A stage fits beside them (rank <= 16) it shortens the first tile's
+  // shrink: the 30K-row per-row x prefill 56.8 -> 55.3 us.
+  static const int cand_base[][3] = {{3, 4, 4}, {2, 4, 4}, {2, 4, 3}, {2, 2, 4}, {3, 3, 3},
+                                     {2, 3, 3}, {2, 2, 3}, {2, 2, 2}};
   static const int cand_x[][3] = {{4, 2, 3}, {6, 2, 2}, {5, 2, 2}, {4, 2, 2}, {3, 2, 3},
                                   {3, 2, 2}, {2, 2, 2}};
   const bool x_heavy = static_cast<int64_t>(p.k_in) * 2 > static_cast<int64_t>(p.n_out) * 4;
@@ -734,7 +736,8 @@ mlg_status launch_grouped(GroupedParams &p, cudaStream_t stream) {
   const int n_chs[2] = {128, 64};
   for (int a = 0; a < 2 && !ok; ++a) {
     const int(*cand)[3] = x_heavy ? cand_x : cand_base;
-    const int nc = 7;
+    const int nc = x_heavy ? static_cast<int>(sizeof(cand_x) / sizeof(cand_x[0]))
+                           : static_cast<int>(sizeof(cand_base) / sizeof(cand_base[0]));
     for (int i = 0; i < nc; ++i) {
       total = plan(p, n_chs[a], cand[i][0], cand[i][1], cand[i][2], n_e);
       if ((ok = total <= kGSmemLimit)) break;

@@ -266,15 +266,23 @@ def mlg_build_moe_row_adapter_host(cu_seqlens, adapter_slots) -> np.ndarray:
     return out
 
 
+# mlg_expert_entry as a numpy record (same 32-byte layout as ExpertEntry), so a
+# table of entries is filled by array assignment rather than field by field.
+_ENTRY_DT = np.dtype([("expert_id", "<u4"), ("reserved0", "<u4"), ("a_addr", "<u8"),
+                      ("b_addr", "<u8"), ("scale", "<f4"), ("reserved1", "<u4")])
+assert _ENTRY_DT.itemsize == ctypes.sizeof(ExpertEntry)
+
+
 def mlg_pack_expert_tables(ids, a_addr, b_addr, scale):
     """Returns host tables (a u64, b u64, scale f32); n_experts = len(a)."""
     n = len(ids)
-    entries = (ExpertEntry * max(n, 1))()
-    for i in range(n):
-        entries[i].expert_id = int(ids[i])
-        entries[i].a_addr = int(a_addr[i])
-        entries[i].b_addr = int(b_addr[i])
-        entries[i].scale = float(scale[i])
+    rec = np.zeros(max(n, 1), _ENTRY_DT)
+    if n:
+        rec["expert_id"][:n] = np.asarray(ids, np.int64).astype(np.uint32)
+        rec["a_addr"][:n] = np.asarray(a_addr).astype(np.uint64)
+        rec["b_addr"][:n] = np.asarray(b_addr).astype(np.uint64)
+        rec["scale"][:n] = np.asarray(scale, np.float32)
+    entries = rec.ctypes.data_as(ctypes.c_void_p)
     n_exp = ctypes.c_uint32(0)
     st = lib().mlg_pack_expert_tables(entries, n, None, None, None, 0, ctypes.byref(n_exp))
     if st != MLG_ERR_BUFFER_TOO_SMALL:

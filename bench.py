@@ -585,7 +585,12 @@ def e2e_measure(prob, steps, device):
     pieces of at most 8192 rows (inside windows), so piece i's rows go up while
     piece i-1 folds and piece i-2's come back, on three streams; the
     GEMM + fold form writes every row of its spans, so its base_out is not
-    uploaded."""
+    uploaded.  Timed twice: with a synchronize after every step, and as a
+    stream of steps where each upload waits only for the previous step's last
+    use of the same device buffer (a piece's rows for its download, the
+    tables / row map / token x for the step's last fold) and one synchronize
+    ends the timed region -- the rate at which a caller feeding batches back
+    to back folds them."""
     import torch
 
     import lora_moe_expert_gb300 as mlg
@@ -603,10 +608,14 @@ def e2e_measure(prob, steps, device):
     h_src = pin(w.src) if w.kind == "grouped" else None
     s = torch.cuda.Stream(device=device)
     h2d = d2h = 0
+    prev_fold = None  # the previous step's last fold (its tables, row map and x are then free)
+    d2h_done = {}  # piece -> the previous step's download of that piece's rows
 
-    def step():
-        nonlocal h2d, d2h
+    def step(sync):
+        nonlocal h2d, d2h, prev_fold
         h2d = d2h = 0
+        if prev_fold is not None:
+            s.wait_event(prev_fold)
         with torch.cuda.stream(s):
             if w.kind == "gather" and w.n_adapters:
                 m = mlg.mlg_build_moe_row_adapter_decode_multi(w.adapter_slots, w.padded_n,
@@ -646,7 +655,11 @@ def e2e_measure(prob, steps, device):
                 h_out.copy_(prob.base.view(torch.int16), non_blocking=True)
                 d2h += h_out.numel() * 2
         if windows is not None:
-            windowed(s)
+            prev_fold = windowed(s)
+        if sync:
+            sync_all()
+
+    def sync_all():
         s.synchronize()
         if windows is not None:
             s_cmp.synchronize()
@@ -672,7 +685,10 @@ def e2e_measure(prob, steps, device):
     def windowed(s_up):
         nonlocal h2d, d2h
         ra = prob.row_adapter
-        for (r0, r1) in windows:
+        done = None
+        for k, (r0, r1) in enumerate(windows):
+            if k in d2h_done:  # the previous step's download of these rows
+                s_up.wait_event(d2h_done[k])
             with torch.cuda.stream(s_up):
                 if xrows:
                     prob.x_rows[r0:r1].view(torch.int16).copy_(h_x[r0:r1], non_blocking=True)
@@ -706,15 +722,24 @@ def e2e_measure(prob, steps, device):
             with torch.cuda.stream(s_d2h):
                 h_out[r0:r1].copy_(prob.base[r0:r1].view(torch.int16), non_blocking=True)
                 d2h += (r1 - r0) * h_out.shape[1] * 2
+                ev = torch.cuda.Event()
+                ev.record(s_d2h)
+                d2h_done[k] = ev
+        return done
 
     for _ in range(3):
-        step()
+        step(True)
     t0 = time.perf_counter()
     for _ in range(steps):
-        step()
+        step(True)
+    dt_sync = (time.perf_counter() - t0) / steps
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step(False)
+    sync_all()
     dt = (time.perf_counter() - t0) / steps
-    return {"s_per_step": dt, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps}
+    return {"s_per_step": dt, "s_per_step_synced": dt_sync, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
 
 
 # ------------------------------------------------------------------ replicas
@@ -844,7 +869,8 @@ def summarize(name, r, peak, steps, cpu=None):
         e = r["e2e"]
         out["e2e"] = {"value": r["rows_set0"] / e["s_per_step"], "unit": "rows/s",
                       "h2d_bytes_per_step": e["h2d_bytes_per_step"],
-                      "d2h_bytes_per_step": e["d2h_bytes_per_step"]}
+                      "d2h_bytes_per_step": e["d2h_bytes_per_step"],
+                      "value_synchronized_steps": r["rows_set0"] / e["s_per_step_synced"]}
     if cpu is not None:
         out["cpu_baseline"] = cpu
     return out
@@ -895,6 +921,8 @@ def main():
                            barrier=True)
     ms_step = max_over_ranks(main_res["ms_total"] / args.steps, device)
     main_res["e2e"]["s_per_step"] = max_over_ranks(main_res["e2e"]["s_per_step"], device)
+    main_res["e2e"]["s_per_step_synced"] = max_over_ranks(main_res["e2e"]["s_per_step_synced"],
+                                                          device)
     peak, peak_kind = measured_peaks()
     per_launch_ms = ms_step / main_res["launches_per_step"]
     achieved = main_res["alg_bytes"] / main_res["launches_per_step"] / (per_launch_ms * 1e-3) / 1e9
@@ -955,7 +983,9 @@ def main():
         "e2e": {"value": job_rows_per_s(main_res["rows_set0"], ws, e2e["s_per_step"] * 1e3),
                 "unit": "rows/s",
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
-                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                "value_synchronized_steps": job_rows_per_s(main_res["rows_set0"], ws,
+                                                           e2e["s_per_step_synced"] * 1e3)},
         "gpu_launches": args.replays * args.steps * main_res["launches_per_step"],
         "clocks": main_res["clocks"],
         "workloads": extras,

@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fold_kernel(const DecodePa
         const int r = (i * 16) / RB, off = (i * 16) % RB;
         cp_async_16(smem_addr(sBw + b_slot<RP>(r) * RB + off), B + i * 16, 16u);
       }
-      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar_w) : "memory");
+      cp_async_arrive_noinc(bar_w);
     }
     return true;
   };

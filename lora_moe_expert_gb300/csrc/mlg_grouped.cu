@@ -15,9 +15,9 @@
 //    list is built on the device from expert_offsets and the tables (no host
 //    copy), and persistent CTAs (one per SM) walk it round-robin (the tiles
 //    of a last, partial round split into pieces of their expand chunks over
-//    the idle CTAs).  The setup
-//    that reads none of the fold's inputs runs before griddepcontrol.wait, so
-//    it overlaps the preceding kernel (programmatic dependent launch);
+//    the idle CTAs).  The setup that reads none of the fold's inputs runs
+//    before griddepcontrol.wait, so it overlaps the preceding kernel
+//    (programmatic dependent launch);
 //  * warp 0 issues the tensor-core work: shrink H = X A_e^T (M=128, N=rank,
 //    K=k_in in 64-wide chunks) into tensor memory, then expand
 //    ACC = [H_hi | H_lo] [B_e | B_e]^T (M=128, N=64/128 columns per chunk) into
@@ -28,7 +28,10 @@
 //    128-byte rows; B_e in rows of 2 * rank bytes, 32- or 64-byte swizzle for
 //    rank 16 / 32, so a B_e stage takes a quarter / half the space); when
 //    a tile's x rows are rows r0.. of x (router, per-row x) they come in as
-//    64 x 64 TMA boxes instead;
+//    64 x 64 TMA boxes instead.  Each producer lane arrives on a stage's full
+//    barrier through cp.async.mbarrier.arrive (landing when its copies have)
+//    and the boxes complete on it by their bytes, so a stage is ready as soon
+//    as its own data is;
 //  * warps 4-11 (two per TMEM lane quarter) scale and split h, then stream
 //    base_out: the pair owns the quarter's 32 rows of the tile, each warp
 //    takes every other 64-column box and runs its own ring of 32x64 TMA
